@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the weight-only quantized GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload w8_decode|w4_g64|w8_large|w4_tiny]
+
+One step is one pass of the hot path over the workload's batch: one wo_gemm
+per (m, N, K) case of the workload, each case with its own weights.  The
+default workload is the A16W8 per-channel decode set (fp16 A with m in
+{1, 4, 16}, uint8 codes, fp16 scale and bias; (N, K) in {(4608,3584),
+(3584,3584), (37888,3584), (3584,18944)}), reported as effective weight GB/s
+(packed code bytes + scale bytes per second).
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize(); each case is replayed from its own CUDA graph
+(one kernel) with CUDA events between cases on the launching stream, so the
+step time and every kernel's duration are device times.  The 12 decode cases
+read 12 distinct weight matrices (about 700 MB per step, over five times the
+L2), so every launch streams its weights from HBM.
+
+Rank 0 prints one JSON line.  `--impl reference` times the CPU oracle (the
+plain C implementation the tests check against) on a bounded sample of the
+same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from weight_only_quantized_fpa_gb300 import inputs  # noqa: E402
+
+METRIC = "weight-only GEMM: weight GB/s (m≤16), TFLOP/s (m≥64), % of roofline"
+
+WORKLOADS = {
+    "w8_decode": dict(config=2, unit="GB/s", dtype="f16",
+                      desc="A16W8 per-channel decode: fp16 A [m,K] ~N(0,1), m in {1,4,16}; "
+                           "uint8 codes w=(q-128)*s, fp16 scale [N] ~U(0.001,0.01), fp16 bias "
+                           "~N(0,0.1); (N,K) in {(4608,3584),(3584,3584),(37888,3584),"
+                           "(3584,18944)}"),
+    "w4_g64": dict(config=4, unit="GB/s", dtype="bf16",
+                   desc="W4A16 group-64 asymmetric, bf16: m in {1,512}; (N,K) in "
+                        "{(2048,2048),(3072,2048),(13312,2048),(131072,2048),(2048,13312)}"),
+    "w8_large": dict(config=3, unit="TFLOP/s", dtype="f16",
+                     desc="A16W8 per-channel large m: m in {256,1024,4096,8192}; (N,K) in "
+                          "{(2048,2048),(4096,4096),(4608,3584)}, fp16"),
+    "w4_tiny": dict(config=1, unit="GB/s", dtype="bf16",
+                    desc="W4A16 tiny: m=1, N=256, K=512, group 64, bf16"),
+}
+
+HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w8_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing leg (for quick local runs)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- workload ---
+
+def workload_cases(name: str):
+    w = WORKLOADS[name]
+    cfg = inputs.GEMM_WORKLOADS[w["config"]]
+    return [inputs.workload_case(w["config"], i) for i in range(len(cfg["shapes"]))]
+
+
+def case_flops(c) -> float:
+    return 2.0 * c.m * c.n * c.k
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, "fallback"
+
+
+def kernel_source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "weight_only_quantized_fpa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(kernel: str, src_hash: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("source_hash") == src_hash:
+            return e
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------- CPU baseline ----
+
+def slice_case(c, n_sub: int):
+    """The first n_sub output channels of a case (a bounded oracle sample)."""
+    import copy
+    s = copy.copy(c)
+    s.n = n_sub
+    s.B = c.B[:n_sub]
+    s.scales = c.scales[:n_sub]
+    s.zeros = None if c.zeros is None else c.zeros[:n_sub]
+    s.bias = None if c.bias is None else c.bias[:n_sub]
+    return s
+
+
+def oracle_pass(cases, frac: float, threads: int):
+    """Run the oracle over every case restricted to a fraction of its output
+    channels (and of its rows for m > 64); returns (seconds, weight bytes,
+    flops)."""
+    import oracle
+    t0 = time.perf_counter()
+    wbytes = 0
+    flops = 0.0
+    for c in cases:
+        n_sub = max(64, int(c.n * frac) // 64 * 64)
+        s = slice_case(c, n_sub)
+        m_sub = c.m if c.m <= 64 else max(1, int(c.m * frac))
+        oracle.gemm(s.A[:m_sub], s.act_dtype, s.B, s.scales, s.zeros, s.bias, m_sub, s.n, s.k,
+                    s.group_size, s.bits, nthreads=threads)
+        wbytes += s.weight_bytes
+        flops += 2.0 * m_sub * s.n * s.k
+    return time.perf_counter() - t0, wbytes, flops
+
+
+def cpu_baseline(cases, unit, budget_s=8.0):
+    threads = os.cpu_count() or 1
+    frac = 1.0 / 64
+    dt, wb, fl = oracle_pass(cases, frac, threads)
+    # grow the sample toward the time budget (bounded: a few passes at most)
+    if dt < budget_s / 4:
+        frac = min(1.0, frac * max(1.0, budget_s / max(dt, 1e-3) / 2))
+        dt, wb, fl = oracle_pass(cases, frac, threads)
+    value = wb / dt / 1e9 if unit == "GB/s" else fl / dt / 1e12
+    return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"every case of the workload on the first {frac:.4f} of its output "
+                      f"channels (rows capped likewise above m=64); {dt:.2f} s wall, "
+                      f"{wb / 1e6:.1f} MB of weights"}
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, x: float) -> float:
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- arms -----
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    cases = workload_cases(args.workload)
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    # size one step so the whole run stays within about two minutes
+    per_step_budget = max(0.2, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    frac = 1.0 / 256
+    dt, _, _ = oracle_pass(cases, frac, threads)
+    frac = max(1.0 / 1024, min(1.0, frac * per_step_budget / max(dt, 1e-3)))
+    for _ in range(args.warmup):
+        oracle_pass(cases, frac, threads)
+    tot_t = tot_b = tot_f = 0.0
+    for _ in range(args.steps):
+        dt, wb, fl = oracle_pass(cases, frac, threads)
+        tot_t += dt
+        tot_b += wb
+        tot_f += fl
+    value = tot_b / tot_t / 1e9 if w["unit"] == "GB/s" else tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": w["unit"],
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["desc"], "cases": len(cases)},
+        "cpu_baseline": {"value": value, "unit": w["unit"], "cores": threads, "kind": "oracle",
+                         "sample": f"each step: every case on the first {frac:.5f} of its "
+                                   "output channels (rows capped likewise above m=64)"},
+        "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import weight_only_quantized_fpa_gb300 as wo
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wo.load_library()
+    w = WORKLOADS[args.workload]
+    cases = workload_cases(args.workload)
+
+    def dt_of(c):
+        return torch.float16 if c.act_dtype == inputs.F16 else torch.bfloat16
+
+    def up16(a, c):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt_of(c))
+
+    dev_cases = []
+    max_ws = 0
+    for c in cases:
+        Brm = torch.from_numpy(c.B).to(dev)
+        Bp = wo.pack(Brm, c.n, c.k, c.bits)
+        del Brm
+        d = dict(c=c, A=up16(c.A, c), B=Bp, s=up16(c.scales, c),
+                 z=None if c.zeros is None else up16(c.zeros, c),
+                 b=None if c.bias is None else up16(c.bias, c),
+                 C=torch.empty((c.m, c.n), dtype=dt_of(c), device=dev))
+        max_ws = max(max_ws, wo.wo_workspace_size(c.m, c.n, c.k, c.group_size, c.bits))
+        dev_cases.append(d)
+    workspace = torch.zeros(max(max_ws, 256), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel()
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(d, A=None, C=None):
+        c = d["c"]
+        wo.wo_gemm(d["A"] if A is None else A, d["B"], d["s"], d["z"], d["b"],
+                   d["C"] if C is None else C, c.m, c.n, c.k, c.group_size, c.bits,
+                   c.act_dtype, workspace, ws_bytes, stream)
+
+    # one CUDA graph per case (one kernel each)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for d in dev_cases:
+            call(d)
+        stream.synchronize()
+        for d in dev_cases:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                call(d)
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    launches_per_step = len(cases)  # one kernel per wo_gemm at these sizes
+    bytes_per_step = sum(c.weight_bytes for c in cases)
+    flops_per_step = sum(case_flops(c) for c in cases)
+    ncase = len(cases)
+
+    def run_steps(nsteps, events=None):
+        with torch.cuda.stream(stream):
+            for s in range(nsteps):
+                for i, g in enumerate(graphs):
+                    if events is not None:
+                        events[s][i].record(stream)
+                    g.replay()
+                if events is not None:
+                    events[s][ncase].record(stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    run_steps(args.warmup)
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(ncase + 1)]
+              for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    start.record(stream)
+    run_steps(args.steps, events)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    per_case_ms = [statistics.fmean(events[s][i].elapsed_time(events[s][i + 1])
+                                    for s in range(args.steps)) for i in range(ncase)]
+    total_ms = max_over_ranks(ws, total_ms)
+    secs = total_ms / 1e3
+
+    if w["unit"] == "GB/s":
+        value = bytes_per_step * args.steps * ws / secs / 1e9
+    else:
+        value = flops_per_step * args.steps * ws / secs / 1e12
+
+    # ---- end to end through the public API with host buffers ----
+    host_A = [torch.empty(d["A"].shape, dtype=d["A"].dtype, pin_memory=True) for d in dev_cases]
+    host_C = [torch.empty(d["C"].shape, dtype=d["C"].dtype, pin_memory=True) for d in dev_cases]
+    for h, d in zip(host_A, dev_cases):
+        h.copy_(d["A"].cpu())
+    h2d = sum(h.numel() * h.element_size() for h in host_A)
+    d2h = sum(h.numel() * h.element_size() for h in host_C)
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for h, d, hc in zip(host_A, dev_cases, host_C):
+                d["A"].copy_(h, non_blocking=True)
+                c = d["c"]
+                wo.gemm(d["A"], d["B"], d["s"], c.n, c.k, c.bits, group_size=c.group_size,
+                        zeros=d["z"], bias=d["b"], out=d["C"], workspace=workspace,
+                        stream=stream)
+                hc.copy_(d["C"], non_blocking=True)
+    for _ in range(min(3, e2e_steps)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    stream.synchronize()
+    e2e_s = max_over_ranks(ws, time.perf_counter() - t0)
+    if w["unit"] == "GB/s":
+        e2e_val = bytes_per_step * e2e_steps * ws / e2e_s / 1e9
+    else:
+        e2e_val = flops_per_step * e2e_steps * ws / e2e_s / 1e12
+
+    if rank != 0:
+        return 0
+
+    hbm_gbs, bf16_tf, peak_src = measured_peaks()
+    kern_ms = sum(per_case_ms)
+    if w["unit"] == "GB/s":
+        achieved = bytes_per_step / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "peak_source": f"hbm_gbs ({peak_src})"}
+        src = ["wo_gemv.cu", "wo_common.cuh"]
+        kname = "gemv_kernel"
+    else:
+        achieved = flops_per_step / (kern_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
+                "frac": achieved / bf16_tf, "peak_source": f"bf16_tflops burst ({peak_src})"}
+        src = ["wo_gemm_tc.cu", "wo_common.cuh"]
+        kname = "gemm_tc_kernel"
+    try:
+        sh = kernel_source_hash(src)
+    except OSError:
+        sh = None
+    tr = traffic_from_profile(kname, sh) if sh else None
+    roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
+    roof["algorithmic_bytes_per_launch"] = bytes_per_step / ncase
+    roof["kernel"] = kname
+
+    line = {
+        "metric": METRIC, "value": value, "unit": w["unit"], "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": w["desc"], "cases": ncase,
+                   "weight_bytes_per_step": bytes_per_step,
+                   "l2": "inputs larger than L2: every case has its own weights "
+                         f"({bytes_per_step / 1e6:.0f} MB per step)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": roof,
+        "cases": [{"m": c.m, "n": c.n, "k": c.k, "us": ms * 1e3,
+                   ("gbs" if w["unit"] == "GB/s" else "tflops"):
+                       (c.weight_bytes / (ms / 1e3) / 1e9) if w["unit"] == "GB/s"
+                       else case_flops(c) / (ms / 1e3) / 1e12}
+                  for c, ms in zip(cases, per_case_ms)],
+        "e2e": {"value": e2e_val, "unit": w["unit"], "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cases, w["unit"])
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, ws, rank)
+    else:
+        rc = run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

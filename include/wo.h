@@ -1,0 +1,163 @@
+/*
+ * wo.h -- C ABI of libwo, the weight-only quantized fpA.intB GEMM for GB300
+ * (sm_103a):
+ *
+ *     C[m, n] = A[m, k] . dequant(B)^T + bias[n]
+ *
+ * A holds fp16 or bf16 activations; B holds integer weight codes of the
+ * output channels (n) along the reduction dimension (k):
+ *   - bits 8 (A16W8): uint8 codes 0..255, w = (q - 128) * scale[n], one scale
+ *     per output channel ("acext User Guide (v1.7)" 1.3.1 Int8 Weight-only;
+ *     "[Misc][Kernel]: Add GPTQAllSpark Quantization": group_size -1, no
+ *     act-order);
+ *   - bits 4 (W4A16): two codes per byte, w = (q - 8) * scale[n][g] +
+ *     zero[n][g] per group g of group_size codes along k (acext 1.3.3 Int4
+ *     Groupwise; vLLM-Omni "cpu_int4.py" module docstring).
+ *
+ * The calls follow the runner convention of acext 1.2.1 (fpAintB GEMM):
+ * the caller owns every buffer, including the workspace whose size the
+ * library reports, and passes an explicit stream; work is stream-ordered and
+ * asynchronous.  No entry point allocates or frees device memory.
+ *
+ * Conventions for every call below:
+ *   - Pointers named for tensors are DEVICE pointers owned by the caller and
+ *     must stay valid until the stream work completes.  A, B, C, out and the
+ *     packed buffers must be 16-byte aligned, the workspace 256-byte aligned,
+ *     scales, zeros and bias 2-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Argument checks happen before any launch; on an error no work is
+ *     enqueued.  WO_ERR_CUDA reports a launch failure (cudaGetLastError).
+ *   - fp16/bf16 tensors are 16-bit IEEE binary16 / bfloat16 values.
+ *   - Every 16-bit output is rounded to nearest even once, from fp32.
+ */
+#ifndef WO_H
+#define WO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define WO_API __attribute__((visibility("default")))
+#else
+#define WO_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WO_OK = 0,
+    WO_ERR_INVALID_ARG = 1, /* a null/misaligned pointer, a bad size or enum */
+    WO_ERR_UNSUPPORTED = 2, /* a valid combination this library does not run */
+    WO_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    WO_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    WO_ERR_TIMEOUT = 5      /* a kernel gave up a bounded wait (see wo_check_workspace) */
+} wo_status;
+
+typedef enum { WO_F16 = 0, WO_BF16 = 1 } wo_dtype;
+
+/* Human-readable name of a status.  Never NULL. */
+WO_API const char* wo_status_string(wo_status s);
+
+/*
+ * Bytes of the packed weight buffer for an [n, k] code matrix: n*k (bits 8)
+ * or n*k/2 (bits 4).  0 for invalid arguments.  Packing keeps the byte count.
+ */
+WO_API size_t wo_packed_bytes(int n, int k, int bits);
+
+/*
+ * Offline repack of row-major codes into the tile-interleaved layout every
+ * GEMM kernel here reads (the analogue of acext's
+ * preprocess_weights_for_mixed_gemm, 1.3.1-1.3.3, run once at load).
+ *   B_rowmajor: bits 8: uint8 [n, k]; bits 4: uint8 [n, k/2] with byte j of a
+ *               row = code 2j | code 2j+1 << 4 (cpu_int4.py docstring).
+ *   B_packed:   wo_packed_bytes(n, k, bits) bytes; must not overlap B_rowmajor.
+ * Layout of B_packed: 512-byte tiles of 16 output channels by 32 (bits 8) or
+ * 64 (bits 4) codes, tiles ordered by channel block then by k; inside a tile
+ * lane L (0..31) owns bytes 16L..16L+15, which hold exactly the codes of the
+ * m16n8k16 A-operand fragments of lane L for the tile's k-steps.
+ * Requires n % 64 == 0, k % 64 == 0, k > 0, n > 0; bits in {4, 8}.
+ * Bit-exact and invertible: wo_unpack(wo_pack(x)) == x.
+ */
+WO_API wo_status wo_pack(const uint8_t* B_rowmajor, uint8_t* B_packed, int n, int k, int bits,
+                  void* stream);
+
+/* Inverse of wo_pack (same arguments, same requirements). */
+WO_API wo_status wo_unpack(const uint8_t* B_packed, uint8_t* B_rowmajor, int n, int k, int bits,
+                    void* stream);
+
+/*
+ * Workspace bytes wo_gemm needs for this problem (acext 1.2.1
+ * getWorkspaceSize).  May be 0.  The workspace must be zero-filled before its
+ * first use (cudaMemset); every call leaves it ready for the next one.  Calls
+ * that share a workspace must be ordered on one stream.
+ */
+WO_API size_t wo_workspace_size(int m, int n, int k, int group_size, int bits);
+
+/*
+ * The weight-only GEMM (acext 1.2.1 gemm(A, B, weight_scales,
+ * weight_zero_points, biases, C, m, n, k, group_size, ...)).
+ *   A:        act_dtype [m, k], row-major.
+ *   B_packed: output of wo_pack for (n, k, bits).
+ *   scales:   act_dtype; per channel ([n]) when group_size is -1 or k,
+ *             otherwise [n, k/group_size].
+ *   zeros:    same shape and dtype as scales, or NULL (= 0).  bits 4 only.
+ *   bias:     act_dtype [n] or NULL.
+ *   C:        act_dtype [m, n], row-major; must not overlap the inputs.
+ *   bits 8: group_size -1 or k (per channel), zeros NULL.
+ *   bits 4: group_size 64 or 128 (a multiple of 64 dividing k), or -1/k.
+ * Requires n % 64 == 0, k % 64 == 0 and k > 0; m == 0 or n == 0 is a no-op.
+ * The kernel is chosen by m: a split-K weight-streaming kernel for small m,
+ * a tcgen05 tensor-core kernel for large m.  Results are deterministic:
+ * identical inputs give bit-identical C.
+ */
+WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales,
+                  const void* zeros, const void* bias, void* C, int m, int n, int k,
+                  int group_size, int bits, wo_dtype act_dtype, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes for wo_moe_ffn with T tokens, the given sizes and top-k.
+ * Same zero-fill rule as wo_workspace_size.
+ */
+WO_API size_t wo_moe_workspace_size(int T, int hidden, int inter, int experts, int topk);
+
+/*
+ * Grouped weight-only MoE FFN (acext 1.2.3 MoE GEMM runner: gating output,
+ * top-k experts per row, fc1 with a gated activation, fc2, routing-weighted
+ * combine):
+ *   ids[t], p[t] = top-k of gating_logits[t] (ties to the lower expert id),
+ *                  p = softmax probabilities over all experts of the chosen
+ *                  ids (renormalised to sum 1 when renormalize != 0);
+ *   for each chosen expert e: [g | u] = A[t] . dequant(fc1_e)^T (2*inter),
+ *                  h = round(silu(g) * u), y = h . dequant(fc2_e)^T;
+ *   out[t] = round(sum_j p[t][j] * y_j).
+ *   A:             act_dtype [T, hidden].
+ *   gating_logits: fp32 [T, experts].
+ *   fc1_packed:    experts consecutive wo_pack outputs of [2*inter, hidden]
+ *                  bits-8 codes; fc1_scales act_dtype [experts, 2*inter].
+ *   fc2_packed:    experts consecutive wo_pack outputs of [hidden, inter];
+ *                  fc2_scales act_dtype [experts, hidden].
+ *   out:           act_dtype [T, hidden].
+ * Requires hidden % 64 == 0, inter % 64 == 0, 1 <= topk <= experts <= 1024.
+ */
+WO_API wo_status wo_moe_ffn(const void* A, const float* gating_logits, const uint8_t* fc1_packed,
+                     const void* fc1_scales, const uint8_t* fc2_packed,
+                     const void* fc2_scales, void* out, int T, int hidden, int inter,
+                     int experts, int topk, int renormalize, wo_dtype act_dtype,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the error word a kernel may
+ * have left in `workspace` (a tensor-core kernel that gave up a bounded wait
+ * writes it instead of hanging).  Returns WO_OK, WO_ERR_TIMEOUT, or
+ * WO_ERR_CUDA when the stream reported an error.
+ */
+WO_API wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WO_H */

@@ -1,0 +1,118 @@
+"""CPU tests of the C ABI: the library builds, loads, exports every symbol
+include/wo.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_only_quantized_fpa_gb300 as wo
+from weight_only_quantized_fpa_gb300 import build as wo_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wo.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wo_build.build()
+    return wo.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"WO_API\s+[\w\s\*]*?\b(wo_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["wo_pack", "wo_unpack", "wo_packed_bytes", "wo_workspace_size", "wo_gemm",
+              "wo_moe_workspace_size", "wo_moe_ffn", "wo_status_string", "wo_check_workspace"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm_103a():
+    # the object files carry the arch in the fatbin; check the build flags instead
+    assert "arch=compute_103a,code=sm_103a" in " ".join(wo_build.ARCH)
+
+
+def test_status_strings(lib):
+    assert wo.wo_status_string(0) == "WO_OK"
+    assert wo.wo_status_string(5) == "WO_ERR_TIMEOUT"
+    assert wo.wo_status_string(99) == "WO_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("n,k,bits,expect", [
+    (256, 512, 4, 256 * 256), (4608, 3584, 8, 4608 * 3584), (64, 64, 8, 4096),
+    (100, 512, 8, 0), (256, 500, 4, 0), (256, 512, 3, 0), (0, 512, 8, 0), (256, 0, 8, 0)])
+def test_packed_bytes(lib, n, k, bits, expect):
+    assert wo.wo_packed_bytes(n, k, bits) == expect
+
+
+def _gemm_status(lib, m=4, n=256, k=512, group=64, bits=4, act=1, A=4096, B=8192, s=64,
+                 z=None, bias=None, C=16384, ws=None, ws_bytes=0):
+    return lib.wo_gemm(A, B, s, z, bias, C, m, n, k, group, bits, act, ws, ws_bytes, None)
+
+
+def test_gemm_rejects_bad_shapes_before_launch(lib):
+    assert _gemm_status(lib, n=100) == 1
+    assert _gemm_status(lib, k=500) == 1
+    assert _gemm_status(lib, k=0) == 1
+    assert _gemm_status(lib, m=-1) == 1
+    assert _gemm_status(lib, bits=3) == 1
+    assert _gemm_status(lib, group=100) == 1   # does not divide k
+    assert _gemm_status(lib, act=2) == 1
+
+
+def test_gemm_unsupported_combinations(lib):
+    assert _gemm_status(lib, bits=8, group=64) == 2       # 8-bit is per channel
+    assert _gemm_status(lib, bits=8, group=-1, z=64) == 2  # 8-bit has no zeros
+    assert _gemm_status(lib, bits=4, group=32) == 2       # groups are multiples of 64
+
+
+def test_gemm_empty_is_noop(lib):
+    assert _gemm_status(lib, m=0, A=None, B=None, s=None, C=None) == 0
+
+
+def test_gemm_rejects_null_and_misaligned(lib):
+    assert _gemm_status(lib, A=None) == 1
+    assert _gemm_status(lib, C=None) == 1
+    assert _gemm_status(lib, A=4096 + 8) == 1
+    assert _gemm_status(lib, s=65) == 1
+
+
+def test_gemm_rejects_small_workspace(lib):
+    m, n, k = 1, 256, 18944
+    need = wo.wo_workspace_size(m, n, k, -1, 8)
+    if need == 0:
+        pytest.skip("this problem needs no workspace")
+    assert _gemm_status(lib, m=m, n=n, k=k, group=-1, bits=8, act=0, ws=None) == 3
+    assert _gemm_status(lib, m=m, n=n, k=k, group=-1, bits=8, act=0, ws=1 << 20,
+                        ws_bytes=need - 1) == 3
+
+
+def test_workspace_size_invalid_is_zero(lib):
+    assert wo.wo_workspace_size(1, 100, 512, -1, 8) == 0
+    assert wo.wo_workspace_size(0, 256, 512, -1, 8) == 0
+
+
+def test_pack_rejects_bad_arguments(lib):
+    # every call below fails validation, so nothing is launched on these
+    # placeholder addresses
+    assert lib.wo_pack(None, 1 << 20, 256, 512, 4, None) == 1
+    assert lib.wo_pack(4096, 1 << 20, 100, 512, 4, None) == 1
+    assert lib.wo_pack(4096 + 4, 1 << 20, 256, 512, 4, None) == 1
+    # overlapping source and destination
+    assert lib.wo_pack(1 << 20, (1 << 20) + 4096, 256, 512, 8, None) == 1
+
+
+def test_library_load_fails_loudly_when_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(wo_build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(wo, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        wo.load_library()

@@ -1,0 +1,171 @@
+"""GPU parity of wo_gemm against the CPU oracle, on the workloads' seeded
+inputs: element by element at sizes the oracle finishes in seconds, and on
+sampled rows at the workloads' full sizes, in the launch configuration the
+bench times.  Tolerance (fp outputs): rel-L2 <= 2e-3 and
+max |C - C_ref| <= 1e-2 * max |C_ref| against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import (DeviceCase, assert_within_tolerance, from_device_bits, sample_rows,
+                     to_device_bits)
+from weight_only_quantized_fpa_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def wo():
+    import weight_only_quantized_fpa_gb300 as w
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w.load_library()
+    return w
+
+
+def _check_full(dc: DeviceCase, what: str):
+    C = dc.run()
+    torch.cuda.synchronize()
+    ref = dc.oracle_rows()
+    return assert_within_tolerance(from_device_bits(C), dc.c.act_dtype, ref, what)
+
+
+def _check_sampled(dc: DeviceCase, what: str, count=12):
+    C = dc.run()
+    torch.cuda.synchronize()
+    rows = sample_rows(dc.c.m, count)
+    ref = dc.oracle_rows(rows)
+    return assert_within_tolerance(from_device_bits(C)[rows], dc.c.act_dtype, ref, what)
+
+
+# ------------------------------------------------------ W4 tiny (config 1) --
+
+def test_w4_tiny(wo):
+    dc = DeviceCase(inputs.workload_case(1, 0))
+    _check_full(dc, "w4 tiny")
+
+
+# ------------------------------------------------------- small odd shapes --
+
+SMALL = [
+    # m, n, k, bits, group, act, zeros, bias
+    (1, 64, 64, 8, -1, inputs.F16, False, True),
+    (3, 192, 320, 8, -1, inputs.F16, False, True),
+    (17, 256, 512, 8, -1, inputs.BF16, False, False),
+    (5, 320, 1024, 4, 64, inputs.BF16, True, True),
+    (16, 128, 640, 4, 64, inputs.F16, True, False),
+    (33, 256, 384, 4, 128, inputs.BF16, True, False),
+    (2, 128, 512, 4, -1, inputs.BF16, True, True),
+    (64, 192, 256, 8, -1, inputs.F16, False, True),
+    (65, 128, 256, 4, 64, inputs.BF16, True, True),
+    (100, 256, 512, 8, -1, inputs.BF16, False, True),
+    (130, 320, 448, 4, 64, inputs.F16, True, False),
+]
+
+
+@pytest.mark.parametrize("m,n,k,bits,group,act,zeros,bias", SMALL)
+def test_small_shapes(wo, m, n, k, bits, group, act, zeros, bias):
+    c = inputs.make_gemm_case(8, m + n + k, m, n, k, bits=bits, group_size=group, act_dtype=act,
+                              scale_lo=0.005 if bits == 4 else 0.001,
+                              scale_hi=0.02 if bits == 4 else 0.01, with_zeros=zeros,
+                              with_bias=bias)
+    _check_full(DeviceCase(c), f"m{m} n{n} k{k} w{bits} g{group}")
+
+
+def test_split_k_long_reduction(wo):
+    # few channels and a long k force many k-slices through the workspace
+    c = inputs.make_gemm_case(8, 77, 4, 64, 18944, bits=8, group_size=-1, act_dtype=inputs.F16,
+                              scale_lo=0.001, scale_hi=0.01, with_zeros=False, with_bias=True)
+    assert wo.wo_workspace_size(4, 64, 18944, -1, 8) > 0
+    _check_full(DeviceCase(c), "split-k")
+
+
+# ------------------------------------------------ A16W8 decode (config 2) --
+
+@pytest.mark.parametrize("case", range(len(inputs.W8_DECODE["shapes"])))
+def test_w8_decode_full(wo, case):
+    dc = DeviceCase(inputs.workload_case(2, case))
+    _check_full(dc, dc.c.name)
+
+
+# ---------------------------------------------- A16W8 large m (config 3) --
+
+@pytest.mark.parametrize("case", range(len(inputs.W8_LARGE["shapes"])))
+def test_w8_large_m_sampled(wo, case):
+    dc = DeviceCase(inputs.workload_case(3, case))
+    _check_sampled(dc, dc.c.name)
+
+
+# ------------------------------------------------- W4 group-64 (config 4) --
+
+@pytest.mark.parametrize("case", range(len(inputs.W4_G64["shapes"])))
+def test_w4_g64(wo, case):
+    dc = DeviceCase(inputs.workload_case(4, case))
+    if dc.c.m == 1:
+        _check_full(dc, dc.c.name)
+    else:
+        _check_sampled(dc, dc.c.name, count=8)
+
+
+# ---------------------------------------------------------- properties -----
+
+def test_deterministic_bit_identical(wo):
+    dc = DeviceCase(inputs.workload_case(2, 3))   # long k: split-K reduction
+    C1 = dc.run().clone()
+    C2 = dc.run().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+def test_integer_exact_case(wo):
+    # integer A in -2..2, codes 126..130, scale 1: exact in fp16 everywhere
+    m, n, k = 5, 128, 256
+    rng = np.random.default_rng(12)
+    Ai = rng.integers(-2, 3, size=(m, k))
+    qi = rng.integers(126, 131, size=(n, k))
+    A = to_device_bits(Ai.astype(np.float16).view(np.uint16), inputs.F16)
+    B = wo.pack(torch.from_numpy(qi.astype(np.uint8)).cuda(), n, k, 8)
+    s = to_device_bits(np.full(n, np.float16(1.0).view(np.uint16)), inputs.F16)
+    C = wo.gemm(A, B, s, n, k, 8)
+    torch.cuda.synchronize()
+    ref = (Ai @ (qi - 128).T).astype(np.float16).view(np.uint16)
+    assert np.array_equal(from_device_bits(C), ref)
+
+
+def test_empty_m_is_noop(wo):
+    c = inputs.workload_case(1, 0)
+    dc = DeviceCase(c)
+    A0 = torch.empty((0, c.k), dtype=dc.A.dtype, device="cuda")
+    C = dc.run(A=A0)
+    assert C.shape == (0, c.n)
+
+
+def test_output_overwrites_poisoned_buffer(wo):
+    dc = DeviceCase(inputs.workload_case(1, 0))
+    out = torch.full((1, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dc.run(out=out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+
+
+def test_workspace_shared_across_shapes(wo):
+    # a long-k call (many k-slices, large partial-sum region) followed by a
+    # wide call (many output tiles) on the same workspace: the arrival
+    # counters live in a fixed area no partials ever overwrite
+    a = DeviceCase(inputs.make_gemm_case(8, 90, 16, 64, 18944, bits=8, group_size=-1,
+                                         act_dtype=inputs.F16, scale_lo=0.001, scale_hi=0.01,
+                                         with_zeros=False, with_bias=True))
+    b = DeviceCase(inputs.make_gemm_case(8, 91, 1, 13312, 2048, bits=4, group_size=64,
+                                         act_dtype=inputs.BF16, scale_lo=0.005, scale_hi=0.02,
+                                         with_zeros=True, with_bias=False))
+    need = max(wo.wo_workspace_size(16, 64, 18944, -1, 8),
+               wo.wo_workspace_size(1, 13312, 2048, 64, 4))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        Ca = a.run(workspace=ws)
+        Cb = b.run(workspace=ws)
+        torch.cuda.synchronize()
+        assert_within_tolerance(from_device_bits(Ca), inputs.F16, a.oracle_rows(), "long k")
+        assert_within_tolerance(from_device_bits(Cb), inputs.BF16, b.oracle_rows(), "wide n")

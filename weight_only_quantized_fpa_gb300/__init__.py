@@ -1,0 +1,248 @@
+"""Python binding of libwo, the GB300 weight-only quantized fpA.intB GEMM.
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``csrc/`` behind the C ABI declared in ``include/wo.h``.  PyTorch provides
+device memory and streams.  There is no CPU fallback: if ``libwo.so`` has
+not been built, every call raises.
+
+The functions named ``wo_*`` mirror the C entry points one for one and take
+torch tensors (device memory) where the C call takes device pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "WO_F16", "WO_BF16", "WoError", "load_library", "library_path",
+    "wo_status_string", "wo_packed_bytes", "wo_pack", "wo_unpack", "wo_workspace_size",
+    "wo_gemm", "wo_moe_workspace_size", "wo_moe_ffn", "wo_check_workspace",
+    "pack", "unpack", "gemm", "moe_ffn", "Workspace",
+]
+
+WO_F16 = 0
+WO_BF16 = 1
+
+_STATUS = {0: "WO_OK", 1: "WO_ERR_INVALID_ARG", 2: "WO_ERR_UNSUPPORTED",
+           3: "WO_ERR_WORKSPACE", 4: "WO_ERR_CUDA", 5: "WO_ERR_TIMEOUT"}
+
+
+class WoError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_STATUS.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libwo.so; raise if it is not built (no fallback path exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"libwo.so is not built ({path}); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.wo_status_string.argtypes = [I]
+        lib.wo_status_string.restype = ctypes.c_char_p
+        lib.wo_packed_bytes.argtypes = [I, I, I]
+        lib.wo_packed_bytes.restype = S
+        lib.wo_pack.argtypes = [P, P, I, I, I, P]
+        lib.wo_pack.restype = I
+        lib.wo_unpack.argtypes = [P, P, I, I, I, P]
+        lib.wo_unpack.restype = I
+        lib.wo_workspace_size.argtypes = [I, I, I, I, I]
+        lib.wo_workspace_size.restype = S
+        lib.wo_gemm.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+        lib.wo_gemm.restype = I
+        lib.wo_moe_workspace_size.argtypes = [I, I, I, I, I]
+        lib.wo_moe_workspace_size.restype = S
+        lib.wo_moe_ffn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+        lib.wo_moe_ffn.restype = I
+        lib.wo_check_workspace.argtypes = [P, S, P]
+        lib.wo_check_workspace.restype = I
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- helpers --
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _raise(status: int, what: str):
+    if status != 0:
+        raise WoError(status, what)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return WO_F16
+    if t.dtype == torch.bfloat16:
+        return WO_BF16
+    raise TypeError(f"activations must be float16 or bfloat16, got {t.dtype}")
+
+
+# ------------------------------------------------------ raw C-ABI mirrors --
+
+def wo_status_string(status: int) -> str:
+    return load_library().wo_status_string(int(status)).decode()
+
+
+def wo_packed_bytes(n: int, k: int, bits: int) -> int:
+    return int(load_library().wo_packed_bytes(n, k, bits))
+
+
+def wo_pack(B_rowmajor, B_packed, n: int, k: int, bits: int, stream=None) -> None:
+    _raise(load_library().wo_pack(_ptr(B_rowmajor), _ptr(B_packed), n, k, bits,
+                                  _stream_ptr(stream)), "wo_pack")
+
+
+def wo_unpack(B_packed, B_rowmajor, n: int, k: int, bits: int, stream=None) -> None:
+    _raise(load_library().wo_unpack(_ptr(B_packed), _ptr(B_rowmajor), n, k, bits,
+                                    _stream_ptr(stream)), "wo_unpack")
+
+
+def wo_workspace_size(m: int, n: int, k: int, group_size: int, bits: int) -> int:
+    return int(load_library().wo_workspace_size(m, n, k, group_size, bits))
+
+
+def wo_gemm(A, B_packed, scales, zeros, bias, C, m: int, n: int, k: int, group_size: int,
+            bits: int, act_dtype: int, workspace, workspace_bytes: int, stream=None) -> None:
+    _raise(load_library().wo_gemm(_ptr(A), _ptr(B_packed), _ptr(scales), _ptr(zeros),
+                                  _ptr(bias), _ptr(C), m, n, k, group_size, bits, act_dtype,
+                                  _ptr(workspace), workspace_bytes, _stream_ptr(stream)),
+           "wo_gemm")
+
+
+def wo_moe_workspace_size(T: int, hidden: int, inter: int, experts: int, topk: int) -> int:
+    return int(load_library().wo_moe_workspace_size(T, hidden, inter, experts, topk))
+
+
+def wo_moe_ffn(A, gating_logits, fc1_packed, fc1_scales, fc2_packed, fc2_scales, out, T: int,
+               hidden: int, inter: int, experts: int, topk: int, renormalize: int,
+               act_dtype: int, workspace, workspace_bytes: int, stream=None) -> None:
+    _raise(load_library().wo_moe_ffn(_ptr(A), _ptr(gating_logits), _ptr(fc1_packed),
+                                     _ptr(fc1_scales), _ptr(fc2_packed), _ptr(fc2_scales),
+                                     _ptr(out), T, hidden, inter, experts, topk,
+                                     int(renormalize), act_dtype, _ptr(workspace),
+                                     workspace_bytes, _stream_ptr(stream)), "wo_moe_ffn")
+
+
+def wo_check_workspace(workspace, workspace_bytes: int, stream=None) -> int:
+    """Synchronise and return the status the kernels left in the workspace."""
+    return int(load_library().wo_check_workspace(_ptr(workspace), workspace_bytes,
+                                                 _stream_ptr(stream)))
+
+
+# ------------------------------------------------- torch-level conveniences --
+
+class Workspace:
+    """A zero-filled device workspace that grows on demand (allocated by torch)."""
+
+    def __init__(self, device=None):
+        import torch
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int):
+        import torch
+        if nbytes <= 0:
+            return None, 0
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf, self.buf.numel()
+
+
+_default_ws: dict = {}
+
+
+def _workspace_for(device, nbytes):
+    key = str(device)
+    ws = _default_ws.get(key)
+    if ws is None:
+        ws = _default_ws[key] = Workspace(device)
+    return ws.get(nbytes)
+
+
+def pack(B_rowmajor, n: int, k: int, bits: int, stream=None):
+    """Row-major codes (uint8 [n, k] or [n, k/2]) -> packed uint8 buffer."""
+    import torch
+    out = torch.empty(wo_packed_bytes(n, k, bits), dtype=torch.uint8, device=B_rowmajor.device)
+    wo_pack(B_rowmajor, out, n, k, bits, stream)
+    return out
+
+
+def unpack(B_packed, n: int, k: int, bits: int, stream=None):
+    import torch
+    shape = (n, k) if bits == 8 else (n, k // 2)
+    out = torch.empty(shape, dtype=torch.uint8, device=B_packed.device)
+    wo_unpack(B_packed, out, n, k, bits, stream)
+    return out
+
+
+def gemm(A, B_packed, scales, n: int, k: int, bits: int, group_size: int = -1, zeros=None,
+         bias=None, out=None, workspace=None, stream=None):
+    """C = A . dequant(B)^T + bias through wo_gemm; returns C [m, n]."""
+    import torch
+    m = A.shape[0]
+    act = _dtype_code(A)
+    if out is None:
+        out = torch.empty((m, n), dtype=A.dtype, device=A.device)
+    need = wo_workspace_size(m, n, k, group_size, bits)
+    if workspace is None:
+        ws, ws_bytes = _workspace_for(A.device, need)
+    else:
+        ws, ws_bytes = workspace, workspace.numel()
+    wo_gemm(A, B_packed, scales, zeros, bias, out, m, n, k, group_size, bits, act, ws, ws_bytes,
+            stream)
+    return out
+
+
+def moe_ffn(A, gating_logits, fc1_packed, fc1_scales, fc2_packed, fc2_scales, hidden: int,
+            inter: int, experts: int, topk: int, renormalize: bool = False, out=None,
+            workspace=None, stream=None):
+    import torch
+    T = A.shape[0]
+    act = _dtype_code(A)
+    if out is None:
+        out = torch.empty((T, hidden), dtype=A.dtype, device=A.device)
+    need = wo_moe_workspace_size(T, hidden, inter, experts, topk)
+    if workspace is None:
+        ws, ws_bytes = _workspace_for(A.device, need)
+    else:
+        ws, ws_bytes = workspace, workspace.numel()
+    wo_moe_ffn(A, gating_logits, fc1_packed, fc1_scales, fc2_packed, fc2_scales, out, T, hidden,
+               inter, experts, topk, int(renormalize), act, ws, ws_bytes, stream)
+    return out

@@ -1,0 +1,186 @@
+// wo_api.cu -- the extern "C" entry points of libwo: argument checks, kernel
+// choice and launch.  Every check runs before any CUDA call, so invalid
+// arguments return a status with nothing enqueued.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "wo_internal.h"
+
+namespace wo {
+
+int num_sms()
+{
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 152;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            v <= 0) {
+            cudaGetLastError();
+            v = 152;
+        }
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Normalised group size: k for per-channel (-1 or k), else the value given.
+int norm_group(int group_size, int k) { return (group_size == -1 || group_size == k) ? k : group_size; }
+
+wo_status check_gemm_shape(int m, int n, int k, int group_size, int bits)
+{
+    if (m < 0 || n < 0 || k <= 0)
+        return WO_ERR_INVALID_ARG;
+    if ((long long)n > (long long)kWsCounters * 128)
+        return WO_ERR_UNSUPPORTED;  // more output tiles than arrival counters
+    if (bits != 4 && bits != 8)
+        return WO_ERR_INVALID_ARG;
+    if (n % 64 != 0 || k % 64 != 0)
+        return WO_ERR_INVALID_ARG;
+    const int g = norm_group(group_size, k);
+    if (g <= 0 || k % g != 0)
+        return WO_ERR_INVALID_ARG;
+    if (bits == 8 && g != k)
+        return WO_ERR_UNSUPPORTED;  // 8-bit weights are per channel
+    if (bits == 4 && g != k && g % 64 != 0)
+        return WO_ERR_UNSUPPORTED;
+    return WO_OK;
+}
+
+wo_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WO_OK : WO_ERR_CUDA; }
+
+}  // namespace
+}  // namespace wo
+
+using namespace wo;
+
+extern "C" {
+
+const char* wo_status_string(wo_status s)
+{
+    switch (s) {
+    case WO_OK: return "WO_OK";
+    case WO_ERR_INVALID_ARG: return "WO_ERR_INVALID_ARG";
+    case WO_ERR_UNSUPPORTED: return "WO_ERR_UNSUPPORTED";
+    case WO_ERR_WORKSPACE: return "WO_ERR_WORKSPACE";
+    case WO_ERR_CUDA: return "WO_ERR_CUDA";
+    case WO_ERR_TIMEOUT: return "WO_ERR_TIMEOUT";
+    }
+    return "WO_ERR_UNKNOWN";
+}
+
+size_t wo_packed_bytes(int n, int k, int bits)
+{
+    if (n <= 0 || k <= 0 || n % 64 != 0 || k % 64 != 0 || (bits != 4 && bits != 8))
+        return 0;
+    return bits == 8 ? (size_t)n * (size_t)k : (size_t)n * (size_t)k / 2;
+}
+
+static wo_status pack_common(const uint8_t* src, uint8_t* dst, int n, int k, int bits,
+                             bool unpack, void* stream)
+{
+    const size_t bytes = wo_packed_bytes(n, k, bits);
+    if (bytes == 0 || !src || !dst || !aligned(src, 16) || !aligned(dst, 16))
+        return WO_ERR_INVALID_ARG;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+    if (s0 < d0 + bytes && d0 < s0 + bytes)
+        return WO_ERR_INVALID_ARG;  // overlapping buffers
+    return cuda_status(launch_pack(src, dst, n, k, bits, unpack, static_cast<cudaStream_t>(stream)));
+}
+
+wo_status wo_pack(const uint8_t* B_rowmajor, uint8_t* B_packed, int n, int k, int bits,
+                  void* stream)
+{
+    return pack_common(B_rowmajor, B_packed, n, k, bits, false, stream);
+}
+
+wo_status wo_unpack(const uint8_t* B_packed, uint8_t* B_rowmajor, int n, int k, int bits,
+                    void* stream)
+{
+    return pack_common(B_packed, B_rowmajor, n, k, bits, true, stream);
+}
+
+size_t wo_workspace_size(int m, int n, int k, int group_size, int bits)
+{
+    if (check_gemm_shape(m, n, k, group_size, bits) != WO_OK || m == 0 || n == 0)
+        return 0;
+    if (m >= kTcMinM) {
+        // bf16 activations with 4-bit weights need an fp16 copy of A; size for
+        // the larger of the two activation dtypes' needs
+        return plan_tc(m, n, k, bits, WO_BF16).ws_bytes;
+    }
+    return plan_gemv(m, n, k, bits).ws_bytes;
+}
+
+wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, const void* zeros,
+                  const void* bias, void* C, int m, int n, int k, int group_size, int bits,
+                  wo_dtype act_dtype, void* workspace, size_t workspace_bytes, void* stream)
+{
+    wo_status st = check_gemm_shape(m, n, k, group_size, bits);
+    if (st != WO_OK)
+        return st;
+    if (act_dtype != WO_F16 && act_dtype != WO_BF16)
+        return WO_ERR_INVALID_ARG;
+    if (bits == 8 && zeros)
+        return WO_ERR_UNSUPPORTED;  // 8-bit weights are scale-only
+    if (m == 0 || n == 0)
+        return WO_OK;
+    if (!A || !B_packed || !scales || !C)
+        return WO_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B_packed, 16) || !aligned(C, 16) || !aligned(scales, 2) ||
+        (zeros && !aligned(zeros, 2)) || (bias && !aligned(bias, 2)))
+        return WO_ERR_INVALID_ARG;
+    const size_t need = wo_workspace_size(m, n, k, group_size, bits);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+        return WO_ERR_WORKSPACE;
+
+    GemmArgs a{};
+    a.A = A;
+    a.B = B_packed;
+    a.scales = scales;
+    a.zeros = zeros;
+    a.bias = bias;
+    a.C = C;
+    a.m = m;
+    a.n = n;
+    a.k = k;
+    a.group = norm_group(group_size, k);
+    a.bits = bits;
+    a.act = act_dtype;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (m >= kTcMinM)
+        return cuda_status(launch_tc(a, plan_tc(m, n, k, bits, act_dtype), s));
+    return cuda_status(launch_gemv(a, plan_gemv(m, n, k, bits), s));
+}
+
+wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, void* stream)
+{
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return WO_ERR_CUDA;
+    if (!workspace || workspace_bytes < kWsHeader)
+        return WO_OK;
+    unsigned flag = 0;
+    if (cudaMemcpy(&flag, workspace, sizeof flag, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return WO_ERR_CUDA;
+    if (flag == 0)
+        return WO_OK;
+    if (cudaMemset(workspace, 0, sizeof flag) != cudaSuccess)
+        return WO_ERR_CUDA;
+    return WO_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,150 @@
+// wo_pack.cu -- offline repack of row-major weight codes into the tile layout
+// of wo_common.cuh, and its inverse.  This is the load-time weight
+// preprocessing step of "acext User Guide (v1.7)" 1.3.1-1.3.3
+// (preprocess_weights_for_mixed_gemm), with a layout of our own: each lane's
+// 16 bytes hold its mma fragments, so the GEMM kernels need no shuffles.
+//
+// Row-major input (vLLM-Omni "cpu_int4.py" module docstring):
+//   8-bit: uint8 [n, k];  4-bit: uint8 [n, k/2], byte j = code 2j | code 2j+1 << 4.
+//
+// One thread builds (or scatters) one lane chunk of 16 bytes.  Every output
+// byte is written by exactly one thread, in both directions: in the 4-bit
+// inverse the two nibbles of a row-major byte (k even and k + 1) come from
+// the same lane word (registers R and R + 4 of the layout), so no two threads
+// share a destination byte.
+#include "wo_common.cuh"
+#include "wo_internal.h"
+
+namespace wo {
+namespace {
+
+// Row and k (within the tile) of byte b of lane (g, t), 8-bit layout.
+__device__ __forceinline__ void u8_coord(int b, int g, int t, int& row, int& kk)
+{
+    const int s = b >> 3;        // k-step
+    const int w = (b >> 2) & 1;  // word within the k-step
+    const int j = b & 3;         // byte within the word
+    row = g + 8 * (j >> 1);
+    kk = 16 * s + 2 * t + 8 * w + (j & 1);
+}
+
+// Row and k (within the tile) of nibble p of word s, lane (g, t), 4-bit layout.
+__device__ __forceinline__ void u4_coord(int s, int p, int g, int t, int& row, int& kk)
+{
+    const int R = p & 3, h = p >> 2;
+    row = g + 8 * (R & 1);
+    kk = 16 * s + 2 * t + 8 * (R >> 1) + h;
+}
+
+template <int BITS>
+__global__ void pack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n,
+                            int k, long long chunks)
+{
+    constexpr int KT = Geom<BITS>::KT;
+    const int ktiles = k / KT;
+    for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < chunks;
+         c += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(c & 31);
+        const long long tile = c >> 5;
+        const int nb = (int)(tile / ktiles);
+        const int kt = (int)(tile % ktiles);
+        const int g = lane >> 2, t = lane & 3;
+        uint32_t words[4];
+        if constexpr (BITS == 8) {
+            for (int wi = 0; wi < 4; ++wi) {
+                uint32_t w = 0;
+                for (int j = 0; j < 4; ++j) {
+                    int row, kk;
+                    u8_coord(4 * wi + j, g, t, row, kk);
+                    const uint32_t v = src[(size_t)(nb * 16 + row) * k + kt * KT + kk];
+                    w |= v << (8 * j);
+                }
+                words[wi] = w;
+            }
+        } else {
+            const int kb = k / 2;
+            for (int s = 0; s < 4; ++s) {
+                uint32_t w = 0;
+                for (int p = 0; p < 8; ++p) {
+                    int row, kk;
+                    u4_coord(s, p, g, t, row, kk);
+                    const int kg = kt * KT + kk;
+                    const uint8_t byte = src[(size_t)(nb * 16 + row) * kb + kg / 2];
+                    const uint32_t q = (kg & 1) ? (byte >> 4) : (byte & 0x0F);
+                    w |= q << (4 * p);
+                }
+                words[s] = w;
+            }
+        }
+        uint4 out = make_uint4(words[0], words[1], words[2], words[3]);
+        *reinterpret_cast<uint4*>(dst + c * 16) = out;
+    }
+}
+
+template <int BITS>
+__global__ void unpack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n,
+                              int k, long long chunks)
+{
+    constexpr int KT = Geom<BITS>::KT;
+    const int ktiles = k / KT;
+    for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < chunks;
+         c += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(c & 31);
+        const long long tile = c >> 5;
+        const int nb = (int)(tile / ktiles);
+        const int kt = (int)(tile % ktiles);
+        const int g = lane >> 2, t = lane & 3;
+        const uint4 in = *reinterpret_cast<const uint4*>(src + c * 16);
+        const uint32_t words[4] = {in.x, in.y, in.z, in.w};
+        if constexpr (BITS == 8) {
+            for (int b = 0; b < 16; ++b) {
+                int row, kk;
+                u8_coord(b, g, t, row, kk);
+                dst[(size_t)(nb * 16 + row) * k + kt * KT + kk] =
+                    (uint8_t)(words[b >> 2] >> (8 * (b & 3)));
+            }
+        } else {
+            const int kb = k / 2;
+            for (int s = 0; s < 4; ++s) {
+                for (int p = 0; p < 4; ++p) {  // p and p + 4: the even and odd k of one byte
+                    int row, kk;
+                    u4_coord(s, p, g, t, row, kk);
+                    const uint32_t lo = (words[s] >> (4 * p)) & 0xF;
+                    const uint32_t hi = (words[s] >> (4 * (p + 4))) & 0xF;
+                    dst[(size_t)(nb * 16 + row) * kb + (kt * KT + kk) / 2] =
+                        (uint8_t)(lo | (hi << 4));
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,
+                        cudaStream_t s)
+{
+    const long long bytes = bits == 8 ? (long long)n * k : (long long)n * k / 2;
+    const long long chunks = bytes / 16;
+    const int threads = 256;
+    long long blocks = (chunks + threads - 1) / threads;
+    const long long cap = (long long)num_sms() * 16;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    if (bits == 8) {
+        if (unpack)
+            unpack_kernel<8><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
+        else
+            pack_kernel<8><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
+    } else {
+        if (unpack)
+            unpack_kernel<4><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
+        else
+            pack_kernel<4><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace wo

@@ -75,11 +75,17 @@ def test_small_shapes(wo, m, n, k, bits, group, act, zeros, bias):
 
 
 def test_split_k_long_reduction(wo):
-    # few channels and a long k force many k-slices through the workspace
+    # few channels and a long k: the k range is split across a cluster of CTAs
     c = inputs.make_gemm_case(8, 77, 4, 64, 18944, bits=8, group_size=-1, act_dtype=inputs.F16,
                               scale_lo=0.001, scale_hi=0.01, with_zeros=False, with_bias=True)
-    assert wo.wo_workspace_size(4, 64, 18944, -1, 8) > 0
     _check_full(DeviceCase(c), "split-k")
+
+
+def test_split_k_long_reduction_w4(wo):
+    c = inputs.make_gemm_case(8, 78, 3, 128, 13312, bits=4, group_size=64,
+                              act_dtype=inputs.BF16, scale_lo=0.005, scale_hi=0.02,
+                              with_zeros=True, with_bias=True)
+    _check_full(DeviceCase(c), "split-k w4")
 
 
 # ------------------------------------------------ A16W8 decode (config 2) --
@@ -111,8 +117,9 @@ def test_w4_g64(wo, case):
 
 # ---------------------------------------------------------- properties -----
 
-def test_deterministic_bit_identical(wo):
-    dc = DeviceCase(inputs.workload_case(2, 3))   # long k: split-K reduction
+@pytest.mark.parametrize("config,case", [(2, 3), (2, 11), (3, 1), (4, 6)])
+def test_deterministic_bit_identical(wo, config, case):
+    dc = DeviceCase(inputs.workload_case(config, case))
     C1 = dc.run().clone()
     C2 = dc.run().clone()
     torch.cuda.synchronize()
@@ -151,21 +158,29 @@ def test_output_overwrites_poisoned_buffer(wo):
 
 
 def test_workspace_shared_across_shapes(wo):
-    # a long-k call (many k-slices, large partial-sum region) followed by a
-    # wide call (many output tiles) on the same workspace: the arrival
-    # counters live in a fixed area no partials ever overwrite
-    a = DeviceCase(inputs.make_gemm_case(8, 90, 16, 64, 18944, bits=8, group_size=-1,
+    # calls of different kernels and shapes sharing one workspace, twice over:
+    # a tensor-core call with a converted-activation scratch region, a
+    # cluster-split decode call and a second tensor-core call of another size
+    a = DeviceCase(inputs.make_gemm_case(8, 90, 200, 256, 1024, bits=4, group_size=64,
+                                         act_dtype=inputs.BF16, scale_lo=0.005, scale_hi=0.02,
+                                         with_zeros=True, with_bias=True))
+    b = DeviceCase(inputs.make_gemm_case(8, 91, 16, 64, 18944, bits=8, group_size=-1,
                                          act_dtype=inputs.F16, scale_lo=0.001, scale_hi=0.01,
                                          with_zeros=False, with_bias=True))
-    b = DeviceCase(inputs.make_gemm_case(8, 91, 1, 13312, 2048, bits=4, group_size=64,
-                                         act_dtype=inputs.BF16, scale_lo=0.005, scale_hi=0.02,
-                                         with_zeros=True, with_bias=False))
-    need = max(wo.wo_workspace_size(16, 64, 18944, -1, 8),
-               wo.wo_workspace_size(1, 13312, 2048, 64, 4))
+    c = DeviceCase(inputs.make_gemm_case(8, 92, 96, 512, 512, bits=8, group_size=-1,
+                                         act_dtype=inputs.BF16, scale_lo=0.001, scale_hi=0.01,
+                                         with_zeros=False, with_bias=False))
+    need = max(wo.wo_workspace_size(200, 256, 1024, 64, 4),
+               wo.wo_workspace_size(16, 64, 18944, -1, 8),
+               wo.wo_workspace_size(96, 512, 512, -1, 8))
+    assert need > 0
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     for _ in range(2):
         Ca = a.run(workspace=ws)
         Cb = b.run(workspace=ws)
+        Cc = c.run(workspace=ws)
         torch.cuda.synchronize()
-        assert_within_tolerance(from_device_bits(Ca), inputs.F16, a.oracle_rows(), "long k")
-        assert_within_tolerance(from_device_bits(Cb), inputs.BF16, b.oracle_rows(), "wide n")
+        assert_within_tolerance(from_device_bits(Ca), inputs.BF16, a.oracle_rows(), "tc w4")
+        assert_within_tolerance(from_device_bits(Cb), inputs.F16, b.oracle_rows(), "decode")
+        assert_within_tolerance(from_device_bits(Cc), inputs.BF16, c.oracle_rows(), "tc w8")
+    assert wo.wo_check_workspace(ws, ws.numel()) == 0

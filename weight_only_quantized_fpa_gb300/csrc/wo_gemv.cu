@@ -24,20 +24,27 @@
 //     ever see exact integers;
 //   - 8-bit per-channel weights (acext 1.3.1) accumulate sum a (q - 128) and
 //     apply scale[n] and bias[n] once at the end;
-//   - split-K: CTAs along grid.y take slices of k; each writes its fp32
-//     partials to the workspace, and the last CTA to arrive (an atomic
-//     counter, no waiting) sums the slices in fixed order, applies the
-//     epilogue and resets the counter.  The result does not depend on the
-//     arrival order.
+//   - split-K without a workspace: the 8 warps of a CTA share the same 32
+//     channels and stream consecutive slices of the CTA's k range (each
+//     keeping kDepth tiles in flight), then reduce through shared memory in
+//     fixed warp order; when k is long relative to n, a thread-block cluster
+//     of up to 8 CTAs along k splits it further and the leader CTA sums the
+//     members' results through distributed shared memory, in rank order.
+//     The result does not depend on timing: it is bit-for-bit repeatable.
+#include <cooperative_groups.h>
+
 #include "wo_common.cuh"
 #include "wo_internal.h"
 
 namespace wo {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kRpw = 2;                      // 16-row channel blocks per warp
-constexpr int kCtaCols = kWarps * kRpw * 16; // output channels per CTA
+namespace cg = cooperative_groups;
+
+constexpr int kWarps = 8;
+constexpr int kRpw = 2;                 // 16-row channel blocks per CTA (all warps share them)
+constexpr int kCtaCols = kRpw * 16;     // output channels per CTA
+constexpr int kMaxCluster = 8;
 
 struct GemvParams {
     const uint16_t* A;
@@ -50,25 +57,33 @@ struct GemvParams {
     int G;               // scale columns per channel row
     int tiles_per_group; // k-tiles per scale group
     int ktiles, ktiles_per_split, splits;
-    float* part;
-    unsigned* counters;
 };
+
+template <int MT>
+__host__ __device__ constexpr int red_floats()  // accumulator floats of one warp
+{
+    return kRpw * MT * 4 * 32;
+}
 
 template <int BITS, int ACT, int MT, bool GROUPED>
 __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
 {
     constexpr int KT = Geom<BITS>::KT;
     constexpr int KS = Geom<BITS>::KSTEPS;
-    constexpr int kUnroll = MT >= 4 ? 2 : 4;
+    constexpr int kDepth = MT <= 2 ? 4 : 2;  // tiles in flight per warp
+    constexpr int RF = red_floats<MT>();
+    extern __shared__ float red[];           // [kWarps][RF], then the CTA result [RF]
+
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int nblocks = p.n >> 4;
-    const int nb0 = (blockIdx.x * kWarps + warp) * kRpw;
-    // n % 64 == 0 makes nblocks a multiple of 4, so a warp is either wholly
-    // inside or wholly past the last channel block.
-    const bool active = nb0 < nblocks;
-    const int kt0 = blockIdx.y * p.ktiles_per_split;
-    const int kt1 = min(kt0 + p.ktiles_per_split, p.ktiles);
+    const int nb0 = blockIdx.x * kRpw;       // n % 64 == 0: both blocks exist
+    // this CTA's k range, then this warp's slice of it
+    const int c0 = blockIdx.y * p.ktiles_per_split;
+    const int c1 = min(c0 + p.ktiles_per_split, p.ktiles);
+    const int per_warp = (c1 - c0 + kWarps - 1) / kWarps;
+    const int kt0 = min(c0 + warp * per_warp, c1);
+    const int kt1 = min(kt0 + per_warp, c1);
+    const int nt = kt1 - kt0;
 
     float acc[kRpw][MT][4];
     float gp[kRpw][MT][4];
@@ -97,174 +112,197 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
         arow[j] = p.A + (size_t)(aval[j] ? r : 0) * p.k + 2 * t;
     }
 
-    if (active) {
-        const uint8_t* wp[kRpw];
+    const uint8_t* wp[kRpw];
+#pragma unroll
+    for (int r = 0; r < kRpw; ++r)
+        wp[r] = p.B + ((size_t)(nb0 + r) * p.ktiles + kt0) * kTileBytes + lane * 16;
+
+    // rolling prefetch: buf[u] holds tile (base + u) while it is consumed and
+    // is refilled with tile (base + u + kDepth) right after
+    uint4 buf[kDepth][kRpw];
+#pragma unroll
+    for (int u = 0; u < kDepth; ++u)
 #pragma unroll
         for (int r = 0; r < kRpw; ++r)
-            wp[r] = p.B + ((size_t)(nb0 + r) * p.ktiles + kt0) * kTileBytes + lane * 16;
+            if (u < nt)
+                buf[u][r] = ld_stream_v4(wp[r] + (size_t)u * kTileBytes);
 
-        for (int kt = kt0; kt < kt1; kt += kUnroll) {
-            uint4 wv[kUnroll][kRpw];
+    for (int base = 0; base < nt; base += kDepth) {
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < kDepth; ++u) {
+            const int i = base + u;
+            if (i < nt) {
+                uint4 cur[kRpw];
 #pragma unroll
-                for (int r = 0; r < kRpw; ++r)
-                    if (kt + u < kt1)
-                        wv[u][r] = ld_stream_v4(wp[r] + (size_t)(kt - kt0 + u) * kTileBytes);
+                for (int r = 0; r < kRpw; ++r) {
+                    cur[r] = buf[u][r];
+                    if (i + kDepth < nt)
+                        buf[u][r] = ld_stream_v4(wp[r] + (size_t)(i + kDepth) * kTileBytes);
+                }
+                const int ktile = kt0 + i;
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int ktile = kt + u;
-                if (ktile < kt1) {
+                for (int s = 0; s < KS; ++s) {
+                    uint32_t bf[MT][2];
 #pragma unroll
-                    for (int s = 0; s < KS; ++s) {
-                        uint32_t bf[MT][2];
+                    for (int j = 0; j < MT; ++j) {
+                        if (aval[j]) {
+                            const uint16_t* ap = arow[j] + ktile * KT + 16 * s;
+                            bf[j][0] = ld_nc_u32(ap);
+                            bf[j][1] = ld_nc_u32(ap + 8);
+                        } else {
+                            bf[j][0] = 0u;
+                            bf[j][1] = 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < kRpw; ++r) {
+                        uint32_t a[4];
+                        tile_frag<BITS, ACT>(cur[r], s, a);
 #pragma unroll
                         for (int j = 0; j < MT; ++j) {
-                            if (aval[j]) {
-                                const uint16_t* ap = arow[j] + ktile * KT + 16 * s;
-                                bf[j][0] = ld_nc_u32(ap);
-                                bf[j][1] = ld_nc_u32(ap + 8);
-                            } else {
-                                bf[j][0] = 0u;
-                                bf[j][1] = 0u;
-                            }
-                        }
-#pragma unroll
-                        for (int r = 0; r < kRpw; ++r) {
-                            uint32_t a[4];
-                            tile_frag<BITS, ACT>(wv[u][r], s, a);
-#pragma unroll
-                            for (int j = 0; j < MT; ++j) {
-                                if constexpr (GROUPED)
-                                    mma16816<ACT>(gp[r][j], a, bf[j][0], bf[j][1]);
-                                else
-                                    mma16816<ACT>(acc[r][j], a, bf[j][0], bf[j][1]);
-                            }
-                        }
-                        if constexpr (GROUPED) {
-                            const uint32_t one = ones_x2<ACT>();
-                            const uint32_t ones[4] = {one, one, one, one};
-#pragma unroll
-                            for (int j = 0; j < MT; ++j)
-                                mma16816<ACT>(rs[j], ones, bf[j][0], bf[j][1]);
+                            if constexpr (GROUPED)
+                                mma16816<ACT>(gp[r][j], a, bf[j][0], bf[j][1]);
+                            else
+                                mma16816<ACT>(acc[r][j], a, bf[j][0], bf[j][1]);
                         }
                     }
                     if constexpr (GROUPED) {
-                        const bool flush =
-                            ((ktile + 1) % p.tiles_per_group == 0) || (ktile + 1 == kt1);
-                        if (flush) {
-                            const int gi = ktile / p.tiles_per_group;
+                        const uint32_t one = ones_x2<ACT>();
+                        const uint32_t ones[4] = {one, one, one, one};
 #pragma unroll
-                            for (int r = 0; r < kRpw; ++r) {
-                                const size_t nlo = (size_t)(nb0 + r) * 16 + g;
-                                const float s_lo = to_f32<ACT>(ld_nc_u16(p.scales + nlo * p.G + gi));
-                                const float s_hi =
-                                    to_f32<ACT>(ld_nc_u16(p.scales + (nlo + 8) * p.G + gi));
-                                float z_lo = 0.f, z_hi = 0.f;
-                                if (p.zeros) {
-                                    z_lo = to_f32<ACT>(ld_nc_u16(p.zeros + nlo * p.G + gi));
-                                    z_hi = to_f32<ACT>(ld_nc_u16(p.zeros + (nlo + 8) * p.G + gi));
-                                }
+                        for (int j = 0; j < MT; ++j)
+                            mma16816<ACT>(rs[j], ones, bf[j][0], bf[j][1]);
+                    }
+                }
+                if constexpr (GROUPED) {
+                    if (((ktile + 1) % p.tiles_per_group == 0) || (i + 1 == nt)) {
+                        const int gi = ktile / p.tiles_per_group;
 #pragma unroll
-                                for (int j = 0; j < MT; ++j) {
-                                    acc[r][j][0] = fmaf(s_lo, gp[r][j][0], fmaf(z_lo, rs[j][0], acc[r][j][0]));
-                                    acc[r][j][1] = fmaf(s_lo, gp[r][j][1], fmaf(z_lo, rs[j][1], acc[r][j][1]));
-                                    acc[r][j][2] = fmaf(s_hi, gp[r][j][2], fmaf(z_hi, rs[j][2], acc[r][j][2]));
-                                    acc[r][j][3] = fmaf(s_hi, gp[r][j][3], fmaf(z_hi, rs[j][3], acc[r][j][3]));
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e)
-                                        gp[r][j][e] = 0.f;
-                                }
+                        for (int r = 0; r < kRpw; ++r) {
+                            const size_t nlo = (size_t)(nb0 + r) * 16 + g;
+                            const float s_lo = to_f32<ACT>(ld_nc_u16(p.scales + nlo * p.G + gi));
+                            const float s_hi = to_f32<ACT>(ld_nc_u16(p.scales + (nlo + 8) * p.G + gi));
+                            float z_lo = 0.f, z_hi = 0.f;
+                            if (p.zeros) {
+                                z_lo = to_f32<ACT>(ld_nc_u16(p.zeros + nlo * p.G + gi));
+                                z_hi = to_f32<ACT>(ld_nc_u16(p.zeros + (nlo + 8) * p.G + gi));
                             }
 #pragma unroll
-                            for (int j = 0; j < MT; ++j)
+                            for (int j = 0; j < MT; ++j) {
+                                acc[r][j][0] = fmaf(s_lo, gp[r][j][0], fmaf(z_lo, rs[j][0], acc[r][j][0]));
+                                acc[r][j][1] = fmaf(s_lo, gp[r][j][1], fmaf(z_lo, rs[j][1], acc[r][j][1]));
+                                acc[r][j][2] = fmaf(s_hi, gp[r][j][2], fmaf(z_hi, rs[j][2], acc[r][j][2]));
+                                acc[r][j][3] = fmaf(s_hi, gp[r][j][3], fmaf(z_hi, rs[j][3], acc[r][j][3]));
 #pragma unroll
                                 for (int e = 0; e < 4; ++e)
-                                    rs[j][e] = 0.f;
+                                    gp[r][j][e] = 0.f;
+                            }
                         }
+#pragma unroll
+                        for (int j = 0; j < MT; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                rs[j][e] = 0.f;
                     }
                 }
             }
         }
     }
 
-    // Accumulator element e of (r, j): channel n = 16*(nb0 + r) + g + 8*(e >> 1),
-    // activation row m = 8*j + 2*t + (e & 1).
-    if (p.splits == 1) {
-        if (!active)
-            return;
+    // ---- reduce the warps' accumulators in fixed order ----
+    // element (r, j, e) of lane L is red[w][((r * MT + j) * 4 + e) * 32 + L]
 #pragma unroll
-        for (int r = 0; r < kRpw; ++r)
+    for (int r = 0; r < kRpw; ++r)
 #pragma unroll
-            for (int j = 0; j < MT; ++j)
+        for (int j = 0; j < MT; ++j)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int nn = (nb0 + r) * 16 + g + 8 * (e >> 1);
-                    const int mm = 8 * j + 2 * t + (e & 1);
-                    if (mm < p.m) {
-                        float v = acc[r][j][e];
-                        if constexpr (!GROUPED)
-                            v *= to_f32<ACT>(ld_nc_u16(p.scales + nn));
-                        if (p.bias)
-                            v += to_f32<ACT>(ld_nc_u16(p.bias + nn));
-                        p.C[(size_t)mm * p.n + nn] = from_f32<ACT>(v);
-                    }
-                }
-        return;
+            for (int e = 0; e < 4; ++e)
+                red[warp * RF + ((r * MT + j) * 4 + e) * 32 + lane] = acc[r][j][e];
+    __syncthreads();
+    float* cta = red + kWarps * RF;
+    for (int idx = threadIdx.x; idx < RF; idx += blockDim.x) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            v += red[w * RF + idx];
+        cta[idx] = v;
     }
 
-    if (active) {
-#pragma unroll
-        for (int r = 0; r < kRpw; ++r)
-#pragma unroll
-            for (int j = 0; j < MT; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int nn = (nb0 + r) * 16 + g + 8 * (e >> 1);
-                    const int mm = 8 * j + 2 * t + (e & 1);
-                    if (mm < p.m)
-                        p.part[((size_t)blockIdx.y * p.m + mm) * p.n + nn] = acc[r][j][e];
-                }
+    // ---- across the cluster (k splits), in rank order ----
+    const bool clustered = p.splits > 1;
+    if (clustered) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every member's result is in its shared memory
+        if (cluster.block_rank() == 0) {
+            for (int idx = threadIdx.x; idx < RF; idx += blockDim.x) {
+                float v = cta[idx];
+                for (int rk = 1; rk < p.splits; ++rk)
+                    v += cluster.map_shared_rank(cta, rk)[idx];
+                cta[idx] = v;
+            }
+        }
+        cluster.sync();  // members stay resident until the leader has read them
+        if (cluster.block_rank() != 0)
+            return;
+    } else {
+        __syncthreads();
     }
-    __threadfence();
-    __syncthreads();
-    __shared__ unsigned s_prev;
-    if (threadIdx.x == 0)
-        s_prev = atomicAdd(&p.counters[blockIdx.x], 1u);
-    __syncthreads();
-    if (s_prev != (unsigned)(p.splits - 1))
-        return;
-    __threadfence();
-    const int n0 = blockIdx.x * kCtaCols;
-    for (int idx = threadIdx.x; idx < p.m * kCtaCols; idx += blockDim.x) {
-        const int mm = idx / kCtaCols;
-        const int nn = n0 + idx % kCtaCols;
-        if (nn >= p.n)
+
+    // ---- epilogue: element idx -> channel n, activation row m ----
+    for (int idx = threadIdx.x; idx < RF; idx += blockDim.x) {
+        const int L = idx & 31;
+        const int e = (idx >> 5) & 3;
+        const int rj = idx >> 7;
+        const int j = rj % MT, r = rj / MT;
+        const int nn = (nb0 + r) * 16 + (L >> 2) + 8 * (e >> 1);
+        const int mm = 8 * j + 2 * (L & 3) + (e & 1);
+        if (mm >= p.m)
             continue;
-        float v = 0.f;
-        for (int s = 0; s < p.splits; ++s)
-            v += __ldcg(p.part + ((size_t)s * p.m + mm) * p.n + nn);
+        float v = cta[idx];
         if constexpr (!GROUPED)
             v *= to_f32<ACT>(ld_nc_u16(p.scales + nn));
         if (p.bias)
             v += to_f32<ACT>(ld_nc_u16(p.bias + nn));
         p.C[(size_t)mm * p.n + nn] = from_f32<ACT>(v);
     }
-    if (threadIdx.x == 0)
-        p.counters[blockIdx.x] = 0u;
+}
+
+template <int BITS, int ACT, int MT, bool GROUPED>
+cudaError_t launch_one(const GemvPlan& plan, const GemvParams& gp, cudaStream_t s)
+{
+    auto kern = gemv_kernel<BITS, ACT, MT, GROUPED>;
+    const int smem = (kWarps + 1) * red_floats<MT>() * (int)sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(plan.grid_x, plan.splits);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (plan.splits > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = plan.splits;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, gp);
 }
 
 template <int BITS, int ACT, bool GROUPED>
-cudaError_t launch_mt(int mt, dim3 grid, const GemvParams& gp, cudaStream_t s)
+cudaError_t launch_mt(const GemvPlan& plan, const GemvParams& gp, cudaStream_t s)
 {
-    const dim3 block(kWarps * 32);
-    switch (mt) {
-    case 1: gemv_kernel<BITS, ACT, 1, GROUPED><<<grid, block, 0, s>>>(gp); break;
-    case 2: gemv_kernel<BITS, ACT, 2, GROUPED><<<grid, block, 0, s>>>(gp); break;
-    case 4: gemv_kernel<BITS, ACT, 4, GROUPED><<<grid, block, 0, s>>>(gp); break;
-    default: gemv_kernel<BITS, ACT, 8, GROUPED><<<grid, block, 0, s>>>(gp); break;
+    switch (plan.mt) {
+    case 1: return launch_one<BITS, ACT, 1, GROUPED>(plan, gp, s);
+    case 2: return launch_one<BITS, ACT, 2, GROUPED>(plan, gp, s);
+    case 4: return launch_one<BITS, ACT, 4, GROUPED>(plan, gp, s);
+    default: return launch_one<BITS, ACT, 8, GROUPED>(plan, gp, s);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -276,25 +314,25 @@ GemvPlan plan_gemv(int m, int n, int k, int bits)
     p.mt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;
     p.m_per_pass = 8 * p.mt;
     p.passes = (m + p.m_per_pass - 1) / p.m_per_pass;
-    p.grid_x = (n + kCtaCols - 1) / kCtaCols;
+    p.grid_x = n / kCtaCols;
     const int KT = bits == 8 ? 32 : 64;
     p.ktiles = k / KT;
-    const int target = num_sms() * 8;  // 128-thread CTAs that keep every SM streaming
+    // enough CTAs for about two per SM; split k across a cluster when the
+    // channel count alone does not provide them, keeping >= 2 tiles per warp
+    const int target = num_sms() * 2;
     int splits = (target + p.grid_x - 1) / p.grid_x;
-    int cap = p.ktiles / 4;
+    int cap = p.ktiles / (2 * kWarps);
     if (cap < 1)
         cap = 1;
-    if (cap > 64)
-        cap = 64;
+    if (cap > kMaxCluster)
+        cap = kMaxCluster;
     if (splits > cap)
         splits = cap;
     if (splits < 1)
         splits = 1;
     p.ktiles_per_split = (p.ktiles + splits - 1) / splits;
     p.splits = (p.ktiles + p.ktiles_per_split - 1) / p.ktiles_per_split;
-    const int prow = m < p.m_per_pass ? m : p.m_per_pass;
-    p.ws_partials = p.splits > 1 ? align_up((size_t)p.splits * prow * n * 4, 256) : 0;
-    p.ws_bytes = p.splits > 1 ? kWsScratch + p.ws_partials : 0;
+    p.ws_bytes = 0;
     return p;
 }
 
@@ -313,10 +351,6 @@ cudaError_t launch_gemv(const GemmArgs& a, const GemvPlan& p, cudaStream_t s)
     gp.ktiles = p.ktiles;
     gp.ktiles_per_split = p.ktiles_per_split;
     gp.splits = p.splits;
-    char* ws = static_cast<char*>(a.ws);
-    gp.counters = p.splits > 1 ? reinterpret_cast<unsigned*>(ws + kWsHeader) : nullptr;
-    gp.part = p.splits > 1 ? reinterpret_cast<float*>(ws + kWsScratch) : nullptr;
-    const dim3 grid(p.grid_x, p.splits);
     for (int pass = 0; pass < p.passes; ++pass) {
         const int m0 = pass * p.m_per_pass;
         const int rows = a.m - m0 < p.m_per_pass ? a.m - m0 : p.m_per_pass;
@@ -325,11 +359,11 @@ cudaError_t launch_gemv(const GemmArgs& a, const GemvPlan& p, cudaStream_t s)
         gp.C = static_cast<uint16_t*>(a.C) + (size_t)m0 * a.n;
         cudaError_t e;
         if (a.bits == 8) {
-            e = a.act == WO_F16 ? launch_mt<8, ACT_F16, false>(p.mt, grid, gp, s)
-                                : launch_mt<8, ACT_BF16, false>(p.mt, grid, gp, s);
+            e = a.act == WO_F16 ? launch_mt<8, ACT_F16, false>(p, gp, s)
+                                : launch_mt<8, ACT_BF16, false>(p, gp, s);
         } else {
-            e = a.act == WO_F16 ? launch_mt<4, ACT_F16, true>(p.mt, grid, gp, s)
-                                : launch_mt<4, ACT_BF16, true>(p.mt, grid, gp, s);
+            e = a.act == WO_F16 ? launch_mt<4, ACT_F16, true>(p, gp, s)
+                                : launch_mt<4, ACT_BF16, true>(p, gp, s);
         }
         if (e != cudaSuccess)
             return e;

@@ -35,12 +35,11 @@ struct GemvPlan {
     int mt;             // 8-row activation tiles per pass (1, 2, 4 or 8)
     int m_per_pass;     // rows per launch (8 * mt)
     int passes;         // launches needed to cover m
-    int grid_x;         // CTAs along n (128 output channels each)
-    int splits;         // CTAs along k
+    int grid_x;         // CTAs along n (32 output channels each)
+    int splits;         // CTAs along k, one thread-block cluster (<= 8)
     int ktiles;         // k / KT
     int ktiles_per_split;
-    size_t ws_partials; // bytes of fp32 partials (0 when splits == 1)
-    size_t ws_bytes;    // total, header and counter area included (0 if unused)
+    size_t ws_bytes;    // workspace bytes (none: the reduction stays on chip)
 };
 
 GemvPlan plan_gemv(int m, int n, int k, int bits);

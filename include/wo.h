@@ -149,6 +149,32 @@ WO_API wo_status wo_moe_ffn(const void* A, const float* gating_logits, const uin
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * wo_gemm without a workspace, for callers that cannot allocate device
+ * memory themselves (for example a plugin running inside an engine that owns
+ * all device memory through its own pool, or latency-critical code that must
+ * not call cudaMalloc, which can synchronise the device).  The pages have no
+ * counterpart: their runners always take a caller-allocated workspace.
+ *   Arguments as for wo_gemm, minus the workspace.  Always runs the
+ *   tensor-core kernel, whatever m is.
+ *   Scratch: a 16.31 MiB array in the library's device memory, held on every
+ *   GPU that loads the library until the process exits.  It must hold the
+ *   fp16 copy of bf16 activations that 4-bit weights need: m*k*2 bytes plus
+ *   m*4 bytes of row scales, each rounded up to 256 bytes, within 16 MiB and
+ *   256 KiB (e.g. m*k <= 8,388,608 and m <= 65,536); larger problems return
+ *   WO_ERR_WORKSPACE with nothing enqueued.  Other cases need no scratch.
+ *   The first call on a device looks up the array's device address and
+ *   zeroes its error word (a blocking cudaMemset), so make that first call
+ *   before any stream capture.  The call allocates and frees nothing.
+ *   Every call shares the array: calls whose kernels overlap on the GPU
+ *   (unordered streams) race on it.  A kernel that gives up a bounded wait
+ *   is not reported by this entry point.
+ */
+WO_API wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed, const void* scales,
+                                    const void* zeros, const void* bias, void* C, int m, int n,
+                                    int k, int group_size, int bits, wo_dtype act_dtype,
+                                    void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the error word a kernel may
  * have left in `workspace` (a tensor-core kernel that gave up a bounded wait
  * writes it instead of hanging).  Returns WO_OK, WO_ERR_TIMEOUT, or

@@ -115,3 +115,13 @@ def test_library_load_fails_loudly_when_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(wo, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         wo.load_library()
+
+
+def test_noalloc_entry_validates_before_any_cuda_call(lib):
+    # invalid shape, unsupported combination, and a problem larger than the
+    # built-in scratch: all rejected before the scratch is touched
+    f = lib.wo_gemm_tc_noalloc
+    assert f(4096, 8192, 64, None, None, 16384, 512, 100, 2048, 64, 4, 1, None) == 1
+    assert f(4096, 8192, 64, 64, None, 16384, 512, 256, 2048, -1, 8, 0, None) == 2
+    assert f(4096, 8192, 64, None, None, 16384, 4096, 256, 4096, 64, 4, 1, None) == 3
+    assert f(4096, 8192, 64, None, None, 16384, 0, 256, 2048, 64, 4, 1, None) == 0

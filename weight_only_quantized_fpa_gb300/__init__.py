@@ -20,6 +20,7 @@ __all__ = [
     "WO_F16", "WO_BF16", "WoError", "load_library", "library_path",
     "wo_status_string", "wo_packed_bytes", "wo_pack", "wo_unpack", "wo_workspace_size",
     "wo_gemm", "wo_moe_workspace_size", "wo_moe_ffn", "wo_check_workspace",
+    "wo_gemm_tc_noalloc",
     "pack", "unpack", "gemm", "moe_ffn", "Workspace",
 ]
 
@@ -77,6 +78,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.wo_moe_ffn.restype = I
         lib.wo_check_workspace.argtypes = [P, S, P]
         lib.wo_check_workspace.restype = I
+        lib.wo_gemm_tc_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
+        lib.wo_gemm_tc_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -158,6 +161,17 @@ def wo_moe_ffn(A, gating_logits, fc1_packed, fc1_scales, fc2_packed, fc2_scales,
                                      _ptr(out), T, hidden, inter, experts, topk,
                                      int(renormalize), act_dtype, _ptr(workspace),
                                      workspace_bytes, _stream_ptr(stream)), "wo_moe_ffn")
+
+
+def wo_gemm_tc_noalloc(A, B_packed, scales, zeros, bias, C, m: int, n: int, k: int,
+                       group_size: int, bits: int, act_dtype: int, stream=None) -> None:
+    """The tensor-core GEMM with the library's built-in scratch: for callers
+    that cannot allocate device memory.  Calls that overlap on the GPU race
+    on the shared scratch."""
+    _raise(load_library().wo_gemm_tc_noalloc(_ptr(A), _ptr(B_packed), _ptr(scales), _ptr(zeros),
+                                             _ptr(bias), _ptr(C), m, n, k, group_size, bits,
+                                             act_dtype, _stream_ptr(stream)),
+           "wo_gemm_tc_noalloc")
 
 
 def wo_check_workspace(workspace, workspace_bytes: int, stream=None) -> int:

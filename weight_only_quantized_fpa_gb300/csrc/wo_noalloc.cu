@@ -1,0 +1,117 @@
+// wo_noalloc.cu -- wo_gemm_tc_noalloc: the tensor-core GEMM with its scratch
+// memory in a file-scope device array instead of a caller-provided workspace.
+//
+// Who needs it: callers that cannot allocate device memory themselves, for
+// instance a plugin that runs inside an engine owning all device memory
+// through its own pool, or latency-critical code that must not call
+// cudaMalloc (which can synchronise the whole device).  They pass inputs and
+// outputs only.
+//
+// The scratch (error word, fp16 copy of bf16 activations and their row
+// scales) lives in g_scratch below; every GPU that loads this library keeps
+// it (16.31 MiB) until the process exits.  Host code cannot use
+// g_scratch's name as a device address, so the first call on each device
+// looks the address up with cudaGetSymbolAddress (with that device current)
+// and caches it.  That first call also zeroes the error word with a blocking
+// cudaMemset, so it should come before any stream capture.
+//
+// All calls share the one array: two calls whose kernels overlap on the GPU
+// (different streams, no ordering between them) race on it.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "wo_internal.h"
+
+namespace wo {
+namespace {
+
+// Size of the built-in scratch: the 64.25 KiB header area every tensor-core
+// call uses, plus 16 MiB for the fp16 copy of bf16 activations (m * k * 2
+// bytes, 4-bit weights only) and 256 KiB for its row scales (m * 4 bytes),
+// e.g. m * k <= 8,388,608 with m <= 65,536.
+constexpr size_t kNoAllocBytes = kWsScratch + ((size_t)16 << 20) + ((size_t)256 << 10);
+
+__device__ __align__(256) unsigned char g_scratch[kNoAllocBytes];
+
+std::mutex g_mu;
+void* g_addr[64] = {nullptr};
+
+// Device address of g_scratch on the current device, set up on first use.
+cudaError_t scratch_address(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaMemset(p, 0, kWsHeader);  // error word starts at zero
+        if (e != cudaSuccess)
+            return e;
+        g_addr[dev] = p;
+    }
+    *out = g_addr[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
+}  // namespace
+}  // namespace wo
+
+using namespace wo;
+
+extern "C" wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed,
+                                        const void* scales, const void* zeros, const void* bias,
+                                        void* C, int m, int n, int k, int group_size, int bits,
+                                        wo_dtype act_dtype, void* stream)
+{
+    if (m < 0 || n < 0 || k <= 0 || (bits != 4 && bits != 8) || n % 64 != 0 || k % 64 != 0)
+        return WO_ERR_INVALID_ARG;
+    if (act_dtype != WO_F16 && act_dtype != WO_BF16)
+        return WO_ERR_INVALID_ARG;
+    const int g = (group_size == -1 || group_size == k) ? k : group_size;
+    if (g <= 0 || k % g != 0)
+        return WO_ERR_INVALID_ARG;
+    if ((bits == 8 && (g != k || zeros)) || (bits == 4 && g != k && g % 64 != 0))
+        return WO_ERR_UNSUPPORTED;
+    if (m == 0 || n == 0)
+        return WO_OK;
+    if (!A || !B_packed || !scales || !C || !aligned16(A) || !aligned16(B_packed) ||
+        !aligned16(C) || !aligned2(scales) || (zeros && !aligned2(zeros)) ||
+        (bias && !aligned2(bias)))
+        return WO_ERR_INVALID_ARG;
+    const TcPlan plan = plan_tc(m, n, k, bits, act_dtype);
+    if (plan.a16_bytes > ((size_t)16 << 20) || plan.rowscale_bytes > ((size_t)256 << 10) ||
+        plan.ws_bytes > kNoAllocBytes)
+        return WO_ERR_WORKSPACE;  // the problem needs more scratch than is built in
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess)
+        return WO_ERR_CUDA;
+
+    GemmArgs a{};
+    a.A = A;
+    a.B = B_packed;
+    a.scales = scales;
+    a.zeros = zeros;
+    a.bias = bias;
+    a.C = C;
+    a.m = m;
+    a.n = n;
+    a.k = k;
+    a.group = g;
+    a.bits = bits;
+    a.act = act_dtype;
+    a.ws = scratch;
+    a.ws_bytes = kNoAllocBytes;
+    return launch_tc(a, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess ? WO_OK
+                                                                                : WO_ERR_CUDA;
+}

@@ -2,7 +2,7 @@
 """Benchmark of the weight-only quantized GEMM on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload w8_decode|w4_g64|w8_large|w4_tiny]
+                    [--workload w8_decode|w4_g64|w8_large|w4_tiny|moe]
 
 One step is one pass of the hot path over the workload's batch: one wo_gemm
 per (m, N, K) case of the workload, each case with its own weights.  The
@@ -57,6 +57,11 @@ WORKLOADS = {
                           "{(2048,2048),(4096,4096),(4608,3584)}, fp16"),
     "w4_tiny": dict(config=1, unit="GB/s", dtype="bf16",
                     desc="W4A16 tiny: m=1, N=256, K=512, group 64, bf16"),
+    "moe": dict(config=5, unit="GB/s", dtype="bf16",
+                desc="MoE grouped weight-only FFN: T=1024 tokens, 64 experts, top-2 of softmax "
+                     "of fp32 logits ~N(0,1); hidden 4096, inter 1408; per expert fc1 "
+                     "[2816,4096] and fc2 [4096,1408] int8 per-channel, bf16 scales "
+                     "~U(0.001,0.01); SiLU-gated fc1, fc2, routing-weighted sum; A bf16 ~N(0,1)"),
 }
 
 HBM_FALLBACK_GBS = 6800.0
@@ -251,9 +256,54 @@ def max_over_ranks(ws, x: float) -> float:
 
 # ---------------------------------------------------------------- arms -----
 
+def run_reference_moe(args):
+    import oracle
+    oracle.build()
+    w = WORKLOADS["moe"]
+    c = inputs.make_moe_case()
+    threads = os.cpu_count() or 1
+    per_expert = c.weight_bytes / c.E
+    per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+
+    def one(ntok, first):
+        tokens = (np.arange(ntok) + first) % c.T
+        t0 = time.perf_counter()
+        oracle.moe_ffn(c.A, c.act_dtype, c.logits, c.fc1, c.fc1_scales, c.fc2, c.fc2_scales,
+                       c.T, c.H, c.I, c.E, c.topk, tokens=tokens, nthreads=threads)
+        dt = time.perf_counter() - t0
+        ids, _ = oracle.moe_route(c.logits[tokens], c.topk)
+        return dt, len(set(ids.reshape(-1).tolist())) * per_expert
+
+    dt, _ = one(2, 0)
+    ntok = max(1, min(c.T, int(2 * per_step_budget / max(dt, 1e-3))))
+    for i in range(args.warmup):
+        one(ntok, i * ntok)
+    tot_t = tot_b = 0.0
+    for i in range(args.steps):
+        dt, b = one(ntok, (args.warmup + i) * ntok)
+        tot_t += dt
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["desc"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {ntok} consecutive tokens; bytes = the weights "
+                                   "of the experts they route to"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
+    if args.workload == "moe":
+        return run_reference_moe(args)
     w = WORKLOADS[args.workload]
     cases = workload_cases(args.workload)
     import oracle
@@ -285,6 +335,134 @@ def run_reference(args, ws, rank):
         "e2e": {"value": value, "unit": w["unit"], "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_moe(args, ws, rank, local):
+    import torch
+
+    import weight_only_quantized_fpa_gb300 as wo
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wo.load_library()
+    w = WORKLOADS["moe"]
+    c = inputs.make_moe_case()
+    dt = torch.bfloat16
+
+    def up16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+
+    A = up16(c.A)
+    logits = torch.from_numpy(c.logits).to(dev)
+    fc1 = wo.pack_experts(torch.from_numpy(c.fc1).to(dev), c.E, 2 * c.I, c.H, 8)
+    fc2 = wo.pack_experts(torch.from_numpy(c.fc2).to(dev), c.E, c.H, c.I, 8)
+    s1, s2 = up16(c.fc1_scales), up16(c.fc2_scales)
+    out = torch.empty((c.T, c.H), dtype=dt, device=dev)
+    need = wo.wo_moe_workspace_size(c.T, c.H, c.I, c.E, c.topk)
+    workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(Ain=None):
+        wo.wo_moe_ffn(A if Ain is None else Ain, logits, fc1, s1, fc2, s2, out, c.T, c.H, c.I,
+                      c.E, c.topk, 0, inputs.BF16, workspace, need, stream)
+
+    with torch.cuda.stream(stream):
+        call()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+    torch.cuda.synchronize()
+    bytes_per_step = c.weight_bytes
+    launches_per_step = 4  # routing, fc1, fc2, combine
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(ws, start.elapsed_time(end))
+    secs = total_ms / 1e3
+    value = bytes_per_step * args.steps * ws / secs / 1e9
+
+    hA = torch.empty(A.shape, dtype=dt, pin_memory=True)
+    hA.copy_(A.cpu())
+    hL = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    hL.copy_(logits.cpu())
+    hO = torch.empty(out.shape, dtype=dt, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 30))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            A.copy_(hA, non_blocking=True)
+            logits.copy_(hL, non_blocking=True)
+            wo.moe_ffn(A, logits, fc1, s1, fc2, s2, c.H, c.I, c.E, c.topk, out=out,
+                       workspace=workspace, stream=stream)
+            hO.copy_(out, non_blocking=True)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    stream.synchronize()
+    e2e_s = max_over_ranks(ws, time.perf_counter() - t0)
+    if rank != 0:
+        return 0
+    hbm_gbs, _, peak_src = measured_peaks()
+    achieved = bytes_per_step / (total_ms / args.steps / 1e3) / 1e9
+    try:
+        sh = kernel_source_hash(["wo_moe.cu", "wo_common.cuh"])
+    except OSError:
+        sh = None
+    tr = traffic_from_profile("expert_gemv_kernel", sh) if sh else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["desc"], "weight_bytes_per_step": bytes_per_step,
+                   "l2": f"inputs larger than L2: {bytes_per_step / 1e6:.0f} MB of expert "
+                         "weights per step",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "peak_source": f"hbm_gbs ({peak_src})",
+                     "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                     "kernel": "wo_moe_ffn (routing + fc1 + fc2 + combine, timed together)",
+                     "algorithmic_bytes_per_launch": bytes_per_step},
+        "e2e": {"value": bytes_per_step * e2e_steps * ws / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": hA.numel() * 2 + hL.numel() * 4,
+                "d2h_bytes_per_step": hO.numel() * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        tokens = np.arange(8)
+        t0 = time.perf_counter()
+        oracle.moe_ffn(c.A, c.act_dtype, c.logits, c.fc1, c.fc1_scales, c.fc2, c.fc2_scales,
+                       c.T, c.H, c.I, c.E, c.topk, tokens=tokens)
+        dt_s = time.perf_counter() - t0
+        ids, _ = oracle.moe_route(c.logits[tokens], c.topk)
+        per_expert = c.weight_bytes / c.E
+        touched = len(set(ids.reshape(-1).tolist())) * per_expert
+        line["cpu_baseline"] = {"value": touched / dt_s / 1e9, "unit": "GB/s",
+                                "cores": os.cpu_count() or 1, "kind": "oracle",
+                                "sample": f"the first 8 tokens ({touched / 1e6:.0f} MB of the "
+                                          f"experts they route to), {dt_s:.2f} s wall"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -473,6 +651,8 @@ def main():
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         rc = run_reference(args, ws, rank)
+    elif args.workload == "moe":
+        rc = run_moe(args, ws, rank, local)
     else:
         rc = run_ours(args, ws, rank, local)
     if ws > 1:

@@ -21,7 +21,7 @@ __all__ = [
     "wo_status_string", "wo_packed_bytes", "wo_pack", "wo_unpack", "wo_workspace_size",
     "wo_gemm", "wo_moe_workspace_size", "wo_moe_ffn", "wo_check_workspace",
     "wo_gemm_tc_noalloc",
-    "pack", "unpack", "gemm", "moe_ffn", "Workspace",
+    "pack", "unpack", "pack_experts", "gemm", "moe_ffn", "Workspace",
 ]
 
 WO_F16 = 0
@@ -215,6 +215,18 @@ def pack(B_rowmajor, n: int, k: int, bits: int, stream=None):
     import torch
     out = torch.empty(wo_packed_bytes(n, k, bits), dtype=torch.uint8, device=B_rowmajor.device)
     wo_pack(B_rowmajor, out, n, k, bits, stream)
+    return out
+
+
+def pack_experts(B_rowmajor, experts: int, n: int, k: int, bits: int, stream=None):
+    """Row-major codes of `experts` matrices [experts, n, ...] -> one buffer of
+    consecutive wo_pack outputs (the layout wo_moe_ffn reads)."""
+    import torch
+    per = wo_packed_bytes(n, k, bits)
+    out = torch.empty(experts * per, dtype=torch.uint8, device=B_rowmajor.device)
+    src = B_rowmajor.reshape(experts, -1)
+    for e in range(experts):
+        wo_pack(src[e], out.data_ptr() + e * per, n, k, bits, stream)
     return out
 
 

@@ -10,7 +10,12 @@
 // Design:
 //   - a warp owns kRpw blocks of 16 output channels and a slice of k; each
 //     lane streams its 16 bytes of every 512-byte packed tile with 128-bit
-//     non-caching loads (kUnroll tiles in flight per block);
+//     non-caching loads, kDepth tiles in flight per block (a rolling
+//     register prefetch that never drains until the slice ends);
+//   - the CTA's slice of the activations (and, for 4-bit weights, the scales
+//     and zeros of its channels and groups) is staged in shared memory once,
+//     after the first weight loads are in flight, so the inner loop waits on
+//     weights only;
 //   - the codes are turned into exact (q - offset) fp16/bf16 pairs in
 //     registers (wo_common.cuh) that are directly the A fragments of
 //     mma.m16n8k16; activations form the B fragments (8 rows of A per mma,
@@ -45,6 +50,7 @@ constexpr int kWarps = 8;
 constexpr int kRpw = 2;                 // 16-row channel blocks per CTA (all warps share them)
 constexpr int kCtaCols = kRpw * 16;     // output channels per CTA
 constexpr int kMaxCluster = 8;
+constexpr int kAsmemBudget = 64 * 1024; // bytes of staged activations per CTA
 
 struct GemvParams {
     const uint16_t* A;
@@ -57,12 +63,32 @@ struct GemvParams {
     int G;               // scale columns per channel row
     int tiles_per_group; // k-tiles per scale group
     int ktiles, ktiles_per_split, splits;
+    int a_stride;        // bytes per staged activation row (ktiles_per_split * KT * 2 + 16)
+    int a_rows;          // staged activation rows (min(m, 8 * MT))
+    int g_span;          // scale groups staged per channel (4-bit)
 };
 
 template <int MT>
 __host__ __device__ constexpr int red_floats()  // accumulator floats of one warp
 {
     return kRpw * MT * 4 * 32;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
 template <int BITS, int ACT, int MT, bool GROUPED>
@@ -72,7 +98,13 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
     constexpr int KS = Geom<BITS>::KSTEPS;
     constexpr int kDepth = MT <= 2 ? 4 : 2;  // tiles in flight per warp
     constexpr int RF = red_floats<MT>();
-    extern __shared__ float red[];           // [kWarps][RF], then the CTA result [RF]
+    // shared memory: [kWarps + 1][RF] floats (reduction), the staged
+    // activations [a_rows][a_stride bytes], then (4-bit) scales and zeros
+    // [kCtaCols][g_span] each as 16-bit values
+    extern __shared__ __align__(16) float red[];
+    uint8_t* a_sm = reinterpret_cast<uint8_t*>(red + (kWarps + 1) * RF);
+    uint16_t* s_sm = reinterpret_cast<uint16_t*>(a_sm + p.a_rows * p.a_stride);
+    uint16_t* z_sm = s_sm + kCtaCols * p.g_span;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -84,6 +116,46 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
     const int kt0 = min(c0 + warp * per_warp, c1);
     const int kt1 = min(kt0 + per_warp, c1);
     const int nt = kt1 - kt0;
+    const int g_lo = GROUPED ? c0 / p.tiles_per_group : 0;
+
+    const uint8_t* wp[kRpw];
+#pragma unroll
+    for (int r = 0; r < kRpw; ++r)
+        wp[r] = p.B + ((size_t)(nb0 + r) * p.ktiles + kt0) * kTileBytes + lane * 16;
+
+    // rolling prefetch: buf[u] holds tile (base + u) while it is consumed and
+    // is refilled with tile (base + u + kDepth) right after
+    uint4 buf[kDepth][kRpw];
+#pragma unroll
+    for (int u = 0; u < kDepth; ++u)
+#pragma unroll
+        for (int r = 0; r < kRpw; ++r)
+            if (u < nt)
+                buf[u][r] = ld_stream_v4(wp[r] + (size_t)u * kTileBytes);
+
+    // ---- stage this CTA's activations (and 4-bit scales/zeros) ----
+    {
+        const int cols8 = (c1 - c0) * KT / 8;  // 16-byte pieces per row
+        const int total = p.a_rows * cols8;
+        const uint32_t a_base = static_cast<uint32_t>(__cvta_generic_to_shared(a_sm));
+        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+            const int row = idx / cols8, c8 = idx % cols8;
+            cp_async16(a_base + row * p.a_stride + c8 * 16,
+                       p.A + (size_t)row * p.k + (size_t)c0 * KT + c8 * 8);
+        }
+        if constexpr (GROUPED) {
+            const int g_hi = (c1 - 1) / p.tiles_per_group;
+            const int gc = g_hi - g_lo + 1;
+            for (int idx = threadIdx.x; idx < kCtaCols * gc; idx += blockDim.x) {
+                const int ch = idx / gc, gg = idx % gc;
+                const size_t src = (size_t)(nb0 * 16 + ch) * p.G + g_lo + gg;
+                s_sm[ch * p.g_span + gg] = ld_nc_u16(p.scales + src);
+                z_sm[ch * p.g_span + gg] = p.zeros ? ld_nc_u16(p.zeros + src) : (uint16_t)0;
+            }
+        }
+        cp_async_wait_all();
+        __syncthreads();
+    }
 
     float acc[kRpw][MT][4];
     float gp[kRpw][MT][4];
@@ -103,29 +175,16 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
         for (int e = 0; e < 4; ++e)
             rs[j][e] = 0.f;
 
-    const uint16_t* arow[MT];
+    // B-fragment addresses in the staged activations: row 8j + g, k pair 2t
+    uint32_t arow[MT];
     bool aval[MT];
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
         const int r = 8 * j + g;
         aval[j] = r < p.m;
-        arow[j] = p.A + (size_t)(aval[j] ? r : 0) * p.k + 2 * t;
+        arow[j] = static_cast<uint32_t>(__cvta_generic_to_shared(a_sm)) +
+                  (aval[j] ? r : 0) * p.a_stride + 4 * t;
     }
-
-    const uint8_t* wp[kRpw];
-#pragma unroll
-    for (int r = 0; r < kRpw; ++r)
-        wp[r] = p.B + ((size_t)(nb0 + r) * p.ktiles + kt0) * kTileBytes + lane * 16;
-
-    // rolling prefetch: buf[u] holds tile (base + u) while it is consumed and
-    // is refilled with tile (base + u + kDepth) right after
-    uint4 buf[kDepth][kRpw];
-#pragma unroll
-    for (int u = 0; u < kDepth; ++u)
-#pragma unroll
-        for (int r = 0; r < kRpw; ++r)
-            if (u < nt)
-                buf[u][r] = ld_stream_v4(wp[r] + (size_t)u * kTileBytes);
 
     for (int base = 0; base < nt; base += kDepth) {
 #pragma unroll
@@ -140,15 +199,16 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
                         buf[u][r] = ld_stream_v4(wp[r] + (size_t)(i + kDepth) * kTileBytes);
                 }
                 const int ktile = kt0 + i;
+                const uint32_t koff = (uint32_t)((ktile - c0) * KT * 2);
 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     uint32_t bf[MT][2];
 #pragma unroll
                     for (int j = 0; j < MT; ++j) {
                         if (aval[j]) {
-                            const uint16_t* ap = arow[j] + ktile * KT + 16 * s;
-                            bf[j][0] = ld_nc_u32(ap);
-                            bf[j][1] = ld_nc_u32(ap + 8);
+                            const uint32_t ap = arow[j] + koff + 32 * s;
+                            bf[j][0] = lds32(ap);
+                            bf[j][1] = lds32(ap + 16);
                         } else {
                             bf[j][0] = 0u;
                             bf[j][1] = 0u;
@@ -176,17 +236,14 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
                 }
                 if constexpr (GROUPED) {
                     if (((ktile + 1) % p.tiles_per_group == 0) || (i + 1 == nt)) {
-                        const int gi = ktile / p.tiles_per_group;
+                        const int gl = ktile / p.tiles_per_group - g_lo;
 #pragma unroll
                         for (int r = 0; r < kRpw; ++r) {
-                            const size_t nlo = (size_t)(nb0 + r) * 16 + g;
-                            const float s_lo = to_f32<ACT>(ld_nc_u16(p.scales + nlo * p.G + gi));
-                            const float s_hi = to_f32<ACT>(ld_nc_u16(p.scales + (nlo + 8) * p.G + gi));
-                            float z_lo = 0.f, z_hi = 0.f;
-                            if (p.zeros) {
-                                z_lo = to_f32<ACT>(ld_nc_u16(p.zeros + nlo * p.G + gi));
-                                z_hi = to_f32<ACT>(ld_nc_u16(p.zeros + (nlo + 8) * p.G + gi));
-                            }
+                            const int ch = r * 16 + g;
+                            const float s_lo = to_f32<ACT>(s_sm[ch * p.g_span + gl]);
+                            const float s_hi = to_f32<ACT>(s_sm[(ch + 8) * p.g_span + gl]);
+                            const float z_lo = to_f32<ACT>(z_sm[ch * p.g_span + gl]);
+                            const float z_hi = to_f32<ACT>(z_sm[(ch + 8) * p.g_span + gl]);
 #pragma unroll
                             for (int j = 0; j < MT; ++j) {
                                 acc[r][j][0] = fmaf(s_lo, gp[r][j][0], fmaf(z_lo, rs[j][0], acc[r][j][0]));
@@ -208,7 +265,6 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const GemvParams p)
             }
         }
     }
-
     // ---- reduce the warps' accumulators in fixed order ----
     // element (r, j, e) of lane L is red[w][((r * MT + j) * 4 + e) * 32 + L]
 #pragma unroll
@@ -271,11 +327,19 @@ template <int BITS, int ACT, int MT, bool GROUPED>
 cudaError_t launch_one(const GemvPlan& plan, const GemvParams& gp, cudaStream_t s)
 {
     auto kern = gemv_kernel<BITS, ACT, MT, GROUPED>;
-    const int smem = (kWarps + 1) * red_floats<MT>() * (int)sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = (kWarps + 1) * red_floats<MT>() * (int)sizeof(float) +
+                     gp.a_rows * gp.a_stride + 2 * kCtaCols * gp.g_span * 2;
+    static int smem_set[64] = {0};  // largest opt-in granted so far, per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (smem > 48 * 1024 && (dev < 0 || dev >= 64 || smem > smem_set[dev])) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
+        if (dev >= 0 && dev < 64)
+            smem_set[dev] = smem;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(plan.grid_x, plan.splits);
@@ -305,34 +369,66 @@ cudaError_t launch_mt(const GemvPlan& plan, const GemvParams& gp, cudaStream_t s
     }
 }
 
+// Shared memory a launch needs (mirrors launch_one).
+size_t gemv_smem(int mt, int a_rows, int a_stride, int g_span)
+{
+    return (size_t)(kWarps + 1) * kRpw * mt * 4 * 32 * 4 + (size_t)a_rows * a_stride +
+           (size_t)2 * kCtaCols * g_span * 2;
+}
+
 }  // namespace
 
-GemvPlan plan_gemv(int m, int n, int k, int bits)
+GemvPlan plan_gemv(int m, int n, int k, int group, int bits)
 {
     GemvPlan p{};
-    const int rows = m < 64 ? m : 64;
-    p.mt = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;
-    p.m_per_pass = 8 * p.mt;
-    p.passes = (m + p.m_per_pass - 1) / p.m_per_pass;
-    p.grid_x = n / kCtaCols;
     const int KT = bits == 8 ? 32 : 64;
     p.ktiles = k / KT;
+    p.grid_x = n / kCtaCols;
+    const int tpg = group / KT;
     // enough CTAs for about two per SM; split k across a cluster when the
     // channel count alone does not provide them, keeping >= 2 tiles per warp
     const int target = num_sms() * 2;
-    int splits = (target + p.grid_x - 1) / p.grid_x;
+    int want = (target + p.grid_x - 1) / p.grid_x;
     int cap = p.ktiles / (2 * kWarps);
     if (cap < 1)
         cap = 1;
     if (cap > kMaxCluster)
         cap = kMaxCluster;
-    if (splits > cap)
-        splits = cap;
-    if (splits < 1)
-        splits = 1;
-    p.ktiles_per_split = (p.ktiles + splits - 1) / splits;
-    p.splits = (p.ktiles + p.ktiles_per_split - 1) / p.ktiles_per_split;
-    p.ws_bytes = 0;
+    if (want > cap)
+        want = cap;
+    if (want < 1)
+        want = 1;
+    // the staged activation slice must fit: try 8-row tiles per pass from
+    // the natural count down, and a larger shared-memory budget last
+    const int rows = m < 64 ? m : 64;
+    const int mt0 = rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;
+    for (int budget : {kAsmemBudget, 160 * 1024}) {
+        for (int mt = mt0; mt >= 1; mt /= 2) {
+            const int prow = m < 8 * mt ? m : 8 * mt;
+            int splits = want;
+            for (; splits <= kMaxCluster; ++splits) {
+                const int kps = (p.ktiles + splits - 1) / splits;
+                const int gspan = bits == 4 ? (kps + tpg - 1) / tpg + 1 : 0;
+                const size_t need = gemv_smem(mt, prow, kps * KT * 2 + 16, gspan);
+                if (need <= (size_t)budget + (size_t)(kWarps + 1) * kRpw * mt * 4 * 32 * 4)
+                    break;
+            }
+            if (splits <= kMaxCluster) {
+                p.mt = mt;
+                p.m_per_pass = 8 * mt;
+                p.passes = (m + p.m_per_pass - 1) / p.m_per_pass;
+                p.ktiles_per_split = (p.ktiles + splits - 1) / splits;
+                p.splits = (p.ktiles + p.ktiles_per_split - 1) / p.ktiles_per_split;
+                p.a_rows = prow;
+                p.a_stride = p.ktiles_per_split * KT * 2 + 16;
+                p.g_span = bits == 4 ? (p.ktiles_per_split + tpg - 1) / tpg + 1 : 0;
+                p.valid = true;
+                p.ws_bytes = 0;
+                return p;
+            }
+        }
+    }
+    p.valid = false;  // k too long to stage even 8 rows per pass
     return p;
 }
 
@@ -351,10 +447,13 @@ cudaError_t launch_gemv(const GemmArgs& a, const GemvPlan& p, cudaStream_t s)
     gp.ktiles = p.ktiles;
     gp.ktiles_per_split = p.ktiles_per_split;
     gp.splits = p.splits;
+    gp.a_stride = p.a_stride;
+    gp.g_span = p.g_span;
     for (int pass = 0; pass < p.passes; ++pass) {
         const int m0 = pass * p.m_per_pass;
         const int rows = a.m - m0 < p.m_per_pass ? a.m - m0 : p.m_per_pass;
         gp.m = rows;
+        gp.a_rows = rows;
         gp.A = static_cast<const uint16_t*>(a.A) + (size_t)m0 * a.k;
         gp.C = static_cast<uint16_t*>(a.C) + (size_t)m0 * a.n;
         cudaError_t e;

@@ -5,7 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/wo.h"
+#include "wo.h"  // include/wo.h, found through -I
 
 namespace wo {
 
@@ -39,10 +39,14 @@ struct GemvPlan {
     int splits;         // CTAs along k, one thread-block cluster (<= 8)
     int ktiles;         // k / KT
     int ktiles_per_split;
+    int a_rows;         // activation rows staged in shared memory per launch
+    int a_stride;       // bytes per staged activation row
+    int g_span;         // scale groups staged per channel (4-bit)
+    bool valid;         // false when k is too long to stage even 8 rows
     size_t ws_bytes;    // workspace bytes (none: the reduction stays on chip)
 };
 
-GemvPlan plan_gemv(int m, int n, int k, int bits);
+GemvPlan plan_gemv(int m, int n, int k, int group, int bits);
 
 struct GemmArgs {
     const void* A;

@@ -61,10 +61,10 @@ wo_status check_gemm_shape(int m, int n, int k, int group_size, int bits)
 wo_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WO_OK : WO_ERR_CUDA; }
 
 // Kernel choice by m: the weight-streaming kernel below kTcMinM rows (when
-// its activation slice can be staged), the tensor-core kernel otherwise.
+// its shared-memory ring fits), the tensor-core kernel otherwise.
 bool use_tc(int m, int n, int k, int group_size, int bits)
 {
-    return m >= kTcMinM || !plan_gemv(m, n, k, norm_group(group_size, k), bits).valid;
+    return m >= kTcMinM || !stream_supported(m, n, k, norm_group(group_size, k), bits);
 }
 
 }  // namespace
@@ -127,7 +127,7 @@ size_t wo_workspace_size(int m, int n, int k, int group_size, int bits)
         // the larger of the two activation dtypes' needs
         return plan_tc(m, n, k, bits, WO_BF16).ws_bytes;
     }
-    return plan_gemv(m, n, k, norm_group(group_size, k), bits).ws_bytes;
+    return stream_workspace_bytes();
 }
 
 wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, const void* zeros,
@@ -170,7 +170,7 @@ wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, co
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (use_tc(m, n, k, group_size, bits))
         return cuda_status(launch_tc(a, plan_tc(m, n, k, bits, act_dtype), s));
-    return cuda_status(launch_gemv(a, plan_gemv(m, n, k, a.group, bits), s));
+    return cuda_status(launch_stream_gemm(a, s));
 }
 
 wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, void* stream)

@@ -29,12 +29,10 @@
 // fp16 by a prepass with a per-row power-of-two scale (exact for bf16 values
 // of normal range), and the weight is fp16 round((q - 8) * s + z) computed
 // by one fused multiply-add per pair from the exact fp16 (q - 8).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "wo_common.cuh"
 #include "wo_internal.h"
 #include "wo_sm100.cuh"
+#include "wo_tmap.h"
 
 namespace wo {
 namespace {
@@ -353,40 +351,6 @@ __global__ void a_to_f16_kernel(const uint16_t* __restrict__ A, uint16_t* __rest
         rowscale[row] = ldexpf(1.f, E);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        else
-            cudaGetLastError();
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-              CUtensorMapSwizzle sw)
-{
-    auto fn = encode_fn();
-    if (!fn)
-        return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BITS, int OT, int ACT>
 cudaError_t launch_tc_t(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& tp,
                         cudaStream_t s)
@@ -441,13 +405,13 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     }
     const int OT = a.bits == 4 ? WO_F16 : a.act;
     CUtensorMap ma, mb;
-    if (!make_map(&ma, OT == WO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+    if (!make_tmap_2d(&ma, OT == WO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   Aop, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2, BK, BM,
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // packed codes viewed as [n/16 rows] x [bytes per 16-channel row / 4] words
     const uint64_t row_bytes = (uint64_t)a.k * 16 * a.bits / 8;
-    if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.B, row_bytes / 4, (uint64_t)a.n / 16,
+    if (!make_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.B, row_bytes / 4, (uint64_t)a.n / 16,
                   row_bytes, BK * 16 * a.bits / 8 / 4, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     if (a.bits == 8)

@@ -30,24 +30,6 @@ int num_sms();  // SM count of the current device (152 when none is visible)
 cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,
                         cudaStream_t s);
 
-// ---- weight-streaming kernel (small m) -----------------------------------
-struct GemvPlan {
-    int mt;             // 8-row activation tiles per pass (1, 2, 4 or 8)
-    int m_per_pass;     // rows per launch (8 * mt)
-    int passes;         // launches needed to cover m
-    int grid_x;         // CTAs along n (32 output channels each)
-    int splits;         // CTAs along k, one thread-block cluster (<= 8)
-    int ktiles;         // k / KT
-    int ktiles_per_split;
-    int a_rows;         // activation rows staged in shared memory per launch
-    int a_stride;       // bytes per staged activation row
-    int g_span;         // scale groups staged per channel (4-bit)
-    bool valid;         // false when k is too long to stage even 8 rows
-    size_t ws_bytes;    // workspace bytes (none: the reduction stays on chip)
-};
-
-GemvPlan plan_gemv(int m, int n, int k, int group, int bits);
-
 struct GemmArgs {
     const void* A;
     const uint8_t* B;
@@ -63,7 +45,10 @@ struct GemmArgs {
     size_t ws_bytes;
 };
 
-cudaError_t launch_gemv(const GemmArgs& a, const GemvPlan& p, cudaStream_t s);
+// small m: the weight-streaming kernel (wo_stream.cu)
+size_t stream_workspace_bytes();
+bool stream_supported(int m, int n, int k, int group, int bits);
+cudaError_t launch_stream_gemm(const GemmArgs& a, cudaStream_t s);
 
 // ---- tensor-core kernel (large m) -----------------------------------------
 constexpr int kTcMinM = 65;  // m at and above which wo_gemm uses the tensor-core kernel

@@ -9,41 +9,34 @@
 //      (renormalised over the chosen ones on request); then a stable
 //      counting sort of the T*k (token, slot) pairs by expert, giving each
 //      expert a contiguous range of rows.
-//   2. expert_gemv_kernel<GATED = true>: per expert and 128 gate channels,
-//      x1 = A[rows] . dequant(fc1_e)^T for the gate channels and the matching
-//      up channels (inter apart), h = round(silu(g) * u) into [rows, inter].
-//   3. expert_gemv_kernel<GATED = false>: y = h[rows] . dequant(fc2_e)^T in
-//      fp32 into [rows, hidden].
+//   2. gather_rows_kernel copies the activation rows into expert order;
+//      then the weight-streaming kernel (wo_stream.cu), gated output, one
+//      CTA row per expert: x1 = A[rows] . dequant(fc1_e)^T for gate channels
+//      and the matching up channels (inter apart), h = round(silu(g) * u)
+//      into [rows, inter].
+//   3. the same kernel, fp32 output: y = h[rows] . dequant(fc2_e)^T into
+//      [rows, hidden].
 //   4. combine_kernel: out[t] = round(sum_j p[t][j] * y[row(t, j)]), j in
 //      ascending order.
 // Every sum has a fixed order, so the result is bit-for-bit repeatable.
 //
-// The expert kernels stream packed 8-bit tiles exactly like the decode
-// kernel (register dequant into mma.m16n8k16 fragments) but share the
-// activation rows among all warps: the warps of a CTA own different channel
-// blocks and walk k together, one 256-wide chunk at a time, reading the
-// expert's gathered rows from a double-buffered shared-memory chunk.
+// The expert GEMMs run up to 64 rows per pass; experts with more rows take
+// several passes over their weights.
 #include <cuda_runtime.h>
 
 #include "wo_common.cuh"
 #include "wo_internal.h"
+#include "wo_stream.h"
 
 namespace wo {
 namespace {
 
-constexpr int kMoeWarps = 8;
-constexpr int kChunk = 256;          // k per lockstep chunk (8 tiles of 32)
-constexpr int kRowsPerPass = 64;     // activation rows per pass (8 n8-tiles)
-constexpr int kMT = kRowsPerPass / 8;
-constexpr int kDepth = 3;            // weight tiles in flight per block and warp
-constexpr int kChunkTiles = kChunk / 32;
-constexpr int kAStride = kChunk * 2 + 16;  // bytes per staged row (padded)
 constexpr int kRouteThreads = 1024;
 
 // ---------------------------------------------------------------- layout ---
 
 struct MoeLayout {
-    size_t ids, wts, pos, offsets, perm_tok, h, y, total;
+    size_t ids, wts, pos, offsets, perm_tok, a_sorted, h, y, total;
 };
 
 MoeLayout moe_layout(int T, int hidden, int inter, int experts, int topk)
@@ -61,6 +54,7 @@ MoeLayout moe_layout(int T, int hidden, int inter, int experts, int topk)
     L.pos = take(P * 4);
     L.offsets = take((size_t)(experts + 1) * 4);
     L.perm_tok = take(P * 4);
+    L.a_sorted = take(P * (size_t)hidden * 2);
     L.h = take(P * (size_t)inter * 2);
     L.y = take(P * (size_t)hidden * 4);
     L.total = off;
@@ -179,191 +173,15 @@ __global__ void __launch_bounds__(kRouteThreads)
     }
 }
 
-// ---------------------------------------------------------- expert GEMV ----
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+// A rows in expert order: a_sorted[p] = A[perm_tok[p]] (16-byte pieces).
+__global__ void gather_rows_kernel(const uint4* __restrict__ A, const int* __restrict__ perm_tok,
+                                   uint4* __restrict__ a_sorted, int row_vecs)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
-struct ExpertParams {
-    const uint16_t* A;      // GATED: tokens [T, K]; else sorted rows [P, K]
-    const int* perm_tok;    // sorted row -> token (GATED only)
-    const int* offsets;     // [E + 1]
-    const uint8_t* W;       // packed weights, expert e at W + e * w_stride
-    size_t w_stride;
-    const uint16_t* scales; // [E, N]
-    int N;                  // output channels of the weight (2*inter for fc1)
-    int K;
-    int inter;              // GATED: channel offset between gate and up
-    uint16_t* H;            // GATED output [P, inter]
-    float* Y;               // plain output [P, N]
-};
-
-// GATED: warp w of CTA x owns gate block (8x + w) and its up block
-// (8x + w + inter/16).  Plain: warp w owns blocks 2(8x + w) and +1.
-template <int ACT, bool GATED>
-__global__ void __launch_bounds__(kMoeWarps * 32)
-    expert_gemv_kernel(const ExpertParams p)
-{
-    extern __shared__ __align__(16) uint8_t a_sm[];  // [2][kRowsPerPass][kAStride]
-    const int e = blockIdx.y;
-    const int row0 = p.offsets[e];
-    const int rows_e = p.offsets[e + 1] - row0;
-    if (rows_e <= 0)
-        return;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int ktiles = p.K / 32;
-    const int nblocks = p.N / 16;
-    int blk[2];
-    bool active;
-    if constexpr (GATED) {
-        blk[0] = blockIdx.x * kMoeWarps + warp;
-        blk[1] = blk[0] + p.inter / 16;
-        active = blk[0] < p.inter / 16;
-    } else {
-        blk[0] = 2 * (blockIdx.x * kMoeWarps + warp);
-        blk[1] = blk[0] + 1;
-        active = blk[1] < nblocks;
-    }
-    const uint8_t* Wexp = p.W + (size_t)e * p.w_stride;
-    const uint16_t* sexp = p.scales + (size_t)e * p.N;
-    const uint32_t a_base = static_cast<uint32_t>(__cvta_generic_to_shared(a_sm));
-    const int nchunks = (p.K + kChunk - 1) / kChunk;
-
-    for (int pass0 = 0; pass0 < rows_e; pass0 += kRowsPerPass) {
-        const int rows = min(kRowsPerPass, rows_e - pass0);
-
-        // stage chunk c of the pass's activation rows into buffer c & 1
-        auto stage = [&](int c) {
-            const int kc = c * kChunk;
-            const int cols8 = min(kChunk, p.K - kc) / 8;
-            const uint32_t buf = a_base + (uint32_t)((c & 1) * kRowsPerPass * kAStride);
-            for (int idx = threadIdx.x; idx < rows * cols8; idx += blockDim.x) {
-                const int r = idx / cols8, c8 = idx % cols8;
-                const int srow = GATED ? p.perm_tok[row0 + pass0 + r] : row0 + pass0 + r;
-                cp_async16(buf + r * kAStride + c8 * 16, p.A + (size_t)srow * p.K + kc + c8 * 8);
-            }
-            cp_async_commit();
-        };
-
-        float acc[2][kMT][4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int j = 0; j < kMT; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    acc[r][j][q] = 0.f;
-
-        const uint8_t* wp[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-            wp[r] = Wexp + (size_t)(active ? blk[r] : 0) * ktiles * kTileBytes + lane * 16;
-        uint4 buf[kDepth][2];
-#pragma unroll
-        for (int u = 0; u < kDepth; ++u)
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-                if (active && u < ktiles)
-                    buf[u][r] = ld_stream_v4(wp[r] + (size_t)u * kTileBytes);
-
-        stage(0);
-        int i = 0;  // tile index along k
-        for (int c = 0; c < nchunks; ++c) {
-            if (c + 1 < nchunks) {
-                stage(c + 1);
-                cp_async_wait_1();
-            } else {
-                cp_async_wait_0();
-            }
-            __syncthreads();
-            const uint32_t abuf = a_base + (uint32_t)((c & 1) * kRowsPerPass * kAStride);
-            const int ct1 = min((c + 1) * kChunkTiles, ktiles);
-            if (active) {
-                for (; i < ct1; i += kDepth) {
-#pragma unroll
-                    for (int u = 0; u < kDepth; ++u) {
-                        const int ii = i + u;
-                        if (ii < ct1) {
-                            uint4 cur[2];
-                            const int slot = ii % kDepth;
-#pragma unroll
-                            for (int r = 0; r < 2; ++r) {
-                                // slots rotate with the absolute tile index
-                                cur[r] = slot == 0 ? buf[0][r] : slot == 1 ? buf[1][r] : buf[2][r];
-                                if (ii + kDepth < ktiles) {
-                                    const uint4 nv = ld_stream_v4(wp[r] + (size_t)(ii + kDepth) * kTileBytes);
-                                    if (slot == 0) buf[0][r] = nv;
-                                    else if (slot == 1) buf[1][r] = nv;
-                                    else buf[2][r] = nv;
-                                }
-                            }
-                            const uint32_t koff = (uint32_t)((ii - c * kChunkTiles) * 64);
-#pragma unroll
-                            for (int s = 0; s < 2; ++s) {
-                                uint32_t a0[4], a1[4];
-                                tile_frag<8, ACT>(cur[0], s, a0);
-                                tile_frag<8, ACT>(cur[1], s, a1);
-#pragma unroll
-                                for (int j = 0; j < kMT; ++j) {
-                                    if (8 * j < rows) {  // warp-uniform
-                                        uint32_t b0 = 0u, b1 = 0u;
-                                        if (8 * j + g < rows) {
-                                            const uint32_t ap = abuf + (8 * j + g) * kAStride + koff + 32 * s + 4 * t;
-                                            b0 = lds32(ap);
-                                            b1 = lds32(ap + 16);
-                                        }
-                                        mma16816<ACT>(acc[0][j], a0, b0, b1);
-                                        mma16816<ACT>(acc[1][j], a1, b0, b1);
-                                    }
-                                }
-                            }
-                        }
-                    }
-                }
-                i = ct1;
-            }
-            __syncthreads();  // the buffer is restaged two chunks later
-        }
-
-        // ---- epilogue: element q of (r, j): channel blk[r]*16 + g + 8*(q>>1),
-        // row 8j + 2t + (q & 1) of this pass ----
-        if (active) {
-#pragma unroll
-            for (int j = 0; j < kMT; ++j) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int rr = 8 * j + 2 * t + (q & 1);
-                    if (rr >= rows)
-                        continue;
-                    const size_t prow = (size_t)(row0 + pass0 + rr);
-                    const int ch0 = blk[0] * 16 + g + 8 * (q >> 1);
-                    const int ch1 = blk[1] * 16 + g + 8 * (q >> 1);
-                    const float v0 = acc[0][j][q] * to_f32<ACT>(ld_nc_u16(sexp + ch0));
-                    const float v1 = acc[1][j][q] * to_f32<ACT>(ld_nc_u16(sexp + ch1));
-                    if constexpr (GATED) {
-                        const float silu = v0 / (1.f + expf(-v0));
-                        p.H[prow * p.inter + ch0] = from_f32<ACT>(silu * v1);
-                    } else {
-                        p.Y[prow * p.N + ch0] = v0;
-                        p.Y[prow * p.N + ch1] = v1;
-                    }
-                }
-            }
-        }
-    }
+    const int p = blockIdx.x;
+    const uint4* src = A + (size_t)perm_tok[p] * row_vecs;
+    uint4* dst = a_sorted + (size_t)p * row_vecs;
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x)
+        dst[i] = src[i];
 }
 
 template <int ACT>
@@ -393,6 +211,7 @@ cudaError_t launch_moe(const void* A, const float* logits, const uint8_t* fc1, c
     int* pos = reinterpret_cast<int*>(ws + L.pos);
     int* offsets = reinterpret_cast<int*>(ws + L.offsets);
     int* perm_tok = reinterpret_cast<int*>(ws + L.perm_tok);
+    uint16_t* a_sorted = reinterpret_cast<uint16_t*>(ws + L.a_sorted);
     uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
     float* y = reinterpret_cast<float*>(ws + L.y);
 
@@ -402,48 +221,60 @@ cudaError_t launch_moe(const void* A, const float* logits, const uint8_t* fc1, c
     if (err != cudaSuccess)
         return err;
 
-    const int smem = 2 * kRowsPerPass * kAStride;
-    static int smem_set[64] = {0};
-    int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess)
+    const int P = T * topk;
+    gather_rows_kernel<<<P, 128, 0, s>>>(static_cast<const uint4*>(A), perm_tok,
+                                         reinterpret_cast<uint4*>(a_sorted), H / 8);
+    if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
-    if (dev < 0 || dev >= 64 || smem_set[dev] < smem) {
-        for (auto kern : {expert_gemv_kernel<ACT, true>, expert_gemv_kernel<ACT, false>})
-            if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-                cudaSuccess)
-                return err;
-        if (dev >= 0 && dev < 64)
-            smem_set[dev] = smem;
-    }
 
-    ExpertParams p1{};
-    p1.A = static_cast<const uint16_t*>(A);
-    p1.perm_tok = perm_tok;
+    // fc1 with the gated activation, on the rows in expert order
+    StreamPlan P1 = plan_stream(64, 2 * I, H, H, 8, OUT_GATED, I);
+    if (!P1.valid)
+        return cudaErrorInvalidValue;
+    StreamParams p1{};
+    p1.A = a_sorted;
+    p1.a_rows_total = P;
     p1.offsets = offsets;
-    p1.W = fc1;
-    p1.w_stride = (size_t)2 * I * H;
+    p1.B = fc1;
+    p1.w_block_rows = E * (2 * I / 16);
+    p1.blocks_per_expert = 2 * I / 16;
     p1.scales = static_cast<const uint16_t*>(fc1_s);
+    p1.s_stride = (size_t)2 * I;
     p1.N = 2 * I;
     p1.K = H;
+    p1.ktiles = H / 32;
+    p1.G = 1;
+    p1.tiles_per_group = H / 32;
     p1.inter = I;
-    p1.H = h;
-    const dim3 g1((I / 16 + kMoeWarps - 1) / kMoeWarps, E);
-    expert_gemv_kernel<ACT, true><<<g1, kMoeWarps * 32, smem, s>>>(p1);
-    if ((err = cudaGetLastError()) != cudaSuccess)
+    p1.kt_per_split = H / 32;
+    p1.splits = 1;
+    p1.stages = P1.stages;
+    p1.C = h;
+    p1.err = reinterpret_cast<unsigned*>(ws);
+    if ((err = launch_stream(p1, P1, 8, ACT, OUT_GATED, E, s)) != cudaSuccess)
         return err;
 
-    ExpertParams p2{};
+    // fc2 to fp32: the sorted rows of h
+    StreamPlan P2 = plan_stream(64, H, I, I, 8, OUT_F32, 0);
+    if (!P2.valid)
+        return cudaErrorInvalidValue;
+    StreamParams p2 = p1;
     p2.A = h;
-    p2.offsets = offsets;
-    p2.W = fc2;
-    p2.w_stride = (size_t)H * I;
+    p2.B = fc2;
+    p2.w_block_rows = E * (H / 16);
+    p2.blocks_per_expert = H / 16;
     p2.scales = static_cast<const uint16_t*>(fc2_s);
+    p2.s_stride = (size_t)H;
     p2.N = H;
     p2.K = I;
+    p2.ktiles = I / 32;
+    p2.tiles_per_group = I / 32;
+    p2.inter = 0;
+    p2.kt_per_split = I / 32;
+    p2.stages = P2.stages;
+    p2.C = nullptr;
     p2.Y = y;
-    const dim3 g2((H / 32 + kMoeWarps - 1) / kMoeWarps, E);
-    expert_gemv_kernel<ACT, false><<<g2, kMoeWarps * 32, smem, s>>>(p2);
-    if ((err = cudaGetLastError()) != cudaSuccess)
+    if ((err = launch_stream(p2, P2, 8, ACT, OUT_F32, E, s)) != cudaSuccess)
         return err;
 
     combine_kernel<ACT><<<T, 256, 0, s>>>(y, pos, wts, static_cast<uint16_t*>(out), H, topk);

@@ -104,6 +104,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
         : "memory");
 }
 
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------- tcgen05 ----
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols)
@@ -197,6 +208,13 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_
     asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
                  "r"(r0), "r"(r1), "r"(r2), "r"(r3)
                  : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
+    return v;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t saddr)

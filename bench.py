@@ -12,11 +12,12 @@ default workload is the A16W8 per-channel decode set (fp16 A with m in
 (packed code bytes + scale bytes per second).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
-and torch.cuda.synchronize(); each case is replayed from its own CUDA graph
-(one kernel) with CUDA events between cases on the launching stream, so the
-step time and every kernel's duration are device times.  The 12 decode cases
-read 12 distinct weight matrices (about 700 MB per step, over five times the
-L2), so every launch streams its weights from HBM.
+and torch.cuda.synchronize(); a step is one CUDA graph holding every case's
+kernel back to back, timed with CUDA events on the launching stream.  The 12
+decode cases read 12 distinct weight matrices (about 700 MB per step, over
+five times the L2), so every launch streams its weights from HBM.  A
+per-case breakdown is measured afterwards, each case replayed alone between
+the others.
 
 Rank 0 prints one JSON line.  `--impl reference` times the CPU oracle (the
 plain C implementation the tests check against) on a bounded sample of the
@@ -77,7 +78,33 @@ def parse_args():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w8_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing leg (for quick local runs)")
+    ap.add_argument("--profile-case", type=int, default=None, metavar="I",
+                    help="profiling mode: run only case I of the workload, --steps calls, "
+                         "and print no JSON (for ncu captures)")
     return ap.parse_args()
+
+
+def run_profile_case(args):
+    import torch
+
+    import weight_only_quantized_fpa_gb300 as wo
+
+    wo.load_library()
+    c = workload_cases(args.workload)[args.profile_case]
+    dt = torch.float16 if c.act_dtype == inputs.F16 else torch.bfloat16
+
+    def up16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(dt)
+
+    A, s = up16(c.A), up16(c.scales)
+    z = None if c.zeros is None else up16(c.zeros)
+    b = None if c.bias is None else up16(c.bias)
+    B = wo.pack(torch.from_numpy(c.B).cuda(), c.n, c.k, c.bits)
+    for _ in range(args.steps):
+        wo.gemm(A, B, s, c.n, c.k, c.bits, group_size=c.group_size, zeros=z, bias=b)
+    torch.cuda.synchronize()
+    print(f"profiled {c.name}: {args.steps} calls", file=sys.stderr)
+    return 0
 
 
 # ------------------------------------------------------------- workload ---
@@ -506,12 +533,17 @@ def run_ours(args, ws, rank, local):
                    d["C"] if C is None else C, c.m, c.n, c.k, c.group_size, c.bits,
                    c.act_dtype, workspace, ws_bytes, stream)
 
-    # one CUDA graph per case (one kernel each)
+    # one CUDA graph per step (every case, one kernel each, back to back) for
+    # the timed region, and one per case for the per-case breakdown
     graphs = []
     with torch.cuda.stream(stream):
         for d in dev_cases:
             call(d)
         stream.synchronize()
+        step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(step_graph, stream=stream):
+            for d in dev_cases:
+                call(d)
         for d in dev_cases:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -524,37 +556,42 @@ def run_ours(args, ws, rank, local):
     flops_per_step = sum(case_flops(c) for c in cases)
     ncase = len(cases)
 
-    def run_steps(nsteps, events=None):
-        with torch.cuda.stream(stream):
-            for s in range(nsteps):
-                for i, g in enumerate(graphs):
-                    if events is not None:
-                        events[s][i].record(stream)
-                    g.replay()
-                if events is not None:
-                    events[s][ncase].record(stream)
-
     sampler = ClockSampler(local)
     sampler.start()
-    run_steps(args.warmup)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step_graph.replay()
     torch.cuda.synchronize()
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(ncase + 1)]
-              for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
-    start.record(stream)
-    run_steps(args.steps, events)
-    end.record(stream)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            step_graph.replay()
+        end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     clocks = sampler.stop()
     total_ms = start.elapsed_time(end)
-    per_case_ms = [statistics.fmean(events[s][i].elapsed_time(events[s][i + 1])
-                                    for s in range(args.steps)) for i in range(ncase)]
     total_ms = max_over_ranks(ws, total_ms)
     secs = total_ms / 1e3
+
+    # per-case breakdown (outside the timed region): each case replayed on its
+    # own between the others, so its weights are not in L2; includes the
+    # launch gap of a lone graph
+    nrep = max(1, min(args.steps, 20))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ncase + 1)] for _ in range(nrep)]
+    with torch.cuda.stream(stream):
+        for r in range(nrep):
+            for i, g in enumerate(graphs):
+                ev[r][i].record(stream)
+                g.replay()
+            ev[r][ncase].record(stream)
+    torch.cuda.synchronize()
+    per_case_ms = [statistics.fmean(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(nrep))
+                   for i in range(ncase)]
 
     if w["unit"] == "GB/s":
         value = bytes_per_step * args.steps * ws / secs / 1e9
@@ -597,18 +634,20 @@ def run_ours(args, ws, rank, local):
         return 0
 
     hbm_gbs, bf16_tf, peak_src = measured_peaks()
-    kern_ms = sum(per_case_ms)
+    # the step graph holds only this library's kernels, one per case, back to
+    # back: their average duration is the step time over the launches
+    kern_ms = total_ms / args.steps
     if w["unit"] == "GB/s":
         achieved = bytes_per_step / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                 "frac": achieved / hbm_gbs, "peak_source": f"hbm_gbs ({peak_src})"}
-        src = ["wo_gemv.cu", "wo_common.cuh"]
-        kname = "gemv_kernel"
+        src = ["wo_stream.cu", "wo_common.cuh", "wo_sm100.cuh"]
+        kname = "stream_kernel"
     else:
         achieved = flops_per_step / (kern_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
                 "frac": achieved / bf16_tf, "peak_source": f"bf16_tflops burst ({peak_src})"}
-        src = ["wo_gemm_tc.cu", "wo_common.cuh"]
+        src = ["wo_gemm_tc.cu", "wo_common.cuh", "wo_sm100.cuh"]
         kname = "gemm_tc_kernel"
     try:
         sh = kernel_source_hash(src)
@@ -618,6 +657,8 @@ def run_ours(args, ws, rank, local):
     roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
     roof["algorithmic_bytes_per_launch"] = bytes_per_step / ncase
     roof["kernel"] = kname
+    roof["timing"] = (f"{ncase} launches per step back to back in one CUDA graph; achieved = "
+                      "algorithmic bytes (or flops) per step / step time")
 
     line = {
         "metric": METRIC, "value": value, "unit": w["unit"], "n_gpus": ws,
@@ -626,10 +667,14 @@ def run_ours(args, ws, rank, local):
         "dtype": w["dtype"], "data": "synthetic",
         "config": {"workload": w["desc"], "cases": ncase,
                    "weight_bytes_per_step": bytes_per_step,
-                   "l2": "inputs larger than L2: every case has its own weights "
-                         f"({bytes_per_step / 1e6:.0f} MB per step)",
+                   "l2": ("inputs larger than L2: every case has its own weights "
+                          f"({bytes_per_step / 1e6:.0f} MB per step)") if bytes_per_step > 129e6
+                         else (f"working set {bytes_per_step / 1e6:.2f} MB fits in L2 and is not "
+                               "flushed: a latency-bound parity case"),
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": roof,
+        "cases_note": "per case: replayed alone between the other cases (cold L2), "
+                      "launch gap of a lone graph included",
         "cases": [{"m": c.m, "n": c.n, "k": c.k, "us": ms * 1e3,
                    ("gbs" if w["unit"] == "GB/s" else "tflops"):
                        (c.weight_bytes / (ms / 1e3) / 1e9) if w["unit"] == "GB/s"
@@ -648,6 +693,8 @@ def run_ours(args, ws, rank, local):
 
 def main():
     args = parse_args()
+    if args.profile_case is not None:
+        return run_profile_case(args)
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         rc = run_reference(args, ws, rank)

@@ -62,6 +62,9 @@ SMALL = [
     (65, 128, 256, 4, 64, inputs.BF16, True, True),
     (100, 256, 512, 8, -1, inputs.BF16, False, True),
     (130, 320, 448, 4, 64, inputs.F16, True, False),
+    (96, 128, 512, 4, -1, inputs.BF16, True, True),     # per-channel 4-bit, tensor cores
+    (80, 256, 1024, 4, 128, inputs.BF16, True, False),  # group 128, tensor cores
+    (24, 256, 1024, 4, 128, inputs.F16, True, True),    # group 128, streaming kernel
 ]
 
 

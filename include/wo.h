@@ -111,6 +111,12 @@ WO_API size_t wo_workspace_size(int m, int n, int k, int group_size, int bits);
  * The kernel is chosen by m: a split-K weight-streaming kernel for small m,
  * a tcgen05 tensor-core kernel for large m.  Results are deterministic:
  * identical inputs give bit-identical C.
+ * Ordering: the small-m kernel uses programmatic dependent launch.  It may
+ * start reading B_packed, scales, zeros and bias while the previous
+ * operation on the stream is still running, so those must not be written by
+ * the immediately preceding kernel on the stream (weights packed at load
+ * time, with any synchronisation in between, are fine).  A is read and C
+ * written only after the previous operation has completed, as usual.
  */
 WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales,
                   const void* zeros, const void* bias, void* C, int m, int n, int k,

@@ -187,3 +187,28 @@ def test_workspace_shared_across_shapes(wo):
         assert_within_tolerance(from_device_bits(Cb), inputs.F16, b.oracle_rows(), "decode")
         assert_within_tolerance(from_device_bits(Cc), inputs.BF16, c.oracle_rows(), "tc w8")
     assert wo.wo_check_workspace(ws, ws.numel()) == 0
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_chained_calls_keep_stream_order(wo, m):
+    # Y = X . W1^T, then X = Y . W2^T on one stream with no sync in between:
+    # the second call must read Y only after the first wrote it, and must not
+    # overwrite X before the first has read it (the small-m kernel starts
+    # early and prefetches weights while the previous kernel finishes)
+    n = k = 3584
+    c1 = inputs.make_gemm_case(8, 200 + m, m, n, k, bits=8, group_size=-1, act_dtype=inputs.F16,
+                               scale_lo=0.001, scale_hi=0.01, with_zeros=False, with_bias=False)
+    c2 = inputs.make_gemm_case(8, 300 + m, m, n, k, bits=8, group_size=-1, act_dtype=inputs.F16,
+                               scale_lo=0.001, scale_hi=0.01, with_zeros=False, with_bias=False)
+    d1, d2 = DeviceCase(c1), DeviceCase(c2)
+    X = d1.A.clone()
+    Y = torch.empty((m, n), dtype=X.dtype, device="cuda")
+    for _ in range(3):
+        X.copy_(d1.A)
+        wo.gemm(X, d1.B, d1.scales, n, k, 8, out=Y)
+        wo.gemm(Y, d2.B, d2.scales, n, k, 8, out=X)
+        torch.cuda.synchronize()
+        y = from_device_bits(Y)
+        assert_within_tolerance(y, inputs.F16, d1.oracle_rows(), "first call")
+        ref2 = oracle.gemm(y, inputs.F16, c2.B, c2.scales, None, None, m, n, k, -1, 8)
+        assert_within_tolerance(from_device_bits(X), inputs.F16, ref2, "second call")

@@ -210,11 +210,19 @@ def _workspace_for(device, nbytes):
     return ws.get(nbytes)
 
 
+def _sync(stream):
+    import torch
+    (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+
+
 def pack(B_rowmajor, n: int, k: int, bits: int, stream=None):
-    """Row-major codes (uint8 [n, k] or [n, k/2]) -> packed uint8 buffer."""
+    """Row-major codes (uint8 [n, k] or [n, k/2]) -> packed uint8 buffer.
+    A load-time step: it waits for the packing to finish, so the GEMMs that
+    prefetch weights early always see the packed bytes."""
     import torch
     out = torch.empty(wo_packed_bytes(n, k, bits), dtype=torch.uint8, device=B_rowmajor.device)
     wo_pack(B_rowmajor, out, n, k, bits, stream)
+    _sync(stream)
     return out
 
 
@@ -227,6 +235,7 @@ def pack_experts(B_rowmajor, experts: int, n: int, k: int, bits: int, stream=Non
     src = B_rowmajor.reshape(experts, -1)
     for e in range(experts):
         wo_pack(src[e], out.data_ptr() + e * per, n, k, bits, stream)
+    _sync(stream)
     return out
 
 

@@ -29,6 +29,10 @@
 //   - when k is long for the number of channels, the k range is split across
 //     a thread-block cluster of up to 8 CTAs and the leader sums the
 //     members' accumulators through distributed shared memory in rank order.
+//   - launched with programmatic dependent launch: the producer fetches the
+//     first stages' weights before waiting for the previous grid, and every
+//     read of activations or routing data and every output write comes after
+//     that wait.
 // Every sum has a fixed order: the result is bit-for-bit repeatable.  Every
 // mbarrier wait is bounded; a wait that runs out records an error word and
 // the CTA winds down (the producer first lets its copies in flight land).
@@ -69,10 +73,9 @@ __host__ inline int stage_bytes_host(int bits, int mt, int nw, int tps)
     return (tx + 1023) / 1024 * 1024;
 }
 
-// Consumer warps and tiles per stage of each configuration (the warps per
-// CTA, with the producer warp, stay a multiple of 4 -- 9 and 16 warps -- so
-// the register file splits evenly across the 4 schedulers).
-__host__ __device__ inline int stream_nw(int out) { return out != OUT_PLAIN ? 15 : 8; }
+// Tiles per stage of each configuration.  Consumer warps: 15 for the MoE
+// experts (16 warps with the producer, so the register file splits evenly
+// across the 4 schedulers), 8 or 4 for the plain GEMM (chosen by the plan).
 __host__ __device__ inline int stream_tps(int mt, int bits, int out)
 {
     const int k_stage = (out != OUT_PLAIN || mt >= 4) ? 64 : 128;
@@ -177,8 +180,15 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2;
 
-    // ---- work of this CTA ----
+    // Programmatic dependent launch: the next grid may start now (it waits
+    // for this one before touching its outputs); this grid waits for the
+    // previous one before reading anything that grid may produce.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const bool moe = p.offsets != nullptr;
+    if (moe)  // the row ranges come from the routing kernel
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- work of this CTA ----
     const int e = moe ? blockIdx.y : 0;
     const int row0 = moe ? p.offsets[e] : 0;
     const int rows_total = moe ? p.offsets[e + 1] - row0 : p.m;
@@ -209,25 +219,44 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             const int brow = e * p.blocks_per_expert;
             const int wrow0 = OUT == OUT_GATED ? brow + blockIdx.x * NW : brow + blockIdx.x * 2 * NW;
             const int wrow1 = brow + p.inter / 16 + blockIdx.x * NW;
+            auto load_w = [&](int s, int kt_s) {
+                uint8_t* wdst = smem + (size_t)s * SG::STAGE + SG::A_BYTES;
+                tma_load_2d(wdst, &tmW, &full[s], kt_s * 64, wrow0);
+                if constexpr (OUT == OUT_GATED)
+                    tma_load_2d(wdst + NW * TPS * kTileBytes, &tmW, &full[s], kt_s * 64, wrow1);
+            };
+            auto load_a = [&](int s, int kt_s, int prow0) {
+                uint8_t* stage = smem + (size_t)s * SG::STAGE;
+#pragma unroll
+                for (int h = 0; h < SG::NHALF; ++h)
+                    tma_load_2d(stage + h * SG::A_BOX, &tmA, &full[s], kt_s * KT + 64 * h, prow0);
+            };
+            // the first ring's weights do not depend on the previous grid:
+            // fetch them before waiting for it
+            const int pre = moe ? 0 : min(S, nst);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], SG::TX);
+                load_w(i, c0 + i * TPS);
+            }
+            if (!moe)
+                asm volatile("griddepcontrol.wait;" ::: "memory");
             int it = 0;
             bool ok = true;
             for (int pass = 0; pass < passes && ok; ++pass) {
                 const int prow0 = row0 + pass * ROWS;
                 for (int st = 0; st < nst; ++st, ++it) {
                     const int s = it % S;
+                    const int kt_s = c0 + st * TPS;
+                    if (it < pre) {  // weights already in flight
+                        load_a(s, kt_s, prow0);
+                        continue;
+                    }
                     ok = mbar_wait_bounded(&empty[s], ((it / S) & 1) ^ 1, abort, p.err, 11, kWaitLimitNs);
                     if (!ok)
                         break;
-                    const int kt_s = c0 + st * TPS;
-                    uint8_t* stage = smem + (size_t)s * SG::STAGE;
                     mbar_arrive_expect_tx(&full[s], SG::TX);
-#pragma unroll
-                    for (int h = 0; h < SG::NHALF; ++h)
-                        tma_load_2d(stage + h * SG::A_BOX, &tmA, &full[s], kt_s * KT + 64 * h, prow0);
-                    uint8_t* wdst = stage + SG::A_BYTES;
-                    tma_load_2d(wdst, &tmW, &full[s], kt_s * 64, wrow0);
-                    if constexpr (OUT == OUT_GATED)
-                        tma_load_2d(wdst + NW * TPS * kTileBytes, &tmW, &full[s], kt_s * 64, wrow1);
+                    load_a(s, kt_s, prow0);
+                    load_w(s, kt_s);
                 }
             }
             if (!ok) {
@@ -379,8 +408,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 if (lane == 0)
                     mbar_arrive(&empty[s]);
             }
-            if (ok && p.splits == 1 && active)
+            if (ok && p.splits == 1 && active) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
                 stream_epilogue<ACT, MT, OUT, GROUPED>(p, acc, blk, row0 + pass * ROWS, rows, sx, lane);
+            }
         }
         if (p.splits > 1) {
             // this CTA's partial sums for the cluster reduction, written into
@@ -425,6 +456,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             }
         }
         cluster.sync();  // members stay until the leader has read them
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
         if (cluster.block_rank() == 0 && warp < NW && !*abort) {
             int blk[2];
             bool active;
@@ -482,30 +514,42 @@ cudaError_t launch_t(const StreamParams& p, const StreamPlan& plan, int grid_y, 
     cfg.blockDim = dim3((NW + 1) * 32);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     if (plan.splits > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = plan.splits;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = plan.splits;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, ma, mw, p);
 }
 
-// plain output: decode configurations (must agree with stream_nw / stream_tps)
-template <int BITS, int ACT>
-cudaError_t launch_plain(const StreamParams& p, const StreamPlan& plan, int grid_y, cudaStream_t s)
+// plain output: decode configurations (must agree with plan_stream / stream_tps)
+template <int BITS, int ACT, int NW>
+cudaError_t launch_plain_nw(const StreamParams& p, const StreamPlan& plan, int grid_y, cudaStream_t s)
 {
     constexpr int T128 = BITS == 8 ? 4 : 2;  // tiles of 128 k
     constexpr int T64 = BITS == 8 ? 2 : 1;   // tiles of 64 k
     switch (plan.mt) {
-    case 1: return launch_t<BITS, ACT, 1, 8, OUT_PLAIN, T128>(p, plan, grid_y, s);
-    case 2: return launch_t<BITS, ACT, 2, 8, OUT_PLAIN, T128>(p, plan, grid_y, s);
-    case 4: return launch_t<BITS, ACT, 4, 8, OUT_PLAIN, T64>(p, plan, grid_y, s);
-    default: return launch_t<BITS, ACT, 8, 8, OUT_PLAIN, T64>(p, plan, grid_y, s);
+    case 1: return launch_t<BITS, ACT, 1, NW, OUT_PLAIN, T128>(p, plan, grid_y, s);
+    case 2: return launch_t<BITS, ACT, 2, NW, OUT_PLAIN, T128>(p, plan, grid_y, s);
+    case 4: return launch_t<BITS, ACT, 4, NW, OUT_PLAIN, T64>(p, plan, grid_y, s);
+    default: return launch_t<BITS, ACT, 8, NW, OUT_PLAIN, T64>(p, plan, grid_y, s);
     }
+}
+
+template <int BITS, int ACT>
+cudaError_t launch_plain(const StreamParams& p, const StreamPlan& plan, int grid_y, cudaStream_t s)
+{
+    return plan.nw == 4 ? launch_plain_nw<BITS, ACT, 4>(p, plan, grid_y, s)
+                        : launch_plain_nw<BITS, ACT, 8>(p, plan, grid_y, s);
 }
 
 constexpr int kMaxCluster = 8;
@@ -522,17 +566,30 @@ StreamPlan plan_stream(int m, int n, int k, int group, int bits, int out, int in
     StreamPlan P{};
     const int rows = m < 64 ? m : 64;
     P.mt = out != OUT_PLAIN ? 8 : rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8;
-    P.nw = stream_nw(out);
     const int tps = stream_tps(P.mt, bits, out);
     const int KT = bits == 8 ? 32 : 64;
     const int ktiles = k / KT;
     const int tpg = group / KT;
+    const int nst_all = (ktiles + tps - 1) / tps;
     const int warps_total = out == OUT_GATED ? inter / 16 : n / 32;
+    if (out != OUT_PLAIN) {
+        P.nw = 15;
+    } else {
+        // 8 consumer warps (256 channels per CTA) unless that leaves SMs idle
+        // even with the largest k split; then 4 (128 channels per CTA)
+        int cap = nst_all / 2;
+        if (cap > kMaxCluster)
+            cap = kMaxCluster;
+        if (cap < 1)
+            cap = 1;
+        const int ctas8 = (warps_total + 7) / 8 * cap;
+        P.nw = ctas8 >= num_sms() ? 8 : 4;
+    }
     P.grid_x = (warps_total + P.nw - 1) / P.nw;
     const size_t budget = out == OUT_PLAIN ? 110 * 1024 : 215 * 1024;
     const size_t stage = (size_t)stage_bytes_host(bits, P.mt, P.nw, tps);
     const size_t red = (size_t)P.nw * 2 * P.mt * 4 * 32 * 4;
-    const int nst_total = (ktiles + tps - 1) / tps;
+    const int nst_total = nst_all;
     int splits = 1;
     if (out == OUT_PLAIN) {
         // as many k splits as keep the grid within one resident wave (two

@@ -2,27 +2,35 @@
 //
 //   C[m, n] = A[m, k] . dequant(B)^T + bias[n]
 //
-// "fpAintB uses mixed-precision quantization where weights are integers but
-// are dequantized back to floating-point numbers before computation" (acext
-// User Guide 1.3.4): here the dequantisation happens tile by tile in shared
-// memory, feeding tcgen05 MMAs that accumulate in tensor memory.
+// The acext User Guide (v1.7) 1.3.4 describes fpA-intB as integer weights
+// that are turned back into floating point before the multiply: here that
+// happens per 64-wide k block on chip, right before tcgen05 MMAs that
+// accumulate in tensor memory.
 //
-// One CTA computes a 128 (m) x 256 (n) tile of C:
-//   warp 0      TMA producer: A tile (128 x 64, 128-byte swizzle) and the
-//               packed code tiles of 256 channels x 64 k into ring 1;
-//   warp 1      allocates 256 TMEM columns; one lane issues the MMAs
-//               (M=128, N=256, K=16, four per 64-wide k block) and commits
-//               them to the ring barriers;
-//   warps 4-11  dequantise ring-1 codes into ring 2: exact (q - 128) for
-//               8-bit codes, fp16 round((q - 8) * s + z) for 4-bit group
-//               codes, written with stmatrix straight into the K-major
-//               128-byte-swizzled operand layout the MMA reads;
-//   warps 4-7   after the last k block: the epilogue reads the fp32
-//               accumulator (tcgen05.ld, one TMEM lane quadrant per warp),
-//               applies scale[n] (8-bit) or the activation row scale
-//               (4-bit), adds bias, rounds once and stores C.
-// Every mbarrier wait is bounded: a wait that runs out records an error
-// word in the workspace header and the CTA winds down (see the abort path).
+// Persistent kernel: one CTA per SM walks output tiles of 128 (m) x BN (n),
+// BN = 256 (or 128 when 256-wide tiles would leave half the SMs idle), in
+// the order tile_coords gives.  Roles (16 warps):
+//   warp 0       TMA producer of the packed code tiles (BN channels x 64 k)
+//                into the code ring;
+//   warp 2       TMA producer of the A tiles (128 x 64, 128-byte swizzle)
+//                into the A ring;
+//   warp 1       allocates 2 * BN TMEM columns (two accumulators); one lane
+//                issues the MMAs (M=128, N=BN, K=16, four per k block) and
+//                commits them to the ring barriers and, at a tile's end, to
+//                the accumulator's "full" barrier;
+//   warps 4-7    epilogue: drain a finished accumulator (tcgen05.ld, one TMEM
+//                lane quadrant per warp), apply scale[n] (8-bit) or the
+//                activation row scale (4-bit), add bias, round once, store C,
+//                and hand the accumulator back -- while the MMAs already run
+//                the next tile into the other accumulator;
+//   warps 8-15   dequantisation: code ring -> registers -> exact (q - 128)
+//                for 8-bit codes or fp16 round((q - 8) * s + z) for 4-bit
+//                group codes, written with stmatrix into the operand ring in
+//                the K-major 128-byte-swizzled layout the MMA reads (4-bit
+//                scales and zeros are loaded into registers a few k blocks
+//                ahead).
+// Every mbarrier wait is bounded: a wait that runs out records an error word
+// in the workspace header and the CTA winds down (see the abort path).
 //
 // Operand types: 8-bit codes run the MMA in the activation dtype, in which
 // q - 128 is exact.  4-bit codes run it in fp16: A is first converted to
@@ -40,30 +48,35 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int kThreads = 384;       // 12 warps
-constexpr int kDequantWarp0 = 4;    // warps 4..11 dequantise
+constexpr int kThreads = 512;       // 16 warps
+constexpr int kEpilogueWarp0 = 4;   // warps 4..7
+constexpr int kDequantWarp0 = 8;    // warps 8..15
 constexpr int kDequantWarps = 8;
-constexpr int kEpilogueWarp0 = 4;   // warps 4..7 run the epilogue
-constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
-template <int BITS>
+template <int BITS, int BN>
 struct TcCfg {
-    static constexpr int S1 = BITS == 8 ? 4 : 5;                // ring-1 stages
-    static constexpr int S2 = 3;                                // ring-2 stages
-    static constexpr int A_BYTES = BM * BK * 2;                 // 16 KiB
-    static constexpr int CODE_BYTES = BN * BK * BITS / 8;       // 16 / 8 KiB
-    static constexpr int STAGE1 = A_BYTES + CODE_BYTES;
-    static constexpr int B_BYTES = BN * BK * 2;                 // 32 KiB
-    static constexpr int TILES_PER_NB = BK / Geom<BITS>::KT;    // packed tiles per 16 rows
-    static constexpr int SMEM = S1 * STAGE1 + S2 * B_BYTES;     // + barriers, see below
+    static constexpr int A_BYTES = BM * BK * 2;                  // 16 KiB
+    static constexpr int C_BYTES = BN * BK * BITS / 8;           // packed codes of a k block
+    static constexpr int B_BYTES = BN * BK * 2;                  // dequantised operand
+    static constexpr int SA = BN == 256 ? 4 : 6;                 // A ring stages
+    static constexpr int SC = (BITS == 8 ? 4 : 6) + (BN == 256 ? 0 : 2);  // code ring stages
+    static constexpr int S2 = BN == 256 ? 3 : 4;                 // operand ring stages
+    static constexpr int TPN = BK / Geom<BITS>::KT;              // packed tiles per 16 rows
+    static constexpr int NT = (BN / 16) * TPN;                   // packed tiles per k block
+    static constexpr int R = NT / kDequantWarps;                 // tiles per dequant warp
+    static constexpr int PF = 3;                                 // 4-bit scales loaded ahead
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr int SMEM = SA * A_BYTES + SC * C_BYTES + S2 * B_BYTES;  // + barriers
+    static_assert(NT % kDequantWarps == 0, "tiles per k block must split evenly");
+    static_assert(SA <= 8 && SC <= 8 && S2 <= 4, "barrier arrays");
 };
 
 struct TcParams {
     int m, n, k;
     int num_kb;              // k / BK
+    int m_tiles, n_tiles;    // output tiles along m and n
     const uint16_t* scales;  // 8-bit: [n]; 4-bit: [n, G]
     const uint16_t* zeros;   // 4-bit only, [n, G] or null
     const uint16_t* bias;    // [n] or null
@@ -71,111 +84,184 @@ struct TcParams {
     uint16_t* C;
     int G;                   // scale groups per channel row
     int group;               // codes per group
+    int vec_ok;              // scales and bias 16-byte aligned: vector loads allowed
     unsigned* err;           // workspace error word
 };
 
-// Per-stage smem: ring-1 stage s = [A tile | code tiles], ring-2 stage = B tile.
 struct Barriers {
-    uint64_t full1[8], empty1[8], full2[4], empty2[4], accum;
+    uint64_t fullA[8], emptyA[8];  // A ring (TMA -> MMA)
+    uint64_t fullC[8], emptyC[8];  // code ring (TMA -> dequant warps)
+    uint64_t full2[4], empty2[4];  // operand ring (dequant warps -> MMA)
+    uint64_t tfull[2], tempty[2];  // the two TMEM accumulators (MMA <-> epilogue)
+    uint64_t mma_done;             // every MMA issued has completed (teardown)
     uint32_t tmem_base;
     int abort;
 };
 
-template <int BITS, int OT, int ACT>
-__device__ __forceinline__ void dequant_stage(const TcParams& p, uint32_t codes_s, uint32_t b_s,
-                                              int n0, int kb, int dw, int lane)
+// Output tile `t` of the persistent walk: n fastest, so that the CTAs
+// running at the same time cover every weight column block for a few
+// consecutive m-tiles; both stay in L2 while those tiles read them.
+__device__ __forceinline__ void tile_coords(const TcParams& p, int t, int bn, int& m0, int& n0)
 {
-    constexpr int KT = Geom<BITS>::KT;
-    constexpr int KS = Geom<BITS>::KSTEPS;
-    constexpr int TPN = TcCfg<BITS>::TILES_PER_NB;
-    constexpr int NT = (BN / 16) * TPN;  // packed tiles per stage
-    const int g = lane >> 2;
-    const int mi = lane >> 3, r8 = lane & 7;
-    for (int tile = dw; tile < NT; tile += kDequantWarps) {
-        const int nb = tile / TPN;          // 16-row block within the 256-row tile
-        const int tl = tile % TPN;          // tile within the 64-wide k block
-        const uint4 v = lds128(codes_s + (uint32_t)(nb * TPN + tl) * kTileBytes + lane * 16);
-        uint32_t s2lo = 0, s2hi = 0, z2lo = 0, z2hi = 0;
-        if constexpr (BITS == 4) {
-            // scale and zero of this lane's two rows for this k block's group,
-            // as fp16 pairs (exact for values in fp16's normal range)
-            const int gi = (kb * BK) / p.group;
-            const int nlo = n0 + nb * 16 + g;
-            float slo = 0.f, shi = 0.f, zlo = 0.f, zhi = 0.f;
-            if (nlo < p.n) {
-                slo = to_f32<ACT>(ld_nc_u16(p.scales + (size_t)nlo * p.G + gi));
-                shi = to_f32<ACT>(ld_nc_u16(p.scales + (size_t)(nlo + 8) * p.G + gi));
-                if (p.zeros) {
-                    zlo = to_f32<ACT>(ld_nc_u16(p.zeros + (size_t)nlo * p.G + gi));
-                    zhi = to_f32<ACT>(ld_nc_u16(p.zeros + (size_t)(nlo + 8) * p.G + gi));
-                }
-            }
-            const uint32_t hs_lo = from_f32<ACT_F16>(slo), hs_hi = from_f32<ACT_F16>(shi);
-            const uint32_t hz_lo = from_f32<ACT_F16>(zlo), hz_hi = from_f32<ACT_F16>(zhi);
-            s2lo = hs_lo | (hs_lo << 16);
-            s2hi = hs_hi | (hs_hi << 16);
-            z2lo = hz_lo | (hz_lo << 16);
-            z2hi = hz_hi | (hz_hi << 16);
-        }
+    m0 = (t / p.n_tiles) * BM;
+    n0 = (t % p.n_tiles) * bn;
+}
+
+// 4-bit: the scale and zero bits of one dequant warp's tiles for one k block
+// (rows g and g + 8 of each tile, low and high halves), loaded a few k
+// blocks ahead of their use.
+template <int BITS, int BN>
+struct DqScales {
+    static constexpr int R = BITS == 4 ? TcCfg<BITS, BN>::R : 1;
+    uint32_t s2[R], z2[R];
+};
+
+template <int BITS, int BN>
+__device__ __forceinline__ void load_scales(const TcParams& p, int n0, int kb, int dw, int lane,
+                                            DqScales<BITS, BN>& c)
+{
+    if constexpr (BITS == 4) {
+        using Cfg = TcCfg<BITS, BN>;
+        const int g = lane >> 2;
+        const int gi = (kb * BK) / p.group;
 #pragma unroll
-        for (int s = 0; s < KS; ++s) {
-            uint32_t a[4];
-            if constexpr (BITS == 8) {
-                tile_frag<8, OT>(v, s, a);
-            } else {
-                const uint32_t w = s == 0 ? v.x : s == 1 ? v.y : s == 2 ? v.z : v.w;
-                a[0] = fma_f16x2(cvt_u4x2<ACT_F16>(w), s2lo, z2lo);
-                a[1] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 4), s2hi, z2hi);
-                a[2] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 8), s2lo, z2lo);
-                a[3] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 12), s2hi, z2hi);
+        for (int r = 0; r < Cfg::R; ++r) {
+            const int nb = (dw + kDequantWarps * r) / Cfg::TPN;
+            const int ch = n0 + nb * 16 + g;
+            c.s2[r] = 0u;
+            c.z2[r] = 0u;
+            if (ch < p.n) {  // n is a multiple of 16: row ch + 8 is in range too
+                const size_t lo = (size_t)ch * p.G + gi, hi = lo + (size_t)8 * p.G;
+                c.s2[r] = (uint32_t)ld_nc_u16(p.scales + lo) | ((uint32_t)ld_nc_u16(p.scales + hi) << 16);
+                if (p.zeros)
+                    c.z2[r] = (uint32_t)ld_nc_u16(p.zeros + lo) | ((uint32_t)ld_nc_u16(p.zeros + hi) << 16);
             }
-            // lane -> row address of matrix mi: rows r8 (+8 for mi odd), k
-            // chunk of 8 codes (+1 for mi >= 2)
-            const int row = nb * 16 + r8 + 8 * (mi & 1);
-            const int chunk = (tl * KT + 16 * s) / 8 + (mi >> 1);
-            const uint32_t addr = b_s + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
-                                  (uint32_t)((chunk ^ (row & 7)) << 4);
-            stmatrix_x4(addr, a[0], a[1], a[2], a[3]);
         }
     }
 }
 
-template <int BITS, int OT, int ACT>
+// Broadcast one 16-bit value (given in the activation dtype) as an fp16 pair.
+template <int ACT>
+__device__ __forceinline__ uint32_t f16_pair(uint32_t bits16)
+{
+    const uint32_t h = from_f32<ACT_F16>(to_f32<ACT>((uint16_t)bits16));
+    return h | (h << 16);
+}
+
+// Dequantise one warp's share of a k block: code stage at c_s -> operand
+// stage at b_s.
+template <int BITS, int OT, int ACT, int BN>
+__device__ __forceinline__ void dequant_stage(uint32_t c_s, const DqScales<BITS, BN>& sc,
+                                              uint32_t b_s, int dw, int lane)
+{
+    using Cfg = TcCfg<BITS, BN>;
+    constexpr int KT = Geom<BITS>::KT;
+    constexpr int KS = Geom<BITS>::KSTEPS;
+    const int mi = lane >> 3, r8 = lane & 7;
+    uint4 v[Cfg::R];
+#pragma unroll
+    for (int r = 0; r < Cfg::R; ++r)  // all shared loads first
+        v[r] = lds128(c_s + (uint32_t)(dw + kDequantWarps * r) * kTileBytes + lane * 16);
+#pragma unroll
+    for (int r = 0; r < Cfg::R; ++r) {
+        const int tile = dw + kDequantWarps * r;
+        const int nb = tile / Cfg::TPN, tl = tile % Cfg::TPN;
+        uint32_t slo = 0, shi = 0, zlo = 0, zhi = 0;
+        if constexpr (BITS == 4) {
+            slo = f16_pair<ACT>(sc.s2[r] & 0xFFFFu);
+            shi = f16_pair<ACT>(sc.s2[r] >> 16);
+            zlo = f16_pair<ACT>(sc.z2[r] & 0xFFFFu);
+            zhi = f16_pair<ACT>(sc.z2[r] >> 16);
+        }
+        // lane -> row address of stmatrix matrix mi: rows r8 (+8 for mi odd),
+        // 16-byte chunk of 8 codes (+1 for mi >= 2)
+        const int row = nb * 16 + r8 + 8 * (mi & 1);
+        const uint32_t row_base = b_s + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            uint32_t a[4];
+            if constexpr (BITS == 8) {
+                tile_frag<8, OT>(v[r], s, a);
+            } else {
+                const uint32_t w = s == 0 ? v[r].x : s == 1 ? v[r].y : s == 2 ? v[r].z : v[r].w;
+                a[0] = fma_f16x2(cvt_u4x2<ACT_F16>(w), slo, zlo);
+                a[1] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 4), shi, zhi);
+                a[2] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 8), slo, zlo);
+                a[3] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 12), shi, zhi);
+            }
+            const int chunk = (tl * KT + 16 * s) / 8 + (mi >> 1);
+            stmatrix_x4(row_base + (uint32_t)((chunk ^ (row & 7)) << 4), a[0], a[1], a[2], a[3]);
+        }
+    }
+}
+
+// 32 consecutive 16-bit values (p 2-byte aligned; 16-byte aligned when vec).
+__device__ __forceinline__ void load32_u16(const uint16_t* p, bool vec, uint32_t (&w)[16])
+{
+    if (vec) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p + 8 * i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = (uint32_t)p[2 * i] | ((uint32_t)p[2 * i + 1] << 16);
+    }
+}
+
+template <int BITS, int OT, int ACT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
                    const TcParams p)
 {
-    using Cfg = TcCfg<BITS>;
+    using Cfg = TcCfg<BITS, BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* ring1 = smem;
-    uint8_t* ring2 = smem + Cfg::S1 * Cfg::STAGE1;
-    Barriers* bars = reinterpret_cast<Barriers*>(ring2 + Cfg::S2 * Cfg::B_BYTES);
+    uint8_t* ringA = smem;
+    uint8_t* ring2 = ringA + Cfg::SA * Cfg::A_BYTES;
+    uint8_t* ringC = ring2 + Cfg::S2 * Cfg::B_BYTES;
+    Barriers* bars = reinterpret_cast<Barriers*>(ringC + Cfg::SC * Cfg::C_BYTES);
     volatile int* abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
     const int num_kb = p.num_kb;
+    const int total_tiles = p.m_tiles * p.n_tiles;
+    const int my_tiles =
+        (int)blockIdx.x < total_tiles ? (total_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_tiles * num_kb;  // k blocks this CTA runs, over all its tiles
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < Cfg::S1; ++s) {
-            mbar_init(&bars->full1[s], 1);
-            mbar_init(&bars->empty1[s], 1);
+        for (int s = 0; s < Cfg::SA; ++s) {
+            mbar_init(&bars->fullA[s], 1);
+            mbar_init(&bars->emptyA[s], 1);
+        }
+        for (int s = 0; s < Cfg::SC; ++s) {
+            mbar_init(&bars->fullC[s], 1);
+            mbar_init(&bars->emptyC[s], kDequantWarps);
         }
         for (int s = 0; s < Cfg::S2; ++s) {
             mbar_init(&bars->full2[s], kDequantWarps * 32);
             mbar_init(&bars->empty2[s], 1);
         }
-        mbar_init(&bars->accum, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars->tfull[a], 1);
+            mbar_init(&bars->tempty[a], 4 * 32);
+        }
+        mbar_init(&bars->mma_done, 1);
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_alloc(&bars->tmem_base, Cfg::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -183,119 +269,187 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 2) {
         if (lane == 0) {
-            // ---- TMA producer ----
-            int issued = 0;
-            for (int i = 0; i < num_kb; ++i) {
-                const int s = i % Cfg::S1;
-                if (!mbar_wait_bounded(&bars->empty1[s], ((i / Cfg::S1) & 1) ^ 1, abort, p.err, 1,
-                                       kWaitLimitNs))
-                    break;
-                uint8_t* st = ring1 + s * Cfg::STAGE1;
-                mbar_arrive_expect_tx(&bars->full1[s], Cfg::STAGE1);
-                tma_load_2d(st, &tmA, &bars->full1[s], i * BK, m0);
-                // codes: row = 16-channel block, x in 32-bit words
-                tma_load_2d(st + Cfg::A_BYTES, &tmB, &bars->full1[s], i * (BK * BITS / 8 * 16 / 4),
-                            n0 / 16);
-                issued = i + 1;
+            // ---- TMA producers: codes (warp 0) and A tiles (warp 2) ----
+            const bool codes = warp == 0;
+            const int S = codes ? Cfg::SC : Cfg::SA;
+            uint64_t* full = codes ? bars->fullC : bars->fullA;
+            uint64_t* empty = codes ? bars->emptyC : bars->emptyA;
+            int c = 0;  // k blocks issued, over all tiles
+            bool ok = true;
+            for (int it = 0; it < my_tiles && ok; ++it) {
+                int m0, n0;
+                tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, BN, m0, n0);
+                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                    const int s = c % S;
+                    if (!mbar_wait_bounded(&empty[s], ((c / S) & 1) ^ 1, abort, p.err, codes ? 1 : 9,
+                                           kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    if (codes) {
+                        mbar_arrive_expect_tx(&full[s], Cfg::C_BYTES);
+                        // one row per 16-channel block, x in 32-bit words
+                        tma_load_2d(ringC + s * Cfg::C_BYTES, &tmC, &full[s],
+                                    kb * (Cfg::C_BYTES / (BN / 16) / 4), n0 / 16);
+                    } else {
+                        mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES);
+                        tma_load_2d(ringA + s * Cfg::A_BYTES, &tmA, &full[s], kb * BK, m0);
+                    }
+                }
             }
-            if (*abort) {
+            if (!ok) {
                 // let the copies already issued land before the CTA exits
                 volatile int never = 0;
-                for (int i = issued - Cfg::S1 > 0 ? issued - Cfg::S1 : 0; i < issued; ++i)
-                    mbar_wait_bounded(&bars->full1[i % Cfg::S1], (i / Cfg::S1) & 1, &never,
-                                      nullptr, 0, kWaitLimitNs);
+                for (int i = c - S > 0 ? c - S : 0; i < c; ++i)
+                    mbar_wait_bounded(&full[i % S], (i / S) & 1, &never, nullptr, 0, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer ----
             constexpr uint32_t idesc = idesc_f16(OT == ACT_BF16 ? 1u : 0u, BM, BN);
-            for (int i = 0; i < num_kb; ++i) {
-                const int s1 = i % Cfg::S1, s2 = i % Cfg::S2;
-                if (!mbar_wait_bounded(&bars->full1[s1], (i / Cfg::S1) & 1, abort, p.err, 2,
-                                       kWaitLimitNs))
+            int c = 0;
+            bool ok = true;
+            for (int it = 0; it < my_tiles && ok; ++it) {
+                const int acc = it & 1;
+                if (!mbar_wait_bounded(&bars->tempty[acc], ((it >> 1) & 1) ^ 1, abort, p.err, 7,
+                                       kWaitLimitNs)) {
+                    ok = false;
                     break;
-                if (!mbar_wait_bounded(&bars->full2[s2], (i / Cfg::S2) & 1, abort, p.err, 3,
-                                       kWaitLimitNs))
-                    break;
+                }
                 tc_fence_after();
-                const uint32_t a_s = smem_addr(ring1 + s1 * Cfg::STAGE1);
-                const uint32_t b_s = smem_addr(ring2 + s2 * Cfg::B_BYTES);
-                const uint64_t ad = desc_sw128(a_s), bd = desc_sw128(b_s);
+                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                    const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
+                    if (!mbar_wait_bounded(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 2,
+                                           kWaitLimitNs) ||
+                        !mbar_wait_bounded(&bars->full2[s2], (c / Cfg::S2) & 1, abort, p.err, 3,
+                                           kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(smem_addr(ringA + sa * Cfg::A_BYTES));
+                    const uint64_t bd = desc_sw128(smem_addr(ring2 + s2 * Cfg::B_BYTES));
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j)  // +32 bytes per 16-wide k step
-                    mma_f16(tmem, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc,
-                            (i > 0 || j > 0) ? 1u : 0u);
-                mma_commit(&bars->empty1[s1]);
-                mma_commit(&bars->empty2[s2]);
+                    for (int j = 0; j < BK / 16; ++j)  // +32 bytes per 16-wide k step
+                        mma_f16(d, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc,
+                                (kb > 0 || j > 0) ? 1u : 0u);
+                    mma_commit(&bars->emptyA[sa]);
+                    mma_commit(&bars->empty2[s2]);
+                }
+                if (ok)
+                    mma_commit(&bars->tfull[acc]);
             }
-            // accumulator complete (also on abort, so the epilogue and the
-            // TMEM release wait for every MMA already issued)
-            mma_commit(&bars->accum);
+            // every MMA issued must finish before TMEM is released (also on abort)
+            mma_commit(&bars->mma_done);
+            volatile int never = 0;
+            mbar_wait_bounded(&bars->mma_done, 0, &never, p.err, 8, kWaitLimitNs);
         }
-    } else if (warp >= kDequantWarp0) {
-        // ---- dequantisation ----
-        const int dw = warp - kDequantWarp0;
-        for (int i = 0; i < num_kb; ++i) {
-            const int s1 = i % Cfg::S1, s2 = i % Cfg::S2;
-            // warp-uniform decisions: stmatrix below needs the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars->full1[s1], (i / Cfg::S1) & 1,
-                                                           abort, p.err, 4, kWaitLimitNs)))
+        __syncwarp();
+    } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+        // ---- epilogue: TMEM lane quadrant q = warp % 4 ----
+        const int q = warp - kEpilogueWarp0;
+        for (int it = 0; it < my_tiles; ++it) {
+            const int acc = it & 1;
+            int m0, n0;
+            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, BN, m0, n0);
+            const bool ok = mbar_wait_bounded(&bars->tfull[acc], (it >> 1) & 1, abort, p.err, 6,
+                                              kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ok && !*abort))  // tcgen05.ld needs the whole warp
                 break;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait_bounded(&bars->empty2[s2], ((i / Cfg::S2) & 1) ^ 1, abort,
-                                              p.err, 5, kWaitLimitNs)))
-                break;
-            dequant_stage<BITS, OT, ACT>(p, smem_addr(ring1 + s1 * Cfg::STAGE1 + Cfg::A_BYTES),
-                                         smem_addr(ring2 + s2 * Cfg::B_BYTES), n0, i, dw, lane);
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->full2[s2]);
-        }
-        // ---- epilogue ----
-        if (warp < kEpilogueWarp0 + 4) {
-            const int q = warp - kEpilogueWarp0;  // TMEM lane quadrant
-            bool ok = mbar_wait_bounded(&bars->accum, 0, abort, p.err, 6, kWaitLimitNs);
-            ok = __all_sync(0xffffffffu, ok && !*abort);  // tcgen05.ld needs the whole warp
             tc_fence_after();
             const int row = m0 + q * 32 + lane;
             float rs = 1.f;
             if (p.rowscale && row < p.m)
                 rs = p.rowscale[row];
-            if (ok) {
-                for (int c = 0; c < BN / 32; ++c) {
-                    const int nc = n0 + c * 32;
-                    if (nc >= p.n)
-                        break;
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-                    tmem_ld_wait();
-                    if (row < p.m) {
-                        uint32_t packed[16];
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                const int nc = n0 + cc * 32;
+                if (nc >= p.n)
+                    break;
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + cc * 32), r);
+                uint32_t sc[16], bi[16];
+                if constexpr (BITS == 8)
+                    load32_u16(p.scales + nc, p.vec_ok != 0, sc);
+                if (p.bias)
+                    load32_u16(p.bias + nc, p.vec_ok != 0, bi);
+                tmem_ld_wait();
+                if (row < p.m) {
+                    uint32_t packed[16];
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
-                            if constexpr (BITS == 8) {
-                                v0 *= to_f32<ACT>(ld_nc_u16(p.scales + nc + j));
-                                v1 *= to_f32<ACT>(ld_nc_u16(p.scales + nc + j + 1));
-                            } else {
-                                v0 *= rs;
-                                v1 *= rs;
-                            }
-                            if (p.bias) {
-                                v0 += to_f32<ACT>(ld_nc_u16(p.bias + nc + j));
-                                v1 += to_f32<ACT>(ld_nc_u16(p.bias + nc + j + 1));
-                            }
-                            packed[j / 2] = (uint32_t)from_f32<ACT>(v0) |
-                                            ((uint32_t)from_f32<ACT>(v1) << 16);
+                    for (int j = 0; j < 16; ++j) {
+                        float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
+                        if constexpr (BITS == 8) {
+                            v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
+                            v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
+                        } else {
+                            v0 *= rs;
+                            v1 *= rs;
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.n + nc);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                                packed[4 * v + 3]);
+                        if (p.bias) {
+                            v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
+                            v1 += to_f32<ACT>((uint16_t)(bi[j] >> 16));
+                        }
+                        packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
                     }
+                    uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.n + nc);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                            packed[4 * v + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->tempty[acc]);
+        }
+    } else if (warp >= kDequantWarp0) {
+        // ---- dequantisation ----
+        const int dw = warp - kDequantWarp0;
+        auto n0_of = [&](int c) {
+            const int it = c / num_kb;
+            int m0, n0;
+            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, BN, m0, n0);
+            return n0;
+        };
+        DqScales<BITS, BN> buf[Cfg::PF];
+        if constexpr (BITS == 4) {
+#pragma unroll
+            for (int j = 0; j < Cfg::PF; ++j)
+                if (j < total)
+                    load_scales<BITS, BN>(p, n0_of(j), j % num_kb, dw, lane, buf[j]);
+        }
+        bool ok = true;
+        for (int c0 = 0; c0 < total && ok; c0 += Cfg::PF) {
+#pragma unroll
+            for (int j = 0; j < Cfg::PF; ++j) {
+                const int c = c0 + j;
+                if (c >= total)
+                    break;
+                const int sc = c % Cfg::SC, s2 = c % Cfg::S2;
+                // warp-uniform decisions: stmatrix below needs the whole warp
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(&bars->fullC[sc], (c / Cfg::SC) & 1, abort, p.err,
+                                                  4, kWaitLimitNs) &&
+                                    mbar_wait_bounded(&bars->empty2[s2], ((c / Cfg::S2) & 1) ^ 1,
+                                                      abort, p.err, 5, kWaitLimitNs))) {
+                    ok = false;
+                    break;
+                }
+                dequant_stage<BITS, OT, ACT, BN>(smem_addr(ringC + sc * Cfg::C_BYTES), buf[j],
+                                                 smem_addr(ring2 + s2 * Cfg::B_BYTES), dw, lane);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->full2[s2]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->emptyC[sc]);
+                if constexpr (BITS == 4) {
+                    if (c + Cfg::PF < total)
+                        load_scales<BITS, BN>(p, n0_of(c + Cfg::PF), (c + Cfg::PF) % num_kb, dw,
+                                              lane, buf[j]);
                 }
             }
         }
@@ -305,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, Cfg::TMEM_COLS);
     }
 }
 
@@ -351,18 +505,40 @@ __global__ void a_to_f16_kernel(const uint16_t* __restrict__ A, uint16_t* __rest
         rowscale[row] = ldexpf(1.f, E);
 }
 
-template <int BITS, int OT, int ACT>
-cudaError_t launch_tc_t(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& tp,
-                        cudaStream_t s)
+// Tile width: 256, or 128 when 256-wide tiles would fill at most half the SMs.
+int tc_bn(int m, int n)
 {
-    constexpr int smem = TcCfg<BITS>::SMEM + (int)sizeof(Barriers) + 1024;
-    auto kern = gemm_tc_kernel<BITS, OT, ACT>;
+    const long long tiles256 = (long long)((m + BM - 1) / BM) * ((n + 255) / 256);
+    return 2 * tiles256 <= num_sms() ? 128 : 256;
+}
+
+template <int BITS, int OT, int ACT, int BN>
+cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaStream_t s)
+{
+    constexpr int smem = TcCfg<BITS, BN>::SMEM + (int)sizeof(Barriers) + 1024;
+    auto kern = gemm_tc_kernel<BITS, OT, ACT, BN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
-    const dim3 grid((tp.n + BN - 1) / BN, (tp.m + BM - 1) / BM);
-    kern<<<grid, kThreads, smem, s>>>(ma, mb, tp);
+    tp.n_tiles = (tp.n + BN - 1) / BN;
+    const long long tiles = (long long)tp.m_tiles * tp.n_tiles;
+    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+    // packed codes viewed as [n/16 rows] x [bytes per 16-channel row / 4] words;
+    // one box = BN/16 rows x one k block
+    CUtensorMap mc;
+    const uint64_t row_bytes = (uint64_t)tp.k * 16 * BITS / 8;
+    if (!make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, B, row_bytes / 4, (uint64_t)tp.n / 16,
+                      row_bytes, BK * 16 * BITS / 8 / 4, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    kern<<<grid, kThreads, smem, s>>>(ma, mc, tp);
     return cudaGetLastError();
+}
+
+template <int BITS, int OT, int ACT>
+cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& tp, cudaStream_t s)
+{
+    return tc_bn(tp.m, tp.n) == 128 ? launch_tc_t<BITS, OT, ACT, 128>(ma, B, tp, s)
+                                    : launch_tc_t<BITS, OT, ACT, 256>(ma, B, tp, s);
 }
 
 }  // namespace
@@ -384,12 +560,15 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     tp.n = a.n;
     tp.k = a.k;
     tp.num_kb = a.k / BK;
+    tp.m_tiles = (a.m + BM - 1) / BM;
     tp.scales = static_cast<const uint16_t*>(a.scales);
     tp.zeros = static_cast<const uint16_t*>(a.zeros);
     tp.bias = static_cast<const uint16_t*>(a.bias);
     tp.C = static_cast<uint16_t*>(a.C);
     tp.G = a.k / a.group;
     tp.group = a.group;
+    tp.vec_ok = (reinterpret_cast<uintptr_t>(a.scales) % 16 == 0) &&
+                (reinterpret_cast<uintptr_t>(a.bias) % 16 == 0);
     tp.err = reinterpret_cast<unsigned*>(ws);
 
     const void* Aop = a.A;
@@ -404,21 +583,16 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
         tp.rowscale = rsc;
     }
     const int OT = a.bits == 4 ? WO_F16 : a.act;
-    CUtensorMap ma, mb;
+    CUtensorMap ma;
     if (!make_tmap_2d(&ma, OT == WO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                  Aop, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2, BK, BM,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    // packed codes viewed as [n/16 rows] x [bytes per 16-channel row / 4] words
-    const uint64_t row_bytes = (uint64_t)a.k * 16 * a.bits / 8;
-    if (!make_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.B, row_bytes / 4, (uint64_t)a.n / 16,
-                  row_bytes, BK * 16 * a.bits / 8 / 4, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+                      Aop, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2, BK, BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (a.bits == 8)
-        return a.act == WO_F16 ? launch_tc_t<8, ACT_F16, ACT_F16>(ma, mb, tp, s)
-                               : launch_tc_t<8, ACT_BF16, ACT_BF16>(ma, mb, tp, s);
-    return a.act == WO_F16 ? launch_tc_t<4, ACT_F16, ACT_F16>(ma, mb, tp, s)
-                           : launch_tc_t<4, ACT_F16, ACT_BF16>(ma, mb, tp, s);
+        return a.act == WO_F16 ? launch_tc_bn<8, ACT_F16, ACT_F16>(ma, a.B, tp, s)
+                               : launch_tc_bn<8, ACT_BF16, ACT_BF16>(ma, a.B, tp, s);
+    return a.act == WO_F16 ? launch_tc_bn<4, ACT_F16, ACT_F16>(ma, a.B, tp, s)
+                           : launch_tc_bn<4, ACT_F16, ACT_BF16>(ma, a.B, tp, s);
 }
 
 }  // namespace wo

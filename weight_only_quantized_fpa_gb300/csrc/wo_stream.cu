@@ -165,6 +165,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     constexpr int KS = Geom<BITS>::KSTEPS;
     constexpr bool GROUPED = BITS == 4;
     constexpr int ROWS = SG::ROWS;
+    constexpr int NV = 2 * MT * 4;  // accumulator values per lane
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled activation boxes
@@ -418,61 +419,75 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             // the ring once every consumer warp is done reading it
             asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
             if (active) {
-                float* red = reinterpret_cast<float*>(smem);
+                // lane-contiguous: lane L of warp w owns values [(32 w + L) * NV, + NV)
+                float4* dst = reinterpret_cast<float4*>(smem) + (size_t)(warp * 32 + lane) * (NV / 4);
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
 #pragma unroll
                     for (int j = 0; j < MT; ++j)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            red[(((warp * 2 + r) * MT + j) * 4 + q) * 32 + lane] = ok ? acc[r][j][q] : 0.f;
+                        dst[r * MT + j] = ok ? make_float4(acc[r][j][0], acc[r][j][1], acc[r][j][2], acc[r][j][3])
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
     }
 
     if (p.splits > 1) {
-        // ---- k split across the cluster: the leader sums in rank order ----
+        // ---- k split across the cluster: rank r finishes the consumer warps
+        // w with w % splits == r, summing every rank's partials in rank order ----
         __syncthreads();
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
-        float* red = reinterpret_cast<float*>(smem);
-        const int nred = NW * 2 * MT * 4 * 32;
-        if (cluster.block_rank() == 0) {
-            float* rp[8];
-#pragma unroll
-            for (int rk = 1; rk < 8; ++rk)
-                rp[rk] = rk < p.splits ? cluster.map_shared_rank(red, rk) : red;
-            for (int idx = threadIdx.x; idx < nred; idx += blockDim.x) {
-                float vals[8];
-#pragma unroll
-                for (int rk = 1; rk < 8; ++rk)
-                    vals[rk] = rk < p.splits ? rp[rk][idx] : 0.f;
-                float v = red[idx];
-#pragma unroll
-                for (int rk = 1; rk < 8; ++rk)
-                    if (rk < p.splits)
-                        v += vals[rk];
-                red[idx] = v;
-            }
-        }
-        cluster.sync();  // members stay until the leader has read them
-        asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
-        if (cluster.block_rank() == 0 && warp < NW && !*abort) {
+        const int rank = (int)cluster.block_rank();
+        if (warp < NW && warp % p.splits == rank && !*abort) {
             int blk[2];
             bool active;
             warp_blocks<OUT>(p, blockIdx.x * NW + warp, blk, active);
             if (active) {
+                float* red = reinterpret_cast<float*>(smem);
+                const size_t off = (size_t)(warp * 32 + lane) * NV;
+                float4 sum[NV / 4];
+#pragma unroll
+                for (int v = 0; v < NV / 4; ++v)
+                    sum[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                // RC ranks' loads in flight at once, then their sums in order
+                constexpr int RC = MT >= 4 ? 1 : 4 / MT;
+                for (int r0 = 0; r0 < p.splits; r0 += RC) {
+                    float4 vals[RC][NV / 4];
+#pragma unroll
+                    for (int u = 0; u < RC; ++u)
+                        if (r0 + u < p.splits) {
+                            const float4* src =
+                                reinterpret_cast<const float4*>(cluster.map_shared_rank(red, r0 + u) + off);
+#pragma unroll
+                            for (int v = 0; v < NV / 4; ++v)
+                                vals[u][v] = src[v];
+                        }
+#pragma unroll
+                    for (int u = 0; u < RC; ++u)
+                        if (r0 + u < p.splits)
+#pragma unroll
+                            for (int v = 0; v < NV / 4; ++v) {
+                                sum[v].x += vals[u][v].x;
+                                sum[v].y += vals[u][v].y;
+                                sum[v].z += vals[u][v].z;
+                                sum[v].w += vals[u][v].w;
+                            }
+                }
                 float acc[2][MT][4];
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
 #pragma unroll
-                    for (int j = 0; j < MT; ++j)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            acc[r][j][q] = red[(((warp * 2 + r) * MT + j) * 4 + q) * 32 + lane];
+                    for (int j = 0; j < MT; ++j) {
+                        acc[r][j][0] = sum[r * MT + j].x;
+                        acc[r][j][1] = sum[r * MT + j].y;
+                        acc[r][j][2] = sum[r * MT + j].z;
+                        acc[r][j][3] = sum[r * MT + j].w;
+                    }
+                asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
                 stream_epilogue<ACT, MT, OUT, GROUPED>(p, acc, blk, row0, min(ROWS, rows_total), sx, lane);
             }
         }
+        cluster.sync();  // every rank stays until the others have read its partials
     }
 }
 

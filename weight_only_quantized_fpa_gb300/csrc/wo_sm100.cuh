@@ -58,19 +58,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// The same try_wait with acquire semantics at cluster scope: the waiter
+// sees every write that arrivals from other CTAs of the cluster released.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete, giving up after `limit_ns`
 // (or at once when another thread of the CTA has already given up, seen
 // through *abort).  Returns false when it gave up; the first thread to give
-// up records `code` in *err and raises *abort.
+// up records `code` in *err and raises *abort.  CLUSTER selects the
+// cluster-scope acquire.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned* err,
                                                   unsigned code, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity))
+    auto try_wait = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_wait())
         return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+        if (try_wait())
             return true;
         if ((it & 63u) == 0) {
             if (*abort)
@@ -83,6 +101,43 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             }
         }
     }
+}
+
+// ------------------------------------------------------------- cluster ----
+
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// Arrive on an mbarrier of a cluster CTA, releasing this thread's earlier
+// writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+                 : "memory");
+}
+
+// Split cluster barrier: every thread arrives once (warp-converged), and a
+// thread that will touch another CTA's shared memory waits first.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ TMA ----

@@ -27,12 +27,18 @@
 //     at each group end, so the tensor cores only see exact integers; 8-bit
 //     per-channel weights (1.3.1) apply scale[n] once at the end;
 //   - when k is long for the number of channels, the k range is split across
-//     a thread-block cluster of up to 8 CTAs and the leader sums the
-//     members' accumulators through distributed shared memory in rank order.
+//     a thread-block cluster of up to 8 CTAs: each consumer warp pushes its
+//     partial sums into a slot in the shared memory of the rank that owns its
+//     channels (rank = warp % splits) and arrives on that rank's mbarrier;
+//     the owner sums the slots in rank order and writes the outputs.  A CTA
+//     leaves as soon as its pushes are out and its own channels are done.
+//   - 8-bit decode rows (m <= 16) accumulate even and odd k-steps in two sets
+//     (summed at the end), two independent mma chains per channel block.
 //   - launched with programmatic dependent launch: the producer fetches the
-//     first stages' weights before waiting for the previous grid, and every
-//     read of activations or routing data and every output write comes after
-//     that wait.
+//     weights of the first stages (for decode, of the CTA's whole k range)
+//     and the consumers their channels' scales and bias before waiting for
+//     the previous grid; every read of activations or routing data and every
+//     output write comes after that wait.
 // Every sum has a fixed order: the result is bit-for-bit repeatable.  Every
 // mbarrier wait is bounded; a wait that runs out records an error word and
 // the CTA winds down (the producer first lets its copies in flight land).
@@ -113,12 +119,37 @@ __device__ __forceinline__ void warp_blocks(const StreamParams& p, int v, int (&
     }
 }
 
+// Scale (8-bit) and bias of the plain output's four channels per lane,
+// blk[r] * 16 + g + 8 h.  They are inputs, so the CTA reads them at its
+// start, before waiting for the previous grid, and their load latency stays
+// off the end of the kernel.
+struct PlainEpi {
+    float s[2][2], b[2][2];
+};
+
+template <int ACT, bool GROUPED>
+__device__ __forceinline__ PlainEpi load_plain_epi(const StreamParams& p, const int (&blk)[2],
+                                                   const uint16_t* sx, int lane)
+{
+    PlainEpi e;
+    const int g = lane >> 2;
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int ch = blk[r] * 16 + g + 8 * h;
+            e.s[r][h] = GROUPED ? 1.f : to_f32<ACT>(ld_nc_u16(sx + ch));
+            e.b[r][h] = p.bias ? to_f32<ACT>(ld_nc_u16(p.bias + ch)) : 0.f;
+        }
+    return e;
+}
+
 // Output of one warp's accumulators: element q of (r, j) is channel
 // blk[r] * 16 + g + 8 (q >> 1), row 8 j + 2 t + (q & 1) of the pass.
 template <int ACT, int MT, int OUT, bool GROUPED>
 __device__ __forceinline__ void stream_epilogue(const StreamParams& p, const float (&acc)[2][MT][4],
                                                 const int (&blk)[2], int prow0, int rows,
-                                                const uint16_t* sx, int lane)
+                                                const uint16_t* sx, const PlainEpi& pe, int lane)
 {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -140,13 +171,15 @@ __device__ __forceinline__ void stream_epilogue(const StreamParams& p, const flo
                 for (int r = 0; r < 2; ++r) {
                     const int ch = blk[r] * 16 + g + 8 * (q >> 1);
                     float v = acc[r][j][q];
-                    if constexpr (!GROUPED)
-                        v *= to_f32<ACT>(ld_nc_u16(sx + ch));
                     if constexpr (OUT == OUT_PLAIN) {
+                        if constexpr (!GROUPED)
+                            v *= pe.s[r][q >> 1];
                         if (p.bias)
-                            v += to_f32<ACT>(ld_nc_u16(p.bias + ch));
+                            v += pe.b[r][q >> 1];
                         p.C[row * p.N + ch] = from_f32<ACT>(v);
                     } else {
+                        if constexpr (!GROUPED)
+                            v *= to_f32<ACT>(ld_nc_u16(sx + ch));
                         p.Y[row * p.N + ch] = v;
                     }
                 }
@@ -166,15 +199,25 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     constexpr bool GROUPED = BITS == 4;
     constexpr int ROWS = SG::ROWS;
     constexpr int NV = 2 * MT * 4;  // accumulator values per lane
+    // decode rows (m <= 16): split each block's mma chain over even / odd k-steps
+    constexpr bool DUAL = !GROUPED && OUT == OUT_PLAIN && MT <= 2;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled activation boxes
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * SG::STAGE);
+    // k split across the cluster: rank r finishes the consumer warps w with
+    // w % splits == r.  pbuf holds, per such warp, one slot per rank that the
+    // ranks push their partial sums into; redbar counts the pushes.
+    const int splits = p.splits;
+    const int fin_warps = (NW + splits - 1) / splits;  // warps a rank finishes, at most
+    float* pbuf = reinterpret_cast<float*>(smem + (size_t)S * SG::STAGE);
+    const size_t pbuf_floats = splits > 1 ? (size_t)fin_warps * splits * 32 * NV : 0;
+    uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + pbuf_floats);
     uint64_t* empty = full + S;
-    int* abort_flag = reinterpret_cast<int*>(empty + S);
+    uint64_t* redbar = empty + S;
+    int* abort_flag = reinterpret_cast<int*>(redbar + 1);
     uint16_t* s_sm = reinterpret_cast<uint16_t*>(abort_flag + 4);
     volatile int* abort = abort_flag;
 
@@ -199,20 +242,36 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     const int passes = (rows_total + ROWS - 1) / ROWS;
     const uint16_t* sx = p.scales + (size_t)e * p.s_stride;
 
+    // consumer warps of this CTA whose pushes this rank receives
+    const int rank = splits > 1 ? (int)cg::this_cluster().block_rank() : 0;
+    int fin_active = 0;
+    if (splits > 1)
+        for (int w = rank; w < NW; w += splits) {
+            int b_[2];
+            bool act_;
+            warp_blocks<OUT>(p, blockIdx.x * NW + w, b_, act_);
+            fin_active += act_ ? 1 : 0;
+        }
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], NW);
         }
+        if (fin_active > 0)
+            mbar_init(redbar, (uint32_t)(fin_active * splits * 32));
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmW);
     }
     __syncthreads();
+    if (splits > 1)
+        cluster_arrive_relaxed();  // barrier inits visible cluster-wide before any push
     if (p.splits == 1 && (rows_total <= 0 || nst <= 0))
         return;  // a whole CTA with nothing to do (an expert without rows)
 
+    PlainEpi pe{};  // consumer lanes: their channels' scale and bias
     if (warp == NW) {
         // ================= producer (one thread) =================
         if (lane == 0) {
@@ -272,6 +331,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         int blk[2];
         bool active;
         warp_blocks<OUT>(p, blockIdx.x * NW + warp, blk, active);
+        if (OUT == OUT_PLAIN && active)
+            pe = load_plain_epi<ACT, GROUPED>(p, blk, sx, lane);
         // 4-bit: this warp's 32 channels' scales and zeros over its k range
         uint16_t* ws_s = s_sm + (size_t)warp * 2 * 32 * p.g_span;
         uint16_t* ws_z = ws_s + 32 * p.g_span;
@@ -367,8 +428,12 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                                         const uint32_t ones[4] = {one, one, one, one};
                                         mma16816<ACT>(rs[j], ones, b[j][0], b[j][1]);
                                     } else {
-                                        mma16816<ACT>(acc[0][j], a0, b[j][0], b[j][1]);
-                                        mma16816<ACT>(acc[1][j], a1, b[j][0], b[j][1]);
+                                        // DUAL: odd k-steps into a second set (gp), so
+                                        // two independent mma chains per block
+                                        float (&d0)[4] = (DUAL && (ks & 1)) ? gp[0][j] : acc[0][j];
+                                        float (&d1)[4] = (DUAL && (ks & 1)) ? gp[1][j] : acc[1][j];
+                                        mma16816<ACT>(d0, a0, b[j][0], b[j][1]);
+                                        mma16816<ACT>(d1, a1, b[j][0], b[j][1]);
                                     }
                                 }
                             }
@@ -409,85 +474,77 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 if (lane == 0)
                     mbar_arrive(&empty[s]);
             }
-            if (ok && p.splits == 1 && active) {
-                asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
-                stream_epilogue<ACT, MT, OUT, GROUPED>(p, acc, blk, row0 + pass * ROWS, rows, sx, lane);
-            }
-        }
-        if (p.splits > 1) {
-            // this CTA's partial sums for the cluster reduction, written into
-            // the ring once every consumer warp is done reading it
-            asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
-            if (active) {
-                // lane-contiguous: lane L of warp w owns values [(32 w + L) * NV, + NV)
-                float4* dst = reinterpret_cast<float4*>(smem) + (size_t)(warp * 32 + lane) * (NV / 4);
+            if constexpr (DUAL) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
 #pragma unroll
                     for (int j = 0; j < MT; ++j)
-                        dst[r * MT + j] = ok ? make_float4(acc[r][j][0], acc[r][j][1], acc[r][j][2], acc[r][j][3])
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            acc[r][j][q] += gp[r][j][q];
             }
-        }
-    }
-
-    if (p.splits > 1) {
-        // ---- k split across the cluster: rank r finishes the consumer warps
-        // w with w % splits == r, summing every rank's partials in rank order ----
-        __syncthreads();
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        const int rank = (int)cluster.block_rank();
-        if (warp < NW && warp % p.splits == rank && !*abort) {
-            int blk[2];
-            bool active;
-            warp_blocks<OUT>(p, blockIdx.x * NW + warp, blk, active);
-            if (active) {
-                float* red = reinterpret_cast<float*>(smem);
-                const size_t off = (size_t)(warp * 32 + lane) * NV;
-                float4 sum[NV / 4];
-#pragma unroll
-                for (int v = 0; v < NV / 4; ++v)
-                    sum[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-                // RC ranks' loads in flight at once, then their sums in order
-                constexpr int RC = MT >= 4 ? 1 : 4 / MT;
-                for (int r0 = 0; r0 < p.splits; r0 += RC) {
-                    float4 vals[RC][NV / 4];
-#pragma unroll
-                    for (int u = 0; u < RC; ++u)
-                        if (r0 + u < p.splits) {
-                            const float4* src =
-                                reinterpret_cast<const float4*>(cluster.map_shared_rank(red, r0 + u) + off);
-#pragma unroll
-                            for (int v = 0; v < NV / 4; ++v)
-                                vals[u][v] = src[v];
-                        }
-#pragma unroll
-                    for (int u = 0; u < RC; ++u)
-                        if (r0 + u < p.splits)
-#pragma unroll
-                            for (int v = 0; v < NV / 4; ++v) {
-                                sum[v].x += vals[u][v].x;
-                                sum[v].y += vals[u][v].y;
-                                sum[v].z += vals[u][v].z;
-                                sum[v].w += vals[u][v].w;
-                            }
-                }
-                float acc[2][MT][4];
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-#pragma unroll
-                    for (int j = 0; j < MT; ++j) {
-                        acc[r][j][0] = sum[r * MT + j].x;
-                        acc[r][j][1] = sum[r * MT + j].y;
-                        acc[r][j][2] = sum[r * MT + j].z;
-                        acc[r][j][3] = sum[r * MT + j].w;
-                    }
+            if (ok && p.splits == 1 && active) {
                 asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
-                stream_epilogue<ACT, MT, OUT, GROUPED>(p, acc, blk, row0, min(ROWS, rows_total), sx, lane);
+                stream_epilogue<ACT, MT, OUT, GROUPED>(p, acc, blk, row0 + pass * ROWS, rows, sx, pe, lane);
             }
         }
-        cluster.sync();  // every rank stays until the others have read its partials
+        if (splits > 1 && active) {
+            // push this warp's partial sums into slot (w / splits, rank) of
+            // rank w % splits, then arrive there (zeros if the loop gave up)
+            cluster_wait();
+            const uint32_t dst_rank = (uint32_t)(warp % splits);
+            const int slot = (warp / splits) * splits + rank;
+            const uint32_t dst =
+                mapa_shared(smem_addr(pbuf + ((size_t)slot * 32 + lane) * NV), dst_rank);
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int j = 0; j < MT; ++j)
+                    st_cluster_v4(dst + (uint32_t)((r * MT + j) * 16),
+                                  ok ? make_float4(acc[r][j][0], acc[r][j][1], acc[r][j][2], acc[r][j][3])
+                                     : make_float4(0.f, 0.f, 0.f, 0.f));
+            mbar_arrive_cluster(mapa_shared(smem_addr(redbar), dst_rank));
+
+            if (warp % splits == rank) {
+                // finish this warp's channels: every rank's partials, in rank order
+                // waits for every push even after an abort elsewhere, so that no rank
+                // writes into this CTA's shared memory after it has exited
+                volatile int never = 0;
+                const bool got = __all_sync(0xffffffffu, mbar_wait_bounded<true>(redbar, 0, &never, p.err,
+                                                                                13, kWaitLimitNs)) &&
+                                 !*abort;
+                if (got) {
+                    const float4* src = reinterpret_cast<const float4*>(pbuf) +
+                                        ((size_t)(warp / splits) * splits * 32 + lane) * (NV / 4);
+                    float4 sum[NV / 4];
+#pragma unroll
+                    for (int v = 0; v < NV / 4; ++v)
+                        sum[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int rk = 0; rk < splits; ++rk) {
+#pragma unroll
+                        for (int v = 0; v < NV / 4; ++v) {
+                            const float4 x = src[(size_t)rk * 32 * (NV / 4) + v];
+                            sum[v].x += x.x;
+                            sum[v].y += x.y;
+                            sum[v].z += x.z;
+                            sum[v].w += x.w;
+                        }
+                    }
+                    float fin[2][MT][4];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int j = 0; j < MT; ++j) {
+                            fin[r][j][0] = sum[r * MT + j].x;
+                            fin[r][j][1] = sum[r * MT + j].y;
+                            fin[r][j][2] = sum[r * MT + j].z;
+                            fin[r][j][3] = sum[r * MT + j].w;
+                        }
+                    asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
+                    stream_epilogue<ACT, MT, OUT, GROUPED>(p, fin, blk, row0, min(ROWS, rows_total), sx, pe, lane);
+                }
+            }
+        }
     }
 }
 
@@ -603,7 +660,6 @@ StreamPlan plan_stream(int m, int n, int k, int group, int bits, int out, int in
     P.grid_x = (warps_total + P.nw - 1) / P.nw;
     const size_t budget = out == OUT_PLAIN ? 110 * 1024 : 215 * 1024;
     const size_t stage = (size_t)stage_bytes_host(bits, P.mt, P.nw, tps);
-    const size_t red = (size_t)P.nw * 2 * P.mt * 4 * 32 * 4;
     const int nst_total = nst_all;
     int splits = 1;
     if (out == OUT_PLAIN) {
@@ -620,22 +676,29 @@ StreamPlan plan_stream(int m, int n, int k, int group, int bits, int out, int in
     }
     for (; splits <= kMaxCluster; ++splits) {
         const int kps = (nst_total + splits - 1) / splits * tps;  // whole stages
+        const int nsplit = (ktiles + kps - 1) / kps;                 // CTAs along k
         const int gspan = bits == 4 ? (kps + tpg - 1) / tpg + 1 : 0;
         const size_t sz = (size_t)P.nw * 2 * 32 * gspan * 2;
-        const size_t fixed = 1024 + sz + 16 + 2 * 8 * 8 + 128;
+        // push buffer of the cluster reduction (see stream_kernel)
+        const size_t pb = nsplit > 1 ? (size_t)((P.nw + nsplit - 1) / nsplit) * nsplit * 32 * (8 * P.mt) * 4 : 0;
+        const size_t fixed = 1024 + pb + sz + 16 + 2 * 8 * 8 + 8 + 128;
         if (fixed + 2 * stage > budget)
             continue;  // not even two stages fit: split k further
         int stages = (int)((budget - fixed) / stage);
         if (stages > 8)
             stages = 8;
-        if ((size_t)stages * stage < red)
-            continue;
-        P.splits = (ktiles + kps - 1) / kps;
+        if (out == OUT_PLAIN && stages > kps / tps) {
+            // no more stages than the CTA's k range has (every weight is then
+            // fetched before the wait for the previous grid), keeping shared
+            // memory free for the next grid's CTAs
+            stages = kps / tps;
+        }
+        P.splits = nsplit;
         P.kt_per_split = kps;
         P.stages = stages;
         P.g_span = gspan;
         P.tps = tps;
-        P.smem = 1024 + (size_t)stages * stage + 2 * 8 * (size_t)stages + 16 + sz;
+        P.smem = 1024 + (size_t)stages * stage + pb + 2 * 8 * (size_t)stages + 8 + 16 + sz;
         P.valid = out == OUT_PLAIN || P.splits == 1;
         return P;
     }

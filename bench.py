@@ -655,7 +655,10 @@ def run_ours(args, ws, rank, local):
         sh = None
     tr = traffic_from_profile(kname, sh) if sh else None
     roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
-    roof["algorithmic_bytes_per_launch"] = bytes_per_step / ncase
+    if w["unit"] == "GB/s":
+        roof["algorithmic_bytes_per_launch"] = bytes_per_step / ncase
+    else:
+        roof["algorithmic_flops_per_launch"] = flops_per_step / ncase
     roof["kernel"] = kname
     roof["timing"] = (f"{ncase} launches per step back to back in one CUDA graph; achieved = "
                       "algorithmic bytes (or flops) per step / step time")

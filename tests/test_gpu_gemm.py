@@ -65,6 +65,9 @@ SMALL = [
     (96, 128, 512, 4, -1, inputs.BF16, True, True),     # per-channel 4-bit, tensor cores
     (80, 256, 1024, 4, 128, inputs.BF16, True, False),  # group 128, tensor cores
     (24, 256, 1024, 4, 128, inputs.F16, True, True),    # group 128, streaming kernel
+    (200, 384, 512, 8, -1, inputs.BF16, False, True),   # tensor cores, ragged m and n tiles
+    (300, 448, 1024, 4, 64, inputs.BF16, True, True),   # 4-bit, tensor cores, ragged
+    (300, 9792, 512, 4, 64, inputs.BF16, True, True),   # 4-bit 256 x 128 tiles, ragged m and n
 ]
 
 

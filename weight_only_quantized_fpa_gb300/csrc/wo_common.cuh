@@ -156,6 +156,15 @@ __device__ __forceinline__ uint32_t cvt_u4x2<ACT_BF16>(uint32_t ws)
     return sub_bf16x2(and_or(ws, 0x000F000Fu, 0x43004300u), 0x43084308u);  // - 136
 }
 
+// fp16 only: the two nibbles at bits (4, 20) of `w` -> (q - 8) pair, no
+// shift.  fp16 with exponent field 21 (bits 0x5400) spans [64, 128) with
+// spacing 1/16, so mantissa bits 4..7 carry weight 1 and 0x54X0 encodes
+// 64 + X exactly; subtracting 72 leaves q - 8.
+__device__ __forceinline__ uint32_t cvt_u4x2_hi_f16(uint32_t w)
+{
+    return sub_f16x2(and_or(w, 0x00F000F0u, 0x54005400u), 0x54805480u);  // - 72
+}
+
 // The four A-operand registers of k-step s of a packed tile.
 template <int BITS, int ACT>
 __device__ __forceinline__ void tile_frag(const uint4& v, int s, uint32_t (&a)[4])
@@ -170,9 +179,14 @@ __device__ __forceinline__ void tile_frag(const uint4& v, int s, uint32_t (&a)[4
     } else {
         const uint32_t w = s == 0 ? v.x : s == 1 ? v.y : s == 2 ? v.z : v.w;
         a[0] = cvt_u4x2<ACT>(w);
-        a[1] = cvt_u4x2<ACT>(w >> 4);
         a[2] = cvt_u4x2<ACT>(w >> 8);
-        a[3] = cvt_u4x2<ACT>(w >> 12);
+        if constexpr (ACT == ACT_F16) {
+            a[1] = cvt_u4x2_hi_f16(w);
+            a[3] = cvt_u4x2_hi_f16(w >> 8);
+        } else {
+            a[1] = cvt_u4x2<ACT>(w >> 4);
+            a[3] = cvt_u4x2<ACT>(w >> 12);
+        }
     }
 }
 

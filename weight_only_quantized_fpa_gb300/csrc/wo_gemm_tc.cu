@@ -9,7 +9,9 @@
 //
 // Persistent kernel: one CTA per SM walks output tiles of 128 (m) x BN (n),
 // BN = 256 (or 128 when 256-wide tiles would leave half the SMs idle), in
-// the order tile_coords gives.  Roles (16 warps):
+// the order tile_coords gives.  4-bit problems large enough use 256 x 128
+// tiles instead: two M=128 MMAs per k step share one dequantised B tile.
+// Roles (16 warps):
 //   warp 0       TMA producer of the packed code tiles (BN channels x 64 k)
 //                into the code ring;
 //   warp 2       TMA producer of the A tiles (128 x 64, 128-byte swizzle)
@@ -55,19 +57,23 @@ constexpr int kDequantWarp0 = 8;    // warps 8..15
 constexpr int kDequantWarps = 8;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
-template <int BITS, int BN>
+// MS: M=128 sub-tiles per output tile.  With MS = 2 (256 x BN tiles) two
+// MMAs share each dequantised B tile, halving the dequantisation per FLOP.
+template <int BITS, int BN, int MS = 1>
 struct TcCfg {
-    static constexpr int A_BYTES = BM * BK * 2;                  // 16 KiB
+    static constexpr int A_SUB = BM * BK * 2;                    // 16 KiB per sub-tile
+    static constexpr int A_BYTES = MS * A_SUB;
     static constexpr int C_BYTES = BN * BK * BITS / 8;           // packed codes of a k block
     static constexpr int B_BYTES = BN * BK * 2;                  // dequantised operand
-    static constexpr int SA = BN == 256 ? 4 : 6;                 // A ring stages
-    static constexpr int SC = (BITS == 8 ? 4 : 6) + (BN == 256 ? 0 : 2);  // code ring stages
+    static constexpr int SA = MS == 2 ? (BITS == 4 ? 4 : 3) : BN == 256 ? 4 : 6;  // A ring stages
+    static constexpr int SC = MS == 2 ? 6 : (BITS == 8 ? 4 : 6) + (BN == 256 ? 0 : 2);  // code ring
     static constexpr int S2 = BN == 256 ? 3 : 4;                 // operand ring stages
     static constexpr int TPN = BK / Geom<BITS>::KT;              // packed tiles per 16 rows
     static constexpr int NT = (BN / 16) * TPN;                   // packed tiles per k block
     static constexpr int R = NT / kDequantWarps;                 // tiles per dequant warp
     static constexpr int PF = 3;                                 // 4-bit scales loaded ahead
-    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t TMEM_COLS = 2 * MS * BN;  // two accumulators of MS sub-tiles
+    static_assert(TMEM_COLS <= 512, "tensor memory");
     static constexpr int SMEM = SA * A_BYTES + SC * C_BYTES + S2 * B_BYTES;  // + barriers
     static_assert(NT % kDequantWarps == 0, "tiles per k block must split evenly");
     static_assert(SA <= 8 && SC <= 8 && S2 <= 4, "barrier arrays");
@@ -85,6 +91,7 @@ struct TcParams {
     int G;                   // scale groups per channel row
     int group;               // codes per group
     int vec_ok;              // scales and bias 16-byte aligned: vector loads allowed
+    int m_fast;              // tile walk: m fastest (else n fastest)
     unsigned* err;           // workspace error word
 };
 
@@ -98,13 +105,20 @@ struct Barriers {
     int abort;
 };
 
-// Output tile `t` of the persistent walk: n fastest, so that the CTAs
-// running at the same time cover every weight column block for a few
-// consecutive m-tiles; both stay in L2 while those tiles read them.
-__device__ __forceinline__ void tile_coords(const TcParams& p, int t, int bn, int& m0, int& n0)
+// Output tile `t` of the persistent walk.  The operand that is larger in
+// bytes is streamed from HBM once: when A is the smaller one the walk goes m
+// fastest (the CTAs running at the same time share each weight tile while
+// every A row stays in L2), otherwise n fastest (they share A tiles while the
+// weights stay in L2).
+__device__ __forceinline__ void tile_coords(const TcParams& p, int t, int bm, int bn, int& m0, int& n0)
 {
-    m0 = (t / p.n_tiles) * BM;
-    n0 = (t % p.n_tiles) * bn;
+    if (p.m_fast) {
+        m0 = (t % p.m_tiles) * bm;
+        n0 = (t / p.m_tiles) * bn;
+    } else {
+        m0 = (t / p.n_tiles) * bm;
+        n0 = (t % p.n_tiles) * bn;
+    }
 }
 
 // 4-bit: the scale and zero bits of one dequant warp's tiles for one k block
@@ -173,9 +187,11 @@ __device__ __forceinline__ void dequant_stage(uint32_t c_s, const DqScales<BITS,
             zlo = f16_pair<ACT>(sc.z2[r] & 0xFFFFu);
             zhi = f16_pair<ACT>(sc.z2[r] >> 16);
         }
-        // lane -> row address of stmatrix matrix mi: rows r8 (+8 for mi odd),
-        // 16-byte chunk of 8 codes (+1 for mi >= 2)
-        const int row = nb * 16 + r8 + 8 * (mi & 1);
+        // lane -> row address of stmatrix matrix mi: rows r8 (+8 for mi >= 2),
+        // 16-byte chunk of 8 codes (+1 for mi odd); matrices 0 and 1 (and 2
+        // and 3) are the two k chunks of the same rows, which the swizzle puts
+        // in different banks
+        const int row = nb * 16 + r8 + 8 * (mi >> 1);
         const uint32_t row_base = b_s + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
 #pragma unroll
         for (int s = 0; s < KS; ++s) {
@@ -184,13 +200,14 @@ __device__ __forceinline__ void dequant_stage(uint32_t c_s, const DqScales<BITS,
                 tile_frag<8, OT>(v[r], s, a);
             } else {
                 const uint32_t w = s == 0 ? v[r].x : s == 1 ? v[r].y : s == 2 ? v[r].z : v[r].w;
+                const uint32_t w8 = w >> 8;
                 a[0] = fma_f16x2(cvt_u4x2<ACT_F16>(w), slo, zlo);
-                a[1] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 4), shi, zhi);
-                a[2] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 8), slo, zlo);
-                a[3] = fma_f16x2(cvt_u4x2<ACT_F16>(w >> 12), shi, zhi);
+                a[1] = fma_f16x2(cvt_u4x2_hi_f16(w), shi, zhi);
+                a[2] = fma_f16x2(cvt_u4x2<ACT_F16>(w8), slo, zlo);
+                a[3] = fma_f16x2(cvt_u4x2_hi_f16(w8), shi, zhi);
             }
-            const int chunk = (tl * KT + 16 * s) / 8 + (mi >> 1);
-            stmatrix_x4(row_base + (uint32_t)((chunk ^ (row & 7)) << 4), a[0], a[1], a[2], a[3]);
+            const int chunk = (tl * KT + 16 * s) / 8 + (mi & 1);
+            stmatrix_x4(row_base + (uint32_t)((chunk ^ (row & 7)) << 4), a[0], a[2], a[1], a[3]);
         }
     }
 }
@@ -214,12 +231,13 @@ __device__ __forceinline__ void load32_u16(const uint16_t* p, bool vec, uint32_t
     }
 }
 
-template <int BITS, int OT, int ACT, int BN>
+template <int BITS, int OT, int ACT, int BN, int MS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
                    const TcParams p)
 {
-    using Cfg = TcCfg<BITS, BN>;
+    using Cfg = TcCfg<BITS, BN, MS>;
+    constexpr int TM = BM * MS;  // output tile height
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -280,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int it = 0; it < my_tiles && ok; ++it) {
                 int m0, n0;
-                tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, BN, m0, n0);
+                tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, TM, BN, m0, n0);
                 for (int kb = 0; kb < num_kb; ++kb, ++c) {
                     const int s = c % S;
                     if (!mbar_wait_bounded(&empty[s], ((c / S) & 1) ^ 1, abort, p.err, codes ? 1 : 9,
@@ -295,7 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     kb * (Cfg::C_BYTES / (BN / 16) / 4), n0 / 16);
                     } else {
                         mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES);
-                        tma_load_2d(ringA + s * Cfg::A_BYTES, &tmA, &full[s], kb * BK, m0);
+#pragma unroll
+                        for (int h = 0; h < MS; ++h)  // rows past m read as zeros
+                            tma_load_2d(ringA + s * Cfg::A_BYTES + h * Cfg::A_SUB, &tmA, &full[s], kb * BK,
+                                        m0 + h * BM);
                     }
                 }
             }
@@ -320,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                const uint32_t d = tmem + (uint32_t)(acc * MS * BN);
                 for (int kb = 0; kb < num_kb; ++kb, ++c) {
                     const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
                     if (!mbar_wait_bounded(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 2,
@@ -331,12 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = desc_sw128(smem_addr(ringA + sa * Cfg::A_BYTES));
                     const uint64_t bd = desc_sw128(smem_addr(ring2 + s2 * Cfg::B_BYTES));
 #pragma unroll
-                    for (int j = 0; j < BK / 16; ++j)  // +32 bytes per 16-wide k step
-                        mma_f16(d, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), idesc,
-                                (kb > 0 || j > 0) ? 1u : 0u);
+                    for (int h = 0; h < MS; ++h) {  // sub-tile h: TMEM columns [h BN, (h + 1) BN)
+                        const uint64_t ad =
+                            desc_sw128(smem_addr(ringA + sa * Cfg::A_BYTES + h * Cfg::A_SUB));
+#pragma unroll
+                        for (int j = 0; j < BK / 16; ++j)  // +32 bytes per 16-wide k step
+                            mma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
+                                    idesc, (kb > 0 || j > 0) ? 1u : 0u);
+                    }
                     mma_commit(&bars->emptyA[sa]);
                     mma_commit(&bars->empty2[s2]);
                 }
@@ -355,52 +380,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < my_tiles; ++it) {
             const int acc = it & 1;
             int m0, n0;
-            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, BN, m0, n0);
+            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, TM, BN, m0, n0);
             const bool ok = mbar_wait_bounded(&bars->tfull[acc], (it >> 1) & 1, abort, p.err, 6,
                                               kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok && !*abort))  // tcgen05.ld needs the whole warp
                 break;
             tc_fence_after();
-            const int row = m0 + q * 32 + lane;
-            float rs = 1.f;
-            if (p.rowscale && row < p.m)
-                rs = p.rowscale[row];
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                const int nc = n0 + cc * 32;
-                if (nc >= p.n)
-                    break;
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + cc * 32), r);
-                uint32_t sc[16], bi[16];
-                if constexpr (BITS == 8)
-                    load32_u16(p.scales + nc, p.vec_ok != 0, sc);
-                if (p.bias)
-                    load32_u16(p.bias + nc, p.vec_ok != 0, bi);
-                tmem_ld_wait();
-                if (row < p.m) {
-                    uint32_t packed[16];
+            for (int h = 0; h < MS; ++h) {
+                const int row = m0 + h * BM + q * 32 + lane;
+                float rs = 1.f;
+                if (p.rowscale && row < p.m)
+                    rs = p.rowscale[row];
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    const int nc = n0 + cc * 32;
+                    if (nc >= p.n)
+                        break;
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) +
+                                           (uint32_t)((acc * MS + h) * BN + cc * 32),
+                                       r);
+                    uint32_t sc[16], bi[16];
+                    if constexpr (BITS == 8)
+                        load32_u16(p.scales + nc, p.vec_ok != 0, sc);
+                    if (p.bias)
+                        load32_u16(p.bias + nc, p.vec_ok != 0, bi);
+                    tmem_ld_wait();
+                    if (row < p.m) {
+                        uint32_t packed[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
-                        if constexpr (BITS == 8) {
-                            v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
-                            v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
-                        } else {
-                            v0 *= rs;
-                            v1 *= rs;
+                        for (int j = 0; j < 16; ++j) {
+                            float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
+                            if constexpr (BITS == 8) {
+                                v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
+                                v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
+                            } else {
+                                v0 *= rs;
+                                v1 *= rs;
+                            }
+                            if (p.bias) {
+                                v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
+                                v1 += to_f32<ACT>((uint16_t)(bi[j] >> 16));
+                            }
+                            packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
                         }
-                        if (p.bias) {
-                            v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
-                            v1 += to_f32<ACT>((uint16_t)(bi[j] >> 16));
-                        }
-                        packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
+                        uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.n + nc);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                                packed[4 * v + 3]);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.n + nc);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                            packed[4 * v + 3]);
                 }
             }
             tc_fence_before();
@@ -412,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto n0_of = [&](int c) {
             const int it = c / num_kb;
             int m0, n0;
-            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, BN, m0, n0);
+            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, TM, BN, m0, n0);
             return n0;
         };
         DqScales<BITS, BN> buf[Cfg::PF];
@@ -505,6 +535,15 @@ __global__ void a_to_f16_kernel(const uint16_t* __restrict__ A, uint16_t* __rest
         rowscale[row] = ldexpf(1.f, E);
 }
 
+// Sub-tiles per output tile: 4-bit codes (whose dequantisation costs the most
+// per weight) use 256 x 128 tiles when m exceeds one sub-tile and those tiles
+// still give every SM one.
+int tc_ms(int m, int n, int bits)
+{
+    const long long tiles = (long long)((m + 2 * BM - 1) / (2 * BM)) * ((n + 127) / 128);
+    return bits == 4 && m > BM && tiles >= num_sms() ? 2 : 1;
+}
+
 // Tile width: 256, or 128 when 256-wide tiles would fill at most half the SMs.
 int tc_bn(int m, int n)
 {
@@ -512,14 +551,16 @@ int tc_bn(int m, int n)
     return 2 * tiles256 <= num_sms() ? 128 : 256;
 }
 
-template <int BITS, int OT, int ACT, int BN>
+template <int BITS, int OT, int ACT, int BN, int MS>
 cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaStream_t s)
 {
-    constexpr int smem = TcCfg<BITS, BN>::SMEM + (int)sizeof(Barriers) + 1024;
-    auto kern = gemm_tc_kernel<BITS, OT, ACT, BN>;
+    constexpr int smem = TcCfg<BITS, BN, MS>::SMEM + (int)sizeof(Barriers) + 1024;
+    static_assert(smem <= 232448, "shared memory per CTA");
+    auto kern = gemm_tc_kernel<BITS, OT, ACT, BN, MS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
+    tp.m_tiles = (tp.m + BM * MS - 1) / (BM * MS);
     tp.n_tiles = (tp.n + BN - 1) / BN;
     const long long tiles = (long long)tp.m_tiles * tp.n_tiles;
     const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
@@ -537,8 +578,10 @@ cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaS
 template <int BITS, int OT, int ACT>
 cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& tp, cudaStream_t s)
 {
-    return tc_bn(tp.m, tp.n) == 128 ? launch_tc_t<BITS, OT, ACT, 128>(ma, B, tp, s)
-                                    : launch_tc_t<BITS, OT, ACT, 256>(ma, B, tp, s);
+    if (tc_ms(tp.m, tp.n, BITS) == 2)
+        return launch_tc_t<BITS, OT, ACT, 128, 2>(ma, B, tp, s);
+    return tc_bn(tp.m, tp.n) == 128 ? launch_tc_t<BITS, OT, ACT, 128, 1>(ma, B, tp, s)
+                                    : launch_tc_t<BITS, OT, ACT, 256, 1>(ma, B, tp, s);
 }
 
 }  // namespace
@@ -560,7 +603,6 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     tp.n = a.n;
     tp.k = a.k;
     tp.num_kb = a.k / BK;
-    tp.m_tiles = (a.m + BM - 1) / BM;
     tp.scales = static_cast<const uint16_t*>(a.scales);
     tp.zeros = static_cast<const uint16_t*>(a.zeros);
     tp.bias = static_cast<const uint16_t*>(a.bias);
@@ -570,6 +612,8 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     tp.vec_ok = (reinterpret_cast<uintptr_t>(a.scales) % 16 == 0) &&
                 (reinterpret_cast<uintptr_t>(a.bias) % 16 == 0);
     tp.err = reinterpret_cast<unsigned*>(ws);
+    // stream the larger operand once (A: m*k*2 bytes, codes: n*k*bits/8)
+    tp.m_fast = (double)a.m * 2.0 <= (double)a.n * a.bits / 8.0;
 
     const void* Aop = a.A;
     if (plan.a16_bytes) {

@@ -68,6 +68,8 @@ SMALL = [
     (200, 384, 512, 8, -1, inputs.BF16, False, True),   # tensor cores, ragged m and n tiles
     (300, 448, 1024, 4, 64, inputs.BF16, True, True),   # 4-bit, tensor cores, ragged
     (300, 9792, 512, 4, 64, inputs.BF16, True, True),   # 4-bit 256 x 128 tiles, ragged m and n
+    (300, 19520, 512, 8, -1, inputs.F16, False, True),  # 256 x 256 tiles, ragged m and n
+    (260, 19584, 512, 4, 64, inputs.BF16, True, False), # 4-bit 256 x 256 tiles, ragged
 ]
 
 

@@ -7,16 +7,16 @@
 // happens per 64-wide k block on chip, right before tcgen05 MMAs that
 // accumulate in tensor memory.
 //
-// Persistent kernel: one CTA per SM walks output tiles of 128 (m) x BN (n),
-// BN = 256 (or 128 when 256-wide tiles would leave half the SMs idle), in
-// the order tile_coords gives.  4-bit problems large enough use 256 x 128
-// tiles instead: two M=128 MMAs per k step share one dequantised B tile.
-// Roles (16 warps):
+// Persistent kernel: one CTA per SM walks output tiles of MS x 128 (m) by BN
+// (n) in the order tile_coords gives; tc_shape picks the shape (256 x 256
+// when the GPU stays full, so that every A and code byte fetched from L2
+// feeds the most FLOPs).  With MS = 2 two M=128 MMAs per k step share one
+// dequantised B tile.  Roles (16 warps):
 //   warp 0       TMA producer of the packed code tiles (BN channels x 64 k)
 //                into the code ring;
 //   warp 2       TMA producer of the A tiles (128 x 64, 128-byte swizzle)
 //                into the A ring;
-//   warp 1       allocates 2 * BN TMEM columns (two accumulators); one lane
+//   warp 1       allocates the TMEM accumulators (two when they fit); one lane
 //                issues the MMAs (M=128, N=BN, K=16, four per k block) and
 //                commits them to the ring barriers and, at a tile's end, to
 //                the accumulator's "full" barrier;
@@ -65,14 +65,17 @@ struct TcCfg {
     static constexpr int A_BYTES = MS * A_SUB;
     static constexpr int C_BYTES = BN * BK * BITS / 8;           // packed codes of a k block
     static constexpr int B_BYTES = BN * BK * 2;                  // dequantised operand
-    static constexpr int SA = MS == 2 ? (BITS == 4 ? 4 : 3) : BN == 256 ? 4 : 6;  // A ring stages
-    static constexpr int SC = MS == 2 ? 6 : (BITS == 8 ? 4 : 6) + (BN == 256 ? 0 : 2);  // code ring
-    static constexpr int S2 = BN == 256 ? 3 : 4;                 // operand ring stages
+    static constexpr int SA = MS == 2 ? (BN == 256 ? 3 : BITS == 4 ? 4 : 3) : BN == 256 ? 4 : 6;  // A ring
+    static constexpr int SC = MS == 2 ? (BN == 256 ? 3 : 6) : (BITS == 8 ? 4 : 6) + (BN == 256 ? 0 : 2);  // codes
+    static constexpr int S2 = MS == 2 && BN == 256 ? 2 : BN == 256 ? 3 : 4;  // operand ring stages
     static constexpr int TPN = BK / Geom<BITS>::KT;              // packed tiles per 16 rows
     static constexpr int NT = (BN / 16) * TPN;                   // packed tiles per k block
     static constexpr int R = NT / kDequantWarps;                 // tiles per dequant warp
     static constexpr int PF = 3;                                 // 4-bit scales loaded ahead
-    static constexpr uint32_t TMEM_COLS = 2 * MS * BN;  // two accumulators of MS sub-tiles
+    // accumulators of MS sub-tiles: two (the epilogue of one tile overlaps the
+    // next tile's main loop) when they fit in the 512 TMEM columns, else one
+    static constexpr int NACC = 2 * MS * BN <= 512 ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = NACC * MS * BN;
     static_assert(TMEM_COLS <= 512, "tensor memory");
     static constexpr int SMEM = SA * A_BYTES + SC * C_BYTES + S2 * B_BYTES;  // + barriers
     static_assert(NT % kDequantWarps == 0, "tiles per k block must split evenly");
@@ -334,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int c = 0;
             bool ok = true;
             for (int it = 0; it < my_tiles && ok; ++it) {
-                const int acc = it & 1;
-                if (!mbar_wait_bounded(&bars->tempty[acc], ((it >> 1) & 1) ^ 1, abort, p.err, 7,
+                const int acc = it % Cfg::NACC, use = it / Cfg::NACC;
+                if (!mbar_wait_bounded(&bars->tempty[acc], (use & 1) ^ 1, abort, p.err, 7,
                                        kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -378,10 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- epilogue: TMEM lane quadrant q = warp % 4 ----
         const int q = warp - kEpilogueWarp0;
         for (int it = 0; it < my_tiles; ++it) {
-            const int acc = it & 1;
+            const int acc = it % Cfg::NACC, use = it / Cfg::NACC;
             int m0, n0;
             tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, TM, BN, m0, n0);
-            const bool ok = mbar_wait_bounded(&bars->tfull[acc], (it >> 1) & 1, abort, p.err, 6,
+            const bool ok = mbar_wait_bounded(&bars->tfull[acc], use & 1, abort, p.err, 6,
                                               kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ok && !*abort))  // tcgen05.ld needs the whole warp
                 break;
@@ -535,20 +538,28 @@ __global__ void a_to_f16_kernel(const uint16_t* __restrict__ A, uint16_t* __rest
         rowscale[row] = ldexpf(1.f, E);
 }
 
-// Sub-tiles per output tile: 4-bit codes (whose dequantisation costs the most
-// per weight) use 256 x 128 tiles when m exceeds one sub-tile and those tiles
-// still give every SM one.
-int tc_ms(int m, int n, int bits)
-{
-    const long long tiles = (long long)((m + 2 * BM - 1) / (2 * BM)) * ((n + 127) / 128);
-    return bits == 4 && m > BM && tiles >= num_sms() ? 2 : 1;
-}
+// Output tile shape: MS sub-tiles of 128 rows by BN columns.
+//   256 x 256 whenever those tiles still give every SM one: A and the codes
+//     are each fetched from L2 once per 256 columns / rows, the least traffic
+//     per FLOP (one accumulator: its 512 TMEM columns leave no room for a
+//     second, so the epilogue does not overlap the next tile);
+//   256 x 128 for 4-bit codes (their dequantisation costs the most per
+//     weight) when those tiles fill the GPU: two MMAs share each B tile;
+//   otherwise 128 x 256, or 128 x 128 when 256-wide tiles would fill at most
+//     half the SMs.
+struct TcShape {
+    int bn, ms;
+};
 
-// Tile width: 256, or 128 when 256-wide tiles would fill at most half the SMs.
-int tc_bn(int m, int n)
+TcShape tc_shape(int m, int n, int bits)
 {
+    const long long mt2 = (m + 2 * BM - 1) / (2 * BM);
+    if (m > BM && mt2 * ((n + 255) / 256) >= num_sms())
+        return {256, 2};
+    if (bits == 4 && m > BM && mt2 * ((n + 127) / 128) >= num_sms())
+        return {128, 2};
     const long long tiles256 = (long long)((m + BM - 1) / BM) * ((n + 255) / 256);
-    return 2 * tiles256 <= num_sms() ? 128 : 256;
+    return {2 * tiles256 <= num_sms() ? 128 : 256, 1};
 }
 
 template <int BITS, int OT, int ACT, int BN, int MS>
@@ -578,10 +589,12 @@ cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaS
 template <int BITS, int OT, int ACT>
 cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& tp, cudaStream_t s)
 {
-    if (tc_ms(tp.m, tp.n, BITS) == 2)
-        return launch_tc_t<BITS, OT, ACT, 128, 2>(ma, B, tp, s);
-    return tc_bn(tp.m, tp.n) == 128 ? launch_tc_t<BITS, OT, ACT, 128, 1>(ma, B, tp, s)
-                                    : launch_tc_t<BITS, OT, ACT, 256, 1>(ma, B, tp, s);
+    const TcShape sh = tc_shape(tp.m, tp.n, BITS);
+    if (sh.ms == 2)
+        return sh.bn == 256 ? launch_tc_t<BITS, OT, ACT, 256, 2>(ma, B, tp, s)
+                            : launch_tc_t<BITS, OT, ACT, 128, 2>(ma, B, tp, s);
+    return sh.bn == 128 ? launch_tc_t<BITS, OT, ACT, 128, 1>(ma, B, tp, s)
+                        : launch_tc_t<BITS, OT, ACT, 256, 1>(ma, B, tp, s);
 }
 
 }  // namespace

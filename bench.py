@@ -599,23 +599,35 @@ def run_ours(args, ws, rank, local):
         value = flops_per_step * args.steps * ws / secs / 1e12
 
     # ---- end to end through the public API with host buffers ----
-    host_A = [torch.empty(d["A"].shape, dtype=d["A"].dtype, pin_memory=True) for d in dev_cases]
-    host_C = [torch.empty(d["C"].shape, dtype=d["C"].dtype, pin_memory=True) for d in dev_cases]
-    for h, d in zip(host_A, dev_cases):
-        h.copy_(d["A"].cpu())
-    h2d = sum(h.numel() * h.element_size() for h in host_A)
-    d2h = sum(h.numel() * h.element_size() for h in host_C)
+    # every step: one pinned host -> device copy of all the cases' activations,
+    # one wo.gemm per case, one device -> host copy of all the outputs
+    a_sizes = [d["A"].numel() for d in dev_cases]
+    c_sizes = [d["C"].numel() for d in dev_cases]
+    a_dt, c_dt = dev_cases[0]["A"].dtype, dev_cases[0]["C"].dtype
+    host_A = torch.empty(sum(a_sizes), dtype=a_dt, pin_memory=True)
+    host_C = torch.empty(sum(c_sizes), dtype=c_dt, pin_memory=True)
+    dev_A = torch.empty(sum(a_sizes), dtype=a_dt, device=dev)
+    dev_C = torch.empty(sum(c_sizes), dtype=c_dt, device=dev)
+    a_views, c_views, off_a, off_c = [], [], 0, 0
+    for d, na, nc in zip(dev_cases, a_sizes, c_sizes):
+        host_A[off_a:off_a + na].copy_(d["A"].reshape(-1).cpu())
+        a_views.append(dev_A[off_a:off_a + na].view(d["A"].shape))
+        c_views.append(dev_C[off_c:off_c + nc].view(d["C"].shape))
+        off_a += na
+        off_c += nc
+    h2d = host_A.numel() * host_A.element_size()
+    d2h = host_C.numel() * host_C.element_size()
     e2e_steps = max(1, min(args.steps, 50))
 
     def e2e_step():
         with torch.cuda.stream(stream):
-            for h, d, hc in zip(host_A, dev_cases, host_C):
-                d["A"].copy_(h, non_blocking=True)
+            dev_A.copy_(host_A, non_blocking=True)
+            for d, Av, Cv in zip(dev_cases, a_views, c_views):
                 c = d["c"]
-                wo.gemm(d["A"], d["B"], d["s"], c.n, c.k, c.bits, group_size=c.group_size,
-                        zeros=d["z"], bias=d["b"], out=d["C"], workspace=workspace,
+                wo.gemm(Av, d["B"], d["s"], c.n, c.k, c.bits, group_size=c.group_size,
+                        zeros=d["z"], bias=d["b"], out=Cv, workspace=workspace,
                         stream=stream)
-                hc.copy_(d["C"], non_blocking=True)
+            host_C.copy_(dev_C, non_blocking=True)
     for _ in range(min(3, e2e_steps)):
         e2e_step()
     torch.cuda.synchronize()

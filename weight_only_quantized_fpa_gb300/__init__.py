@@ -48,6 +48,8 @@ def library_path() -> str:
 def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     """Load libwo.so; raise if it is not built (no fallback path exists)."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -137,8 +139,15 @@ def wo_unpack(B_packed, B_rowmajor, n: int, k: int, bits: int, stream=None) -> N
                                     _stream_ptr(stream)), "wo_unpack")
 
 
+_ws_sizes: dict = {}
+
+
 def wo_workspace_size(m: int, n: int, k: int, group_size: int, bits: int) -> int:
-    return int(load_library().wo_workspace_size(m, n, k, group_size, bits))
+    key = (m, n, k, group_size, bits)
+    v = _ws_sizes.get(key)
+    if v is None:  # a pure function of the shape: computed once per shape
+        v = _ws_sizes[key] = int(load_library().wo_workspace_size(m, n, k, group_size, bits))
+    return v
 
 
 def wo_gemm(A, B_packed, scales, zeros, bias, C, m: int, n: int, k: int, group_size: int,

@@ -52,6 +52,8 @@ class DeviceMoe:
     (64, 512, 192, 16, 2, inputs.F16, True),
     (5, 128, 64, 4, 1, inputs.BF16, False),
     (300, 256, 256, 6, 3, inputs.BF16, False),   # > 64 rows per expert: several passes
+    (48, 384, 128, 12, 4, inputs.F16, True),     # tensor-core experts, fp16, top-4
+    (6, 256, 128, 32, 2, inputs.BF16, False),    # most experts without rows
 ])
 def test_moe_small(wo, T, H, I, E, topk, act, renorm):
     c = inputs.make_moe_case(T=T, H=H, I=I, E=E, topk=topk, act_dtype=act, case=T + E,

@@ -100,7 +100,7 @@ struct TcParams {
 
 struct Barriers {
     uint64_t fullA[8], emptyA[8];  // A ring (TMA -> MMA)
-    uint64_t fullC[8], emptyC[8];  // code ring (TMA -> dequant warps)
+    uint64_t fullC[16], emptyC[16];  // code ring (TMA -> dequant warps)
     uint64_t full2[4], empty2[4];  // operand ring (dequant warps -> MMA)
     uint64_t tfull[2], tempty[2];  // the two TMEM accumulators (MMA <-> epilogue)
     uint64_t mma_done;             // every MMA issued has completed (teardown)
@@ -597,6 +597,315 @@ cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& t
                         : launch_tc_t<BITS, OT, ACT, 256, 1>(ma, B, tp, s);
 }
 
+
+// ============================================================ MoE experts ===
+//
+// Grouped expert GEMMs of the MoE FFN (acext User Guide (v1.7) 1.2.3) on the
+// tensor cores, "swap AB": an expert's 8-bit weights, dequantised exactly to
+// (q - 128) in the activation dtype, are the MMA's 128-row operand (output
+// channels), and the expert's token rows (in expert order, a chunk of up to
+// kMoeNT at a time) are its N operand, so an expert's few dozen rows still
+// fill the tensor pipe while its weights stream from HBM once per chunk.
+// Work items: (expert, block of 128 output channels); for the gated fc1 an
+// item carries the 128 gate channels and the matching 128 up channels
+// (inter apart) so the epilogue can form h = silu(gate) * up.  Roles as in
+// gemm_tc_kernel: warp 0 codes TMA, warp 2 activation TMA, warp 1 MMA,
+// warps 4-7 epilogue (TMEM lanes are channels, columns are tokens), warps
+// 8-15 dequantisation.
+
+constexpr int kMoeNT = 64;  // token rows per chunk (the MMA's N)
+
+template <bool GATED>
+struct MoeCfg {
+    static constexpr int WR = GATED ? 256 : 128;         // weight rows per item
+    static constexpr int A_BYTES = kMoeNT * BK * 2;       // 8 KiB of token rows
+    static constexpr int C_BYTES = WR * BK;               // packed codes of a k block
+    static constexpr int B_BYTES = WR * BK * 2;           // dequantised operand
+    // The codes stream from HBM: their ring holds 128 KiB, the bytes in flight
+    // one SM needs at HBM rate under load; token rows come from L2 and the
+    // operand ring only covers the dequant -> MMA hand-off.
+    static constexpr int SA = 4, SC = GATED ? 8 : 16, S2 = GATED ? 2 : 3;
+    static_assert(SC <= 16 && S2 <= 4 && SA <= 8, "barrier arrays");
+    static constexpr int COLS = (GATED ? 2 : 1) * kMoeNT; // TMEM columns per accumulator
+    static constexpr uint32_t TMEM_COLS = 2 * COLS;
+    static constexpr int SMEM = SA * A_BYTES + SC * C_BYTES + S2 * B_BYTES;
+};
+
+struct MoeTcParams {
+    const int* offsets;      // [E + 1] row ranges of the experts (rows in expert order)
+    int E, nb;               // experts, 128-channel blocks per expert
+    int num_kb;              // K / BK
+    int inter;               // gated: channel distance gate -> up (and h row length)
+    int n_out;               // plain: output row length (hidden)
+    int rows_per_expert_w;   // weight rows of one expert (2 * inter or hidden)
+    const uint16_t* scales;  // [E, rows_per_expert_w] in the activation dtype
+    uint16_t* H;             // gated output h [rows, inter]
+    float* Y;                // fp32 output [rows, n_out]
+    unsigned* err;
+};
+
+// Chunks of expert e's rows: its row range and how many kMoeNT chunks it needs.
+__device__ __forceinline__ void moe_rows(const MoeTcParams& p, int e, int& r0, int& cnt, int& chunks)
+{
+    r0 = p.offsets[e];
+    cnt = p.offsets[e + 1] - r0;
+    chunks = cnt > 0 ? (cnt + kMoeNT - 1) / kMoeNT : 0;
+}
+
+template <bool GATED, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
+                  const MoeTcParams p)
+{
+    using Cfg = MoeCfg<GATED>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* ringA = smem;
+    uint8_t* ring2 = ringA + Cfg::SA * Cfg::A_BYTES;
+    uint8_t* ringC = ring2 + Cfg::S2 * Cfg::B_BYTES;
+    Barriers* bars = reinterpret_cast<Barriers*>(ringC + Cfg::SC * Cfg::C_BYTES);
+    volatile int* abort = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_kb = p.num_kb;
+    const int items = p.E * p.nb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::SA; ++s) {
+            mbar_init(&bars->fullA[s], 1);
+            mbar_init(&bars->emptyA[s], 1);
+        }
+        for (int s = 0; s < Cfg::SC; ++s) {
+            mbar_init(&bars->fullC[s], 1);
+            mbar_init(&bars->emptyC[s], kDequantWarps);
+        }
+        for (int s = 0; s < Cfg::S2; ++s) {
+            mbar_init(&bars->full2[s], kDequantWarps * 32);
+            mbar_init(&bars->empty2[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars->tfull[a], 1);
+            mbar_init(&bars->tempty[a], 4 * 32);
+        }
+        mbar_init(&bars->mma_done, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0 || warp == 2) {
+        if (lane == 0) {
+            // ---- TMA producers: codes (warp 0) and token rows (warp 2) ----
+            const bool codes = warp == 0;
+            const int S = codes ? Cfg::SC : Cfg::SA;
+            uint64_t* full = codes ? bars->fullC : bars->fullA;
+            uint64_t* empty = codes ? bars->emptyC : bars->emptyA;
+            int c = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                const int e = it / p.nb, nb = it % p.nb;
+                int r0, cnt, chunks;
+                moe_rows(p, e, r0, cnt, chunks);
+                const int wrow = (e * p.rows_per_expert_w + nb * 128) / 16;  // 16-channel block row
+                for (int ch = 0; ch < chunks && ok; ++ch) {
+                    for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                        const int s = c % S;
+                        if (!mbar_wait_bounded(&empty[s], ((c / S) & 1) ^ 1, abort, p.err, codes ? 21 : 22,
+                                               kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        if (codes) {
+                            mbar_arrive_expect_tx(&full[s], Cfg::C_BYTES);
+                            uint8_t* dst = ringC + s * Cfg::C_BYTES;
+                            tma_load_2d(dst, &tmC, &full[s], kb * (BK * 16 / 4), wrow);
+                            if constexpr (GATED)  // the matching up channels, inter rows further
+                                tma_load_2d(dst + 128 * BK, &tmC, &full[s], kb * (BK * 16 / 4),
+                                            wrow + p.inter / 16);
+                        } else {
+                            mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES);
+                            tma_load_2d(ringA + s * Cfg::A_BYTES, &tmA, &full[s], kb * BK,
+                                        r0 + ch * kMoeNT);
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int i = c - S > 0 ? c - S : 0; i < c; ++i)
+                    mbar_wait_bounded(&full[i % S], (i / S) & 1, &never, nullptr, 0, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer: D[channels, tokens] += W[channels, k] . X[tokens, k]^T ----
+            constexpr uint32_t idesc = idesc_f16(ACT == ACT_BF16 ? 1u : 0u, 128, kMoeNT);
+            int c = 0, t = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                int r0, cnt, chunks;
+                moe_rows(p, it / p.nb, r0, cnt, chunks);
+                for (int ch = 0; ch < chunks && ok; ++ch, ++t) {
+                    const int acc = t & 1;
+                    if (!mbar_wait_bounded(&bars->tempty[acc], ((t >> 1) & 1) ^ 1, abort, p.err, 27,
+                                           kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(acc * Cfg::COLS);
+                    for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                        const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
+                        if (!mbar_wait_bounded(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 23,
+                                               kWaitLimitNs) ||
+                            !mbar_wait_bounded(&bars->full2[s2], (c / Cfg::S2) & 1, abort, p.err, 24,
+                                               kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t w_s = smem_addr(ring2 + s2 * Cfg::B_BYTES);
+                        const uint64_t wd = desc_sw128(w_s);
+                        const uint64_t xd = desc_sw128(smem_addr(ringA + sa * Cfg::A_BYTES));
+#pragma unroll
+                        for (int j = 0; j < BK / 16; ++j) {
+                            mma_f16(d, wd + (uint64_t)(2 * j), xd + (uint64_t)(2 * j), idesc,
+                                    (kb > 0 || j > 0) ? 1u : 0u);
+                            if constexpr (GATED)  // up rows: operand rows 128..255, 16 KiB on
+                                mma_f16(d + kMoeNT, desc_sw128(w_s + 128 * 128) + (uint64_t)(2 * j),
+                                        xd + (uint64_t)(2 * j), idesc, (kb > 0 || j > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&bars->emptyA[sa]);
+                        mma_commit(&bars->empty2[s2]);
+                    }
+                    if (ok)
+                        mma_commit(&bars->tfull[acc]);
+                }
+            }
+            mma_commit(&bars->mma_done);
+            volatile int never = 0;
+            mbar_wait_bounded(&bars->mma_done, 0, &never, p.err, 28, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+        // ---- epilogue: lane = channel (TMEM lane quadrant warp % 4), column = token ----
+        const int q = warp - kEpilogueWarp0;
+        int t = 0;
+        for (int it = blockIdx.x; it < items; it += gridDim.x) {
+            const int e = it / p.nb, nb = it % p.nb;
+            int r0, cnt, chunks;
+            moe_rows(p, e, r0, cnt, chunks);
+            const int chl = nb * 128 + q * 32 + lane;  // output channel within the expert
+            const uint16_t* se = p.scales + (size_t)e * p.rows_per_expert_w;
+            const float s0 = to_f32<ACT>(ld_nc_u16(se + chl));
+            const float s1 = GATED ? to_f32<ACT>(ld_nc_u16(se + p.inter + chl)) : 0.f;
+            bool ok = true;
+            for (int ch = 0; ch < chunks; ++ch, ++t) {
+                const int acc = t & 1;
+                const bool got = mbar_wait_bounded(&bars->tfull[acc], (t >> 1) & 1, abort, p.err, 26,
+                                                   kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, got && !*abort)) {  // tcgen05.ld needs the whole warp
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Cfg::COLS);
+#pragma unroll 1
+                for (int cc = 0; cc < kMoeNT / 32; ++cc) {
+                    const int tok0 = ch * kMoeNT + cc * 32;
+                    if (tok0 >= cnt)
+                        break;  // warp-uniform
+                    uint32_t r[32], u[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)(cc * 32), r);
+                    if constexpr (GATED)
+                        tmem_ld_32x32b_x32(tbase + (uint32_t)(kMoeNT + cc * 32), u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (tok0 + j < cnt) {  // rows past the expert's range are not its own
+                            const size_t row = (size_t)(r0 + tok0 + j);
+                            const float g = __uint_as_float(r[j]) * s0;
+                            if constexpr (GATED) {
+                                const float up = __uint_as_float(u[j]) * s1;
+                                p.H[row * p.inter + chl] = from_f32<ACT>(g / (1.f + expf(-g)) * up);
+                            } else {
+                                p.Y[row * p.n_out + chl] = g;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars->tempty[acc]);
+            }
+            if (!ok)
+                break;
+        }
+    } else if (warp >= kDequantWarp0) {
+        // ---- dequantisation: exact (q - 128) in the activation dtype ----
+        const int dw = warp - kDequantWarp0;
+        const DqScales<8, Cfg::WR> none{};
+        int c = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+            int r0, cnt, chunks;
+            moe_rows(p, it / p.nb, r0, cnt, chunks);
+            for (int ch = 0; ch < chunks && ok; ++ch) {
+                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                    const int sc = c % Cfg::SC, s2 = c % Cfg::S2;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_bounded(&bars->fullC[sc], (c / Cfg::SC) & 1, abort, p.err,
+                                                      24, kWaitLimitNs) &&
+                                        mbar_wait_bounded(&bars->empty2[s2], ((c / Cfg::S2) & 1) ^ 1,
+                                                          abort, p.err, 25, kWaitLimitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    dequant_stage<8, ACT, ACT, Cfg::WR>(smem_addr(ringC + sc * Cfg::C_BYTES), none,
+                                                        smem_addr(ring2 + s2 * Cfg::B_BYTES), dw, lane);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars->full2[s2]);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bars->emptyC[sc]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+}
+
+template <bool GATED, int ACT>
+cudaError_t launch_moe_tc_t(const CUtensorMap& ma, const CUtensorMap& mc, const MoeTcParams& mp,
+                            cudaStream_t s)
+{
+    constexpr int smem = MoeCfg<GATED>::SMEM + (int)sizeof(Barriers) + 1024;
+    static_assert(smem <= 232448, "shared memory per CTA");
+    auto kern = moe_tc_kernel<GATED, ACT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    const int items = mp.E * mp.nb;
+    const int grid = items < num_sms() ? items : num_sms();
+    kern<<<grid, kThreads, smem, s>>>(ma, mc, mp);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 TcPlan plan_tc(int m, int n, int k, int bits, int act)
@@ -650,6 +959,47 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
                                : launch_tc_bn<8, ACT_BF16, ACT_BF16>(ma, a.B, tp, s);
     return a.act == WO_F16 ? launch_tc_bn<4, ACT_F16, ACT_F16>(ma, a.B, tp, s)
                            : launch_tc_bn<4, ACT_F16, ACT_BF16>(ma, a.B, tp, s);
+}
+
+}  // namespace wo
+
+namespace wo {
+
+bool moe_tc_supported(int hidden, int inter) { return hidden % 128 == 0 && inter % 128 == 0; }
+
+cudaError_t launch_moe_tc(bool gated, int act, const void* rows, int total_rows, int k,
+                          const uint8_t* codes, const void* scales, int experts, int n_out,
+                          int inter, const int* offsets, void* out, unsigned* err, cudaStream_t s)
+{
+    MoeTcParams mp{};
+    mp.offsets = offsets;
+    mp.E = experts;
+    mp.nb = (gated ? inter : n_out) / 128;
+    mp.num_kb = k / BK;
+    mp.inter = inter;
+    mp.n_out = n_out;
+    mp.rows_per_expert_w = gated ? 2 * inter : n_out;
+    mp.scales = static_cast<const uint16_t*>(scales);
+    mp.H = gated ? static_cast<uint16_t*>(out) : nullptr;
+    mp.Y = gated ? nullptr : static_cast<float*>(out);
+    mp.err = err;
+    // token rows: [total_rows, k], kMoeNT x 64 boxes, 128-byte swizzle
+    CUtensorMap ma, mc;
+    if (!make_tmap_2d(&ma, act == WO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      rows, (uint64_t)k, (uint64_t)total_rows, (uint64_t)k * 2, BK, kMoeNT,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    // all experts' packed codes: one row per 16-channel block, k * 16 bytes each
+    const uint64_t row_bytes = (uint64_t)k * 16;
+    const uint64_t block_rows = (uint64_t)experts * mp.rows_per_expert_w / 16;
+    if (!make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, codes, row_bytes / 4, block_rows, row_bytes,
+                      BK * 16 / 4, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (gated)
+        return act == WO_F16 ? launch_moe_tc_t<true, ACT_F16>(ma, mc, mp, s)
+                             : launch_moe_tc_t<true, ACT_BF16>(ma, mc, mp, s);
+    return act == WO_F16 ? launch_moe_tc_t<false, ACT_F16>(ma, mc, mp, s)
+                         : launch_moe_tc_t<false, ACT_BF16>(ma, mc, mp, s);
 }
 
 }  // namespace wo

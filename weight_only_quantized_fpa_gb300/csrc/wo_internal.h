@@ -62,4 +62,12 @@ struct TcPlan {
 TcPlan plan_tc(int m, int n, int k, int bits, int act);
 cudaError_t launch_tc(const GemmArgs& a, const TcPlan& p, cudaStream_t s);
 
+// MoE expert GEMMs on the tensor cores (8-bit codes; hidden and inter
+// multiples of 128): gated fc1 -> h [rows, inter] in the activation dtype,
+// or fc2 -> fp32 [rows, n_out]; rows are in expert order, offsets[E + 1].
+bool moe_tc_supported(int hidden, int inter);
+cudaError_t launch_moe_tc(bool gated, int act, const void* rows, int total_rows, int k,
+                          const uint8_t* codes, const void* scales, int experts, int n_out,
+                          int inter, const int* offsets, void* out, unsigned* err, cudaStream_t s);
+
 }  // namespace wo

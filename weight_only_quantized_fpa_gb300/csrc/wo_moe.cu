@@ -3,25 +3,28 @@
 // activation -> fc2 -> routing-weighted combine), 8-bit per-channel expert
 // weights.
 //
-//   1. route_sort_kernel (one CTA): per token, top-k of the fp32 logits
-//      (ties to the lower expert id, compared exactly as stored) and the
-//      softmax probabilities of the chosen experts over all experts
-//      (renormalised over the chosen ones on request); then a stable
-//      counting sort of the T*k (token, slot) pairs by expert, giving each
-//      expert a contiguous range of rows.
+//   1. route_topk_kernel (a warp per token): top-k of the fp32 logits (ties
+//      to the lower expert id, compared exactly as stored) and the softmax
+//      probabilities of the chosen experts over all experts (renormalised
+//      over the chosen ones on request); route_sort_kernel (one CTA): a
+//      stable counting sort of the T*k (token, slot) pairs by expert, giving
+//      each expert a contiguous range of rows.
 //   2. gather_rows_kernel copies the activation rows into expert order;
-//      then the weight-streaming kernel (wo_stream.cu), gated output, one
-//      CTA row per expert: x1 = A[rows] . dequant(fc1_e)^T for gate channels
-//      and the matching up channels (inter apart), h = round(silu(g) * u)
-//      into [rows, inter].
-//   3. the same kernel, fp32 output: y = h[rows] . dequant(fc2_e)^T into
-//      [rows, hidden].
+//      then fc1 with the gated output: x1 = A[rows] . dequant(fc1_e)^T for
+//      gate channels and the matching up channels (inter apart),
+//      h = round(silu(g) * u) into [rows, inter];
+//   3. fc2 to fp32: y = h[rows] . dequant(fc2_e)^T into [rows, hidden].
+//      Steps 2 and 3 run on the tensor cores (moe_tc_kernel in
+//      wo_gemm_tc.cu: the expert's dequantised weights are the MMA's
+//      128-row operand, its rows the N operand) when hidden and inter are
+//      multiples of 128, else on the weight-streaming kernel (wo_stream.cu,
+//      one CTA row per expert, mma.sync).
 //   4. combine_kernel: out[t] = round(sum_j p[t][j] * y[row(t, j)]), j in
 //      ascending order.
 // Every sum has a fixed order, so the result is bit-for-bit repeatable.
 //
-// The expert GEMMs run up to 64 rows per pass; experts with more rows take
-// several passes over their weights.
+// The expert GEMMs run up to 64 rows per pass (chunk); experts with more rows
+// take several passes over their weights.
 #include <cuda_runtime.h>
 
 #include "wo_common.cuh"
@@ -31,7 +34,8 @@
 namespace wo {
 namespace {
 
-constexpr int kRouteThreads = 1024;
+constexpr int kTopkWarps = 8;   // tokens per top-k CTA
+constexpr int kSortWarps = 32;  // warps of the sorting CTA
 
 // ---------------------------------------------------------------- layout ---
 
@@ -63,113 +67,132 @@ MoeLayout moe_layout(int T, int hidden, int inter, int experts, int topk)
 
 // ------------------------------------------------------------- routing -----
 
-__global__ void __launch_bounds__(kRouteThreads)
-    route_sort_kernel(const float* __restrict__ logits, int T, int E, int topk, int renorm,
-                      int* __restrict__ ids, float* __restrict__ wts, int* __restrict__ pos,
-                      int* __restrict__ offsets, int* __restrict__ perm_tok)
+// Top-k and softmax weights, one warp per token.
+__global__ void __launch_bounds__(kTopkWarps * 32)
+    route_topk_kernel(const float* __restrict__ logits, int T, int E, int topk, int renorm,
+                      int* __restrict__ ids, float* __restrict__ wts)
 {
-    extern __shared__ int cnt[];  // [E] counts, then [E] running offsets
-    int* run = cnt + E;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        cnt[e] = 0;
-    __syncthreads();
-
-    // ---- top-k and softmax weights, one warp per token ----
-    for (int tok = warp; tok < T; tok += nwarps) {
-        const float* lg = logits + (size_t)tok * E;
-        float mx = -INFINITY;
-        for (int e = lane; e < E; e += 32)
-            mx = fmaxf(mx, lg[e]);
-        for (int o = 16; o > 0; o >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float den = 0.f;
-        for (int e = lane; e < E; e += 32)
-            den += expf(lg[e] - mx);
-        for (int o = 16; o > 0; o >>= 1)
-            den += __shfl_xor_sync(0xffffffffu, den, o);
-        int chosen[8];
-        float wsum = 0.f;
-        for (int j = 0; j < topk; ++j) {
-            // best remaining logit; on equal values the lower id wins
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-            for (int e = lane; e < E; e += 32) {
-                bool taken = false;
-                for (int q = 0; q < j; ++q)
-                    taken |= chosen[q] == e;
-                const float v = lg[e];
-                if (!taken && (v > bv || (v == bv && e < bi) || bi == 0x7fffffff)) {
-                    bv = v;
-                    bi = e;
-                }
-            }
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            chosen[j] = bi;
-            const float w = expf(bv - mx) / den;
-            wsum += w;
-            if (lane == 0) {
-                ids[(size_t)tok * topk + j] = bi;
-                wts[(size_t)tok * topk + j] = w;
+    const int lane = threadIdx.x & 31;
+    const int tok = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    if (tok >= T)
+        return;
+    const float* lg = logits + (size_t)tok * E;
+    float mx = -INFINITY;
+    for (int e = lane; e < E; e += 32)
+        mx = fmaxf(mx, lg[e]);
+    for (int o = 16; o > 0; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float den = 0.f;
+    for (int e = lane; e < E; e += 32)
+        den += expf(lg[e] - mx);
+    for (int o = 16; o > 0; o >>= 1)
+        den += __shfl_xor_sync(0xffffffffu, den, o);
+    int chosen[8];
+    float w[8];
+    float wsum = 0.f;
+    for (int j = 0; j < topk; ++j) {
+        // best remaining logit; on equal values the lower id wins
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            bool taken = false;
+            for (int q = 0; q < j; ++q)
+                taken |= chosen[q] == e;
+            const float v = lg[e];
+            if (!taken && (v > bv || (v == bv && e < bi) || bi == 0x7fffffff)) {
+                bv = v;
+                bi = e;
             }
         }
-        if (renorm && lane == 0)
-            for (int j = 0; j < topk; ++j)
-                wts[(size_t)tok * topk + j] /= wsum;
-        if (lane == 0)
-            for (int j = 0; j < topk; ++j)
-                atomicAdd(&cnt[chosen[j]], 1);
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        chosen[j] = bi;
+        w[j] = expf(bv - mx) / den;
+        wsum += w[j];
+    }
+    if (lane == 0)
+        for (int j = 0; j < topk; ++j) {
+            ids[(size_t)tok * topk + j] = chosen[j];
+            wts[(size_t)tok * topk + j] = renorm ? w[j] / wsum : w[j];
+        }
+}
+
+// Stable counting sort of the P = T * topk (token, slot) pairs by expert in
+// one CTA: warp v owns the slots [v L, (v + 1) L).  Per-warp counts per
+// expert give each expert's total and offset and each warp's base inside
+// the expert; each warp then places its slots in slot order, so an expert's
+// rows keep the slot order (deterministic).
+__global__ void __launch_bounds__(kSortWarps * 32)
+    route_sort_kernel(const int* __restrict__ ids, int P, int E, int topk, int* __restrict__ pos,
+                      int* __restrict__ offsets, int* __restrict__ perm_tok)
+{
+    extern __shared__ int sm[];
+    int* base = sm;                      // [kSortWarps][E]: counts, then bases
+    int* off = sm + kSortWarps * E;      // [E] expert offsets
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int L = (P + kSortWarps - 1) / kSortWarps;
+    const int s0 = warp * L, s1 = min(P, s0 + L);
+    for (int i = threadIdx.x; i < kSortWarps * E; i += blockDim.x)
+        base[i] = 0;
+    __syncthreads();
+    for (int slot = s0 + lane; slot < s1; slot += 32)
+        atomicAdd(&base[warp * E + ids[slot]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int v = 0; v < kSortWarps; ++v) {
+            const int c = base[v * E + e];
+            base[v * E + e] = run;
+            run += c;
+        }
+        off[e] = run;  // the expert's total, for the scan below
     }
     __syncthreads();
-
-    // ---- expert offsets (exclusive scan) and the stable counting sort ----
     if (warp == 0) {
         int carry = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const int c = e < E ? cnt[e] : 0;
+        for (int b = 0; b < E; b += 32) {
+            const int e = b + lane;
+            const int c = e < E ? off[e] : 0;
             int incl = c;
             for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                const int x = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o)
-                    incl += v;
+                    incl += x;
             }
             if (e < E) {
+                off[e] = carry + incl - c;
                 offsets[e] = carry + incl - c;
-                run[e] = carry + incl - c;
             }
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0)
             offsets[E] = carry;
+    }
+    __syncthreads();
+    int* my = base + warp * E;
+    for (int b = s0; b < s1; b += 32) {
+        const int slot = b + lane;
+        const bool ok = slot < s1;
+        const int e = ok ? ids[slot] : -1 - lane;  // unique dummies for idle lanes
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        int p = 0;
+        if (ok)
+            p = off[e] + my[e] + rank;
         __syncwarp();
-        const int P = T * topk;
-        for (int base = 0; base < P; base += 32) {
-            const int slot = base + lane;
-            const bool ok = slot < P;
-            const int e = ok ? ids[slot] : -1 - lane;  // unique dummies for idle lanes
-            const unsigned same = __match_any_sync(0xffffffffu, e);
-            const int rank = __popc(same & ((1u << lane) - 1u));
-            int p = 0;
-            if (ok)
-                p = run[e] + rank;
-            __syncwarp();
-            if (ok) {
-                pos[slot] = p;
-                perm_tok[p] = slot / topk;
-                if (rank == __popc(same) - 1)  // last lane of this expert's group
-                    run[e] += __popc(same);
-            }
-            __syncwarp();
+        if (ok) {
+            pos[slot] = p;
+            perm_tok[p] = slot / topk;
+            if (rank == __popc(same) - 1)  // last lane of this expert's group
+                my[e] += __popc(same);
         }
+        __syncwarp();
     }
 }
 
@@ -215,17 +238,37 @@ cudaError_t launch_moe(const void* A, const float* logits, const uint8_t* fc1, c
     uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
     float* y = reinterpret_cast<float*>(ws + L.y);
 
-    route_sort_kernel<<<1, kRouteThreads, 2 * E * (int)sizeof(int), s>>>(
-        logits, T, E, topk, renorm, ids, wts, pos, offsets, perm_tok);
+    route_topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(
+        logits, T, E, topk, renorm, ids, wts);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess)
         return err;
-
     const int P = T * topk;
+    const int sort_smem = (kSortWarps + 1) * E * (int)sizeof(int);
+    if ((err = cudaFuncSetAttribute(route_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    sort_smem)) != cudaSuccess)
+        return err;
+    route_sort_kernel<<<1, kSortWarps * 32, sort_smem, s>>>(ids, P, E, topk, pos, offsets, perm_tok);
+    if ((err = cudaGetLastError()) != cudaSuccess)
+        return err;
+
     gather_rows_kernel<<<P, 128, 0, s>>>(static_cast<const uint4*>(A), perm_tok,
                                          reinterpret_cast<uint4*>(a_sorted), H / 8);
     if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
+
+    if (moe_tc_supported(H, I)) {
+        // tensor-core expert GEMMs: fc1 (gated) into h, fc2 into fp32 y
+        unsigned* errw = reinterpret_cast<unsigned*>(ws);
+        if ((err = launch_moe_tc(true, ACT, a_sorted, P, H, fc1, fc1_s, E, 2 * I, I, offsets, h,
+                                 errw, s)) != cudaSuccess)
+            return err;
+        if ((err = launch_moe_tc(false, ACT, h, P, I, fc2, fc2_s, E, H, 0, offsets, y, errw, s)) !=
+            cudaSuccess)
+            return err;
+        combine_kernel<ACT><<<T, 256, 0, s>>>(y, pos, wts, static_cast<uint16_t*>(out), H, topk);
+        return cudaGetLastError();
+    }
 
     // fc1 with the gated activation, on the rows in expert order
     StreamPlan P1 = plan_stream(64, 2 * I, H, H, 8, OUT_GATED, I);

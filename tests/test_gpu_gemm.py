@@ -70,6 +70,8 @@ SMALL = [
     (300, 9792, 512, 4, 64, inputs.BF16, True, True),   # 4-bit 256 x 128 tiles, ragged m and n
     (300, 19520, 512, 8, -1, inputs.F16, False, True),  # 256 x 256 tiles, ragged m and n
     (260, 19584, 512, 4, 64, inputs.BF16, True, False), # 4-bit 256 x 256 tiles, ragged
+    (200, 320, 6144, 8, -1, inputs.BF16, False, True),  # k split in 2, ragged m and n
+    (130, 448, 12288, 4, 64, inputs.BF16, True, True),  # 4-bit, k split in 4, ragged
 ]
 
 
@@ -125,8 +127,10 @@ def test_w4_g64(wo, case):
 
 # ---------------------------------------------------------- properties -----
 
-@pytest.mark.parametrize("config,case", [(2, 3), (2, 11), (3, 1), (4, 6)])
+@pytest.mark.parametrize("config,case", [(2, 3), (2, 11), (3, 1), (4, 6), (4, 9)])
 def test_deterministic_bit_identical(wo, config, case):
+    # (4, 9) splits k: the partial sums are added in split order whichever
+    # unit arrives last, and the per-tile counters return to zero
     dc = DeviceCase(inputs.workload_case(config, case))
     C1 = dc.run().clone()
     C2 = dc.run().clone()

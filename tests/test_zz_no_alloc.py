@@ -54,9 +54,9 @@ def test_noalloc_matches_wo_gemm(wo, m, n, k, bits, group, act, zeros, bias):
         assert st == 0, wo.wo_status_string(st)
         torch.cuda.synchronize()
         got = from_device_bits(out)
+        # within tolerance, not bit for bit: for some shapes wo_gemm splits k
+        # through its workspace, which the built-in scratch does not do
         assert_within_tolerance(got, act, inputs_to_f64(ref_bits, act), "no-alloc vs wo_gemm")
-        if m >= 65:                   # same kernel as wo_gemm picks: identical bits
-            assert np.array_equal(got, ref_bits)
 
 
 def inputs_to_f64(bits, act):

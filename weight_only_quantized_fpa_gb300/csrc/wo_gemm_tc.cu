@@ -95,6 +95,9 @@ struct TcParams {
     int group;               // codes per group
     int vec_ok;              // scales and bias 16-byte aligned: vector loads allowed
     int m_fast;              // tile walk: m fastest (else n fastest)
+    int splits;              // k split: units per output tile (1: none)
+    float* partial;          // splits > 1: fp32 partial tiles, [tile * splits + s][h][BN / 32][128][32]
+    unsigned* counters;      // splits > 1: per-tile arrival counters (kept at zero between calls)
     unsigned* err;           // workspace error word
 };
 
@@ -106,6 +109,7 @@ struct Barriers {
     uint64_t mma_done;             // every MMA issued has completed (teardown)
     uint32_t tmem_base;
     int abort;
+    int is_last;                   // k split: this CTA reduces the tile
 };
 
 // Output tile `t` of the persistent walk.  The operand that is larger in
@@ -252,11 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_kb = p.num_kb;
-    const int total_tiles = p.m_tiles * p.n_tiles;
-    const int my_tiles =
-        (int)blockIdx.x < total_tiles ? (total_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int total = my_tiles * num_kb;  // k blocks this CTA runs, over all its tiles
+    // work units: (output tile, k range); unit u is tile u / splits, k blocks
+    // [(u % splits) kps, + kps)
+    const int splits = p.splits, kps = p.num_kb / splits;
+    const int total_units = p.m_tiles * p.n_tiles * splits;
+    const int my_tiles =  // units this CTA runs
+        (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int total = my_tiles * kps;  // k blocks this CTA runs, over all its units
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::SA; ++s) {
@@ -300,9 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int c = 0;  // k blocks issued, over all tiles
             bool ok = true;
             for (int it = 0; it < my_tiles && ok; ++it) {
+                const int u = (int)blockIdx.x + it * (int)gridDim.x;
                 int m0, n0;
-                tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, TM, BN, m0, n0);
-                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                tile_coords(p, u / splits, TM, BN, m0, n0);
+                const int kb0 = (u % splits) * kps;
+                for (int kb = kb0; kb < kb0 + kps; ++kb, ++c) {
                     const int s = c % S;
                     if (!mbar_wait_bounded(&empty[s], ((c / S) & 1) ^ 1, abort, p.err, codes ? 1 : 9,
                                            kWaitLimitNs)) {
@@ -345,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * MS * BN);
-                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                const int kb0 = (((int)blockIdx.x + it * (int)gridDim.x) % splits) * kps;
+                for (int kb = kb0; kb < kb0 + kps; ++kb, ++c) {
                     const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
                     if (!mbar_wait_bounded(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 2,
                                            kWaitLimitNs) ||
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < BK / 16; ++j)  // +32 bytes per 16-wide k step
                             mma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
-                                    idesc, (kb > 0 || j > 0) ? 1u : 0u);
+                                    idesc, (kb > kb0 || j > 0) ? 1u : 0u);
                     }
                     mma_commit(&bars->emptyA[sa]);
                     mma_commit(&bars->empty2[s2]);
@@ -380,80 +389,173 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
         // ---- epilogue: TMEM lane quadrant q = warp % 4 ----
         const int q = warp - kEpilogueWarp0;
+        // scale (8-bit) or row scale (4-bit), bias, one rounding: 32 values of
+        // row `row`, columns nc..nc+31
+        auto finish = [&](int row, int nc, float rs, const float (&v)[32]) {
+            uint32_t sc[16], bi[16];
+            if constexpr (BITS == 8)
+                load32_u16(p.scales + nc, p.vec_ok != 0, sc);
+            if (p.bias)
+                load32_u16(p.bias + nc, p.vec_ok != 0, bi);
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float v0 = v[2 * j], v1 = v[2 * j + 1];
+                if constexpr (BITS == 8) {
+                    v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
+                    v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
+                } else {
+                    v0 *= rs;
+                    v1 *= rs;
+                }
+                if (p.bias) {
+                    v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
+                    v1 += to_f32<ACT>((uint16_t)(bi[j] >> 16));
+                }
+                packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.n + nc);
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                dst[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
+        };
+        volatile int* is_last = &bars->is_last;
         for (int it = 0; it < my_tiles; ++it) {
+            const int u = (int)blockIdx.x + it * (int)gridDim.x;
+            const int tile = u / splits;
             const int acc = it % Cfg::NACC, use = it / Cfg::NACC;
             int m0, n0;
-            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, TM, BN, m0, n0);
-            const bool ok = mbar_wait_bounded(&bars->tfull[acc], use & 1, abort, p.err, 6,
-                                              kWaitLimitNs);
-            if (!__all_sync(0xffffffffu, ok && !*abort))  // tcgen05.ld needs the whole warp
-                break;
-            tc_fence_after();
+            tile_coords(p, tile, TM, BN, m0, n0);
+            const bool got = mbar_wait_bounded(&bars->tfull[acc], use & 1, abort, p.err, 6,
+                                               kWaitLimitNs);
+            const bool live = __all_sync(0xffffffffu, got && !*abort);  // tcgen05.ld: whole warp
+            if (splits == 1) {
+                if (!live)
+                    break;
+                tc_fence_after();
 #pragma unroll 1
-            for (int h = 0; h < MS; ++h) {
-                const int row = m0 + h * BM + q * 32 + lane;
-                float rs = 1.f;
-                if (p.rowscale && row < p.m)
-                    rs = p.rowscale[row];
+                for (int h = 0; h < MS; ++h) {
+                    const int row = m0 + h * BM + q * 32 + lane;
+                    const float rs = (p.rowscale && row < p.m) ? p.rowscale[row] : 1.f;
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    const int nc = n0 + cc * 32;
-                    if (nc >= p.n)
-                        break;
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) +
-                                           (uint32_t)((acc * MS + h) * BN + cc * 32),
-                                       r);
-                    uint32_t sc[16], bi[16];
-                    if constexpr (BITS == 8)
-                        load32_u16(p.scales + nc, p.vec_ok != 0, sc);
-                    if (p.bias)
-                        load32_u16(p.bias + nc, p.vec_ok != 0, bi);
-                    tmem_ld_wait();
-                    if (row < p.m) {
-                        uint32_t packed[16];
+                    for (int cc = 0; cc < BN / 32; ++cc) {
+                        const int nc = n0 + cc * 32;
+                        if (nc >= p.n)
+                            break;
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) +
+                                               (uint32_t)((acc * MS + h) * BN + cc * 32),
+                                           r);
+                        tmem_ld_wait();
+                        if (row < p.m) {
+                            float v[32];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
-                            if constexpr (BITS == 8) {
-                                v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
-                                v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
-                            } else {
-                                v0 *= rs;
-                                v1 *= rs;
-                            }
-                            if (p.bias) {
-                                v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
-                                v1 += to_f32<ACT>((uint16_t)(bi[j] >> 16));
-                            }
-                            packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __uint_as_float(r[j]);
+                            finish(row, nc, rs, v);
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.n + nc);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                                packed[4 * v + 3]);
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(&bars->tempty[acc]);
+                continue;
+            }
+            // ---- k split: this unit's accumulator -> its fp32 partial tile; the
+            // unit that arrives last at the tile's counter sums the partials in
+            // split order and writes C (deterministic, and no unit waits) ----
+            float* part = p.partial + (size_t)u * TM * BN;
+            if (live) {
+                tc_fence_after();
+                for (int h = 0; h < MS; ++h)
+#pragma unroll 1
+                    for (int cc = 0; cc < BN / 32; ++cc) {
+                        if (n0 + cc * 32 >= p.n)
+                            break;
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) +
+                                               (uint32_t)((acc * MS + h) * BN + cc * 32),
+                                           r);
+                        tmem_ld_wait();
+                        // [h][cc][row of the sub-tile][32]: a warp writes 4 KiB contiguously
+                        float4* dst = reinterpret_cast<float4*>(
+                            part + ((size_t)(h * (BN / 32) + cc) * BM + q * 32 + lane) * 32);
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+                            dst[w] = make_float4(__uint_as_float(r[4 * w]), __uint_as_float(r[4 * w + 1]),
+                                                 __uint_as_float(r[4 * w + 2]), __uint_as_float(r[4 * w + 3]));
+                    }
             }
             tc_fence_before();
             mbar_arrive(&bars->tempty[acc]);
+            __threadfence();
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+            if (warp == kEpilogueWarp0 && lane == 0) {
+                if (*abort) {
+                    *is_last = -1;
+                } else {
+                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
+                    *is_last = prev == (unsigned)(splits - 1) ? 1 : 0;
+                }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const int last = *is_last;
+            if (last < 0)
+                break;  // every epilogue warp read the same value
+            if (last) {
+                __threadfence();
+#pragma unroll 1
+                for (int h = 0; h < MS; ++h) {
+                    const int row = m0 + h * BM + q * 32 + lane;
+                    const float rs = (p.rowscale && row < p.m) ? p.rowscale[row] : 1.f;
+#pragma unroll 1
+                    for (int cc = 0; cc < BN / 32; ++cc) {
+                        const int nc = n0 + cc * 32;
+                        if (nc >= p.n)
+                            break;
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = 0.f;
+                        for (int sp = 0; sp < splits; ++sp) {
+                            const float4* src = reinterpret_cast<const float4*>(
+                                p.partial + (size_t)(tile * splits + sp) * TM * BN +
+                                ((size_t)(h * (BN / 32) + cc) * BM + q * 32 + lane) * 32);
+#pragma unroll
+                            for (int w = 0; w < 8; ++w) {
+                                const float4 x = __ldcg(src + w);
+                                v[4 * w] += x.x;
+                                v[4 * w + 1] += x.y;
+                                v[4 * w + 2] += x.z;
+                                v[4 * w + 3] += x.w;
+                            }
+                        }
+                        if (row < p.m)
+                            finish(row, nc, rs, v);
+                    }
+                }
+                if (warp == kEpilogueWarp0 && lane == 0)
+                    p.counters[tile] = 0u;  // ready for the next call
+            }
         }
     } else if (warp >= kDequantWarp0) {
         // ---- dequantisation ----
         const int dw = warp - kDequantWarp0;
         auto n0_of = [&](int c) {
-            const int it = c / num_kb;
+            const int u = (int)blockIdx.x + (c / kps) * (int)gridDim.x;
             int m0, n0;
-            tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, TM, BN, m0, n0);
+            tile_coords(p, u / splits, TM, BN, m0, n0);
             return n0;
+        };
+        auto kb_of = [&](int c) {  // k block of the CTA's c-th k block
+            const int u = (int)blockIdx.x + (c / kps) * (int)gridDim.x;
+            return (u % splits) * kps + c % kps;
         };
         DqScales<BITS, BN> buf[Cfg::PF];
         if constexpr (BITS == 4) {
 #pragma unroll
             for (int j = 0; j < Cfg::PF; ++j)
                 if (j < total)
-                    load_scales<BITS, BN>(p, n0_of(j), j % num_kb, dw, lane, buf[j]);
+                    load_scales<BITS, BN>(p, n0_of(j), kb_of(j), dw, lane, buf[j]);
         }
         bool ok = true;
         for (int c0 = 0; c0 < total && ok; c0 += Cfg::PF) {
@@ -481,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&bars->emptyC[sc]);
                 if constexpr (BITS == 4) {
                     if (c + Cfg::PF < total)
-                        load_scales<BITS, BN>(p, n0_of(c + Cfg::PF), (c + Cfg::PF) % num_kb, dw,
+                        load_scales<BITS, BN>(p, n0_of(c + Cfg::PF), kb_of(c + Cfg::PF), dw,
                                               lane, buf[j]);
                 }
             }
@@ -573,8 +675,8 @@ cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaS
         return e;
     tp.m_tiles = (tp.m + BM * MS - 1) / (BM * MS);
     tp.n_tiles = (tp.n + BN - 1) / BN;
-    const long long tiles = (long long)tp.m_tiles * tp.n_tiles;
-    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+    const long long units = (long long)tp.m_tiles * tp.n_tiles * tp.splits;
+    const int grid = (int)(units < num_sms() ? units : num_sms());
     // packed codes viewed as [n/16 rows] x [bytes per 16-channel row / 4] words;
     // one box = BN/16 rows x one k block
     CUtensorMap mc;
@@ -587,9 +689,9 @@ cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaS
 }
 
 template <int BITS, int OT, int ACT>
-cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& tp, cudaStream_t s)
+cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& tp, const TcPlan& sh,
+                         cudaStream_t s)
 {
-    const TcShape sh = tc_shape(tp.m, tp.n, BITS);
     if (sh.ms == 2)
         return sh.bn == 256 ? launch_tc_t<BITS, OT, ACT, 256, 2>(ma, B, tp, s)
                             : launch_tc_t<BITS, OT, ACT, 128, 2>(ma, B, tp, s);
@@ -908,12 +1010,32 @@ cudaError_t launch_moe_tc_t(const CUtensorMap& ma, const CUtensorMap& mc, const 
 
 }  // namespace
 
-TcPlan plan_tc(int m, int n, int k, int bits, int act)
+TcPlan plan_tc(int m, int n, int k, int bits, int act, bool allow_split)
 {
     TcPlan p{};
+    const TcShape sh = tc_shape(m, n, bits);
+    p.bn = sh.bn;
+    p.ms = sh.ms;
+    p.splits = 1;
+    const int num_kb = k / BK;
+    const long long tiles256 = (long long)((m + BM - 1) / BM) * ((n + 255) / 256);
+    if (allow_split && sh.ms == 1) {
+        // too few 128 x 256 tiles for the SMs and a long k: split k instead of
+        // narrowing the tiles (each unit keeps at least 48 k blocks, so the
+        // partial tiles' round trip through the workspace stays small; the
+        // per-tile counters live in the workspace's counter area)
+        for (int sp = 8; sp >= 2; sp /= 2)
+            if (num_kb % sp == 0 && num_kb / sp >= 48 && tiles256 * sp <= num_sms() &&
+                tiles256 <= (long long)kWsCounters) {
+                p.bn = 256;
+                p.splits = sp;
+                break;
+            }
+    }
     p.a16_bytes = (bits == 4 && act == WO_BF16) ? align_up((size_t)m * k * 2, 256) : 0;
     p.rowscale_bytes = p.a16_bytes ? align_up((size_t)m * 4, 256) : 0;
-    p.ws_bytes = kWsScratch + p.a16_bytes + p.rowscale_bytes;
+    p.partial_bytes = p.splits > 1 ? align_up((size_t)tiles256 * p.splits * BM * 256 * 4, 256) : 0;
+    p.ws_bytes = kWsScratch + p.a16_bytes + p.rowscale_bytes + p.partial_bytes;
     return p;
 }
 
@@ -934,6 +1056,11 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     tp.vec_ok = (reinterpret_cast<uintptr_t>(a.scales) % 16 == 0) &&
                 (reinterpret_cast<uintptr_t>(a.bias) % 16 == 0);
     tp.err = reinterpret_cast<unsigned*>(ws);
+    tp.splits = plan.splits;
+    tp.counters = reinterpret_cast<unsigned*>(ws + kWsHeader);
+    tp.partial = plan.splits > 1
+                     ? reinterpret_cast<float*>(ws + kWsScratch + plan.a16_bytes + plan.rowscale_bytes)
+                     : nullptr;
     // stream the larger operand once (A: m*k*2 bytes, codes: n*k*bits/8)
     tp.m_fast = (double)a.m * 2.0 <= (double)a.n * a.bits / 8.0;
 
@@ -955,10 +1082,10 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (a.bits == 8)
-        return a.act == WO_F16 ? launch_tc_bn<8, ACT_F16, ACT_F16>(ma, a.B, tp, s)
-                               : launch_tc_bn<8, ACT_BF16, ACT_BF16>(ma, a.B, tp, s);
-    return a.act == WO_F16 ? launch_tc_bn<4, ACT_F16, ACT_F16>(ma, a.B, tp, s)
-                           : launch_tc_bn<4, ACT_F16, ACT_BF16>(ma, a.B, tp, s);
+        return a.act == WO_F16 ? launch_tc_bn<8, ACT_F16, ACT_F16>(ma, a.B, tp, plan, s)
+                               : launch_tc_bn<8, ACT_BF16, ACT_BF16>(ma, a.B, tp, plan, s);
+    return a.act == WO_F16 ? launch_tc_bn<4, ACT_F16, ACT_F16>(ma, a.B, tp, plan, s)
+                           : launch_tc_bn<4, ACT_F16, ACT_BF16>(ma, a.B, tp, plan, s);
 }
 
 }  // namespace wo

@@ -54,12 +54,16 @@ cudaError_t launch_stream_gemm(const GemmArgs& a, cudaStream_t s);
 constexpr int kTcMinM = 65;  // m at and above which wo_gemm uses the tensor-core kernel
 
 struct TcPlan {
+    int bn, ms;             // output tile: ms x 128 rows by bn columns
+    int splits;             // k split (units per tile); 1: none
     size_t a16_bytes;       // fp16 copy of a bf16 A (4-bit weights only)
     size_t rowscale_bytes;  // its per-row power-of-two scales
+    size_t partial_bytes;   // k split: fp32 partial tiles
     size_t ws_bytes;        // total, header and counter area included
 };
 
-TcPlan plan_tc(int m, int n, int k, int bits, int act);
+// allow_split = false plans without the k split (no partial-tile scratch).
+TcPlan plan_tc(int m, int n, int k, int bits, int act, bool allow_split = true);
 cudaError_t launch_tc(const GemmArgs& a, const TcPlan& p, cudaStream_t s);
 
 // MoE expert GEMMs on the tensor cores (8-bit codes; hidden and inter

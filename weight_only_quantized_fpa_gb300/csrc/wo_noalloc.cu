@@ -32,7 +32,7 @@ namespace {
 // e.g. m * k <= 8,388,608 with m <= 65,536.
 constexpr size_t kNoAllocBytes = kWsScratch + ((size_t)16 << 20) + ((size_t)256 << 10);
 
-__device__ __align__(256) unsigned char g_scratch[kNoAllocBytes];
+static __device__ __align__(256) unsigned char g_scratch[kNoAllocBytes];
 
 std::mutex g_mu;
 void* g_addr[64] = {nullptr};
@@ -89,7 +89,7 @@ extern "C" wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed,
         !aligned16(C) || !aligned2(scales) || (zeros && !aligned2(zeros)) ||
         (bias && !aligned2(bias)))
         return WO_ERR_INVALID_ARG;
-    const TcPlan plan = plan_tc(m, n, k, bits, act_dtype);
+    const TcPlan plan = plan_tc(m, n, k, bits, act_dtype, false);  // no k split: no partial tiles
     if (plan.a16_bytes > ((size_t)16 << 20) || plan.rowscale_bytes > ((size_t)256 << 10) ||
         plan.ws_bytes > kNoAllocBytes)
         return WO_ERR_WORKSPACE;  // the problem needs more scratch than is built in

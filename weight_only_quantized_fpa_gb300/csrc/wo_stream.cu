@@ -339,11 +339,32 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         const int g_lo = GROUPED ? c0 / p.tiles_per_group : 0;
         if (GROUPED && active) {
             const int gc = (c1 - 1) / p.tiles_per_group - g_lo + 1;
-            for (int idx = lane; idx < 32 * gc; idx += 32) {
-                const int ch = idx / gc, gg = idx % gc;
-                const size_t src = (size_t)(blk[ch >> 4] * 16 + (ch & 15)) * p.G + g_lo + gg;
-                ws_s[ch * p.g_span + gg] = ld_nc_u16(sx + src);
-                ws_z[ch * p.g_span + gg] = p.zeros ? ld_nc_u16(p.zeros + src) : (uint16_t)0;
+            // batches of 8 per lane: all 16 loads in flight before the stores
+            // (one memory round trip per batch, not two per value)
+            constexpr int NB = 8;
+            for (int base = 0; base < 32 * gc; base += 32 * NB) {
+                uint16_t sv[NB], zv[NB];
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const int idx = base + b * 32 + lane;
+                    sv[b] = zv[b] = 0;
+                    if (idx < 32 * gc) {
+                        const int ch = idx / gc, gg = idx % gc;
+                        const size_t src = (size_t)(blk[ch >> 4] * 16 + (ch & 15)) * p.G + g_lo + gg;
+                        sv[b] = ld_nc_u16(sx + src);
+                        if (p.zeros)
+                            zv[b] = ld_nc_u16(p.zeros + src);
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const int idx = base + b * 32 + lane;
+                    if (idx < 32 * gc) {
+                        const int ch = idx / gc, gg = idx % gc;
+                        ws_s[ch * p.g_span + gg] = sv[b];
+                        ws_z[ch * p.g_span + gg] = zv[b];
+                    }
+                }
             }
             __syncwarp();
         }

@@ -184,7 +184,9 @@ WO_API wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed, cons
  * Synchronises `stream`, then reads and clears the error word a kernel may
  * have left in `workspace` (a tensor-core kernel that gave up a bounded wait
  * writes it instead of hanging).  Returns WO_OK, WO_ERR_TIMEOUT, or
- * WO_ERR_CUDA when the stream reported an error.
+ * WO_ERR_CUDA when the stream reported an error.  After WO_ERR_TIMEOUT the
+ * workspace's counters may not be back at zero: zero-fill the workspace
+ * again before its next use.
  */
 WO_API wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, void* stream);
 

@@ -190,6 +190,19 @@ WO_API wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed, cons
  */
 WO_API wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages): launches one
+ * CTA whose thread waits on an mbarrier that nothing ever arrives on, with
+ * the same bounded wait the kernels use but a limit of `limit_us`
+ * microseconds (1..1000000).  The wait runs out, the CTA records its error
+ * code in `workspace`'s error word and exits; the GPU is not left hanging
+ * and the context stays usable.  wo_check_workspace then returns
+ * WO_ERR_TIMEOUT (and clears the word).  workspace: at least 256 bytes,
+ * 256-byte aligned.
+ */
+WO_API wo_status wo_selftest_wait_timeout(void* workspace, size_t workspace_bytes, unsigned limit_us,
+                                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["wo_pack", "wo_unpack", "wo_packed_bytes", "wo_workspace_size", "wo_gemm",
-              "wo_moe_workspace_size", "wo_moe_ffn", "wo_status_string", "wo_check_workspace"]:
+              "wo_moe_workspace_size", "wo_moe_ffn", "wo_status_string", "wo_check_workspace",
+              "wo_selftest_wait_timeout"]:
         assert n in names
 
 
@@ -125,3 +126,18 @@ def test_noalloc_entry_validates_before_any_cuda_call(lib):
     assert f(4096, 8192, 64, 64, None, 16384, 512, 256, 2048, -1, 8, 0, None) == 2
     assert f(4096, 8192, 64, None, None, 16384, 4096, 256, 4096, 64, 4, 1, None) == 3
     assert f(4096, 8192, 64, None, None, 16384, 0, 256, 2048, 64, 4, 1, None) == 0
+
+
+def test_selftest_rejects_bad_arguments_without_launching(lib):
+    # argument errors come back before any launch (nothing runs on the CPU machine)
+    import ctypes
+    buf = ctypes.create_string_buffer(1024)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    f = lib.wo_selftest_wait_timeout
+    f.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(None, 256, 1000, None) == 1          # no workspace
+    assert f(addr, 128, 1000, None) == 1          # too small for the header
+    assert f(addr + 8, 256, 1000, None) == 1      # not 256-byte aligned
+    assert f(addr, 256, 0, None) == 1             # limit out of range
+    assert f(addr, 256, 2000000, None) == 1

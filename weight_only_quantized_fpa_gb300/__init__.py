@@ -20,7 +20,7 @@ __all__ = [
     "WO_F16", "WO_BF16", "WoError", "load_library", "library_path",
     "wo_status_string", "wo_packed_bytes", "wo_pack", "wo_unpack", "wo_workspace_size",
     "wo_gemm", "wo_moe_workspace_size", "wo_moe_ffn", "wo_check_workspace",
-    "wo_gemm_tc_noalloc",
+    "wo_gemm_tc_noalloc", "wo_selftest_wait_timeout",
     "pack", "unpack", "pack_experts", "gemm", "moe_ffn", "Workspace",
 ]
 
@@ -82,6 +82,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.wo_check_workspace.restype = I
         lib.wo_gemm_tc_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
         lib.wo_gemm_tc_noalloc.restype = I
+        lib.wo_selftest_wait_timeout.argtypes = [P, S, ctypes.c_uint, P]
+        lib.wo_selftest_wait_timeout.restype = I
         _lib = lib
         return lib
 
@@ -181,6 +183,12 @@ def wo_gemm_tc_noalloc(A, B_packed, scales, zeros, bias, C, m: int, n: int, k: i
                                              _ptr(bias), _ptr(C), m, n, k, group_size, bits,
                                              act_dtype, _stream_ptr(stream)),
            "wo_gemm_tc_noalloc")
+
+
+def wo_selftest_wait_timeout(workspace, workspace_bytes: int, limit_us: int, stream=None) -> None:
+    """Launch a wait that runs out after limit_us (the kernels' failure path)."""
+    _raise(load_library().wo_selftest_wait_timeout(_ptr(workspace), workspace_bytes, limit_us,
+                                                   _stream_ptr(stream)), "wo_selftest_wait_timeout")
 
 
 def wo_check_workspace(workspace, workspace_bytes: int, stream=None) -> int:

@@ -169,6 +169,26 @@ def test_output_overwrites_poisoned_buffer(wo):
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("m,n,k,bits,group", [(200, 384, 512, 8, -1), (4096, 4096, 1024, 8, -1),
+                                                (300, 448, 1024, 4, 64)])
+def test_output_16_byte_aligned(wo, m, n, k, bits, group):
+    # C 16- but not 32-byte aligned: the tensor-core epilogue stores 16 bytes
+    # at a time instead of 32
+    c = inputs.make_gemm_case(8, 95 + m, m, n, k, bits=bits, group_size=group, act_dtype=inputs.BF16,
+                              scale_lo=0.005 if bits == 4 else 0.001,
+                              scale_hi=0.02 if bits == 4 else 0.01, with_zeros=bits == 4,
+                              with_bias=True)
+    dc = DeviceCase(c)
+    buf = torch.empty(m * n + 8, dtype=dc.A.dtype, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    out = buf[8:].view(m, n)  # 16 bytes past a 32-byte boundary
+    dc.run(out=out)
+    torch.cuda.synchronize()
+    rows = sample_rows(m, 16)
+    assert_within_tolerance(from_device_bits(out)[rows], c.act_dtype, dc.oracle_rows(rows),
+                            "16-byte aligned C")
+
+
 def test_workspace_shared_across_shapes(wo):
     # calls of different kernels and shapes sharing one workspace, twice over:
     # a tensor-core call with a converted-activation scratch region, a

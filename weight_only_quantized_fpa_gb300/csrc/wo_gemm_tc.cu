@@ -93,8 +93,8 @@ struct TcParams {
     uint16_t* C;
     int G;                   // scale groups per channel row
     int group;               // codes per group
-    int vec_ok;              // scales and bias 16-byte aligned: vector loads allowed
     int m_fast;              // tile walk: m fastest (else n fastest)
+    int c_v8;                // C 32-byte aligned (and n % 16 == 0): 32-byte stores
     int splits;              // k split: units per output tile (1: none)
     float* partial;          // splits > 1: fp32 partial tiles, [tile * splits + s][h][BN / 32][128][32]
     unsigned* counters;      // splits > 1: per-tile arrival counters (kept at zero between calls)
@@ -219,25 +219,6 @@ __device__ __forceinline__ void dequant_stage(uint32_t c_s, const DqScales<BITS,
     }
 }
 
-// 32 consecutive 16-bit values (p 2-byte aligned; 16-byte aligned when vec).
-__device__ __forceinline__ void load32_u16(const uint16_t* p, bool vec, uint32_t (&w)[16])
-{
-    if (vec) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4*>(p + 8 * i);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            w[i] = (uint32_t)p[2 * i] | ((uint32_t)p[2 * i + 1] << 16);
-    }
-}
-
 template <int BITS, int OT, int ACT, int BN, int MS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
@@ -263,6 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int my_tiles =  // units this CTA runs
         (int)blockIdx.x < total_units ? (total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int total = my_tiles * kps;  // k blocks this CTA runs, over all its units
+    // one accumulator (its epilogue cannot overlap the next tile's MMAs): the
+    // dequantisation warps, idle while it drains, drain two thirds of it
+    const bool helpers = Cfg::NACC == 1 && splits == 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::SA; ++s) {
@@ -279,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars->tfull[a], 1);
-            mbar_init(&bars->tempty[a], 4 * 32);
+            mbar_init(&bars->tempty[a], helpers ? 4 * 32 + kDequantWarps : 4 * 32);
         }
         mbar_init(&bars->mma_done, 1);
         bars->abort = 0;
@@ -295,6 +279,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+
+    // A tile's column scales (8-bit) and bias are fetched into registers
+    // before its accumulator is ready, BN / 32 columns per lane (CW
+    // column pairs), so that their latency hides behind the MMAs; the
+    // drain gathers each 32-column chunk's values with shuffles.
+    constexpr int CW = BN / 64;
+    uint32_t csc[CW], cbi[CW];
+    auto col_pair = [&](const uint16_t* v, int col) -> uint32_t {
+        if (col >= p.n)
+            return 0u;
+        const uint32_t lo = __ldg(v + col);
+        return col + 1 < p.n ? lo | ((uint32_t)__ldg(v + col + 1) << 16) : lo;
+    };
+    auto stage_cols = [&](int n0) {
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+            const int col = n0 + 2 * (lane * CW + i);
+            csc[i] = BITS == 8 ? col_pair(p.scales, col) : 0u;
+            cbi[i] = p.bias ? col_pair(p.bias, col) : 0u;
+        }
+    };
+    // chunk cc's 32 scales and bias values, as 16 pairs (whole warp)
+    auto gather = [&](int cc, uint32_t (&sc)[16], uint32_t (&bi)[16]) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int src = (cc * 16 + j) / CW;
+            if constexpr (BITS == 8)  // 4-bit: the scales were applied to the codes
+                sc[j] = __shfl_sync(0xffffffffu, csc[j % CW], src);
+            if (p.bias)
+                bi[j] = __shfl_sync(0xffffffffu, cbi[j % CW], src);
+        }
+    };
+    // scale (8-bit) or row scale (4-bit), bias, one rounding: 32 values of
+    // row `row`, columns nc..nc+31
+    auto finish = [&](int row, int nc, float rs, const float (&v)[32], const uint32_t (&sc)[16],
+                      const uint32_t (&bi)[16]) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            float v0 = v[2 * j], v1 = v[2 * j + 1];
+            if constexpr (BITS == 8) {
+                v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
+                v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
+            } else {
+                v0 *= rs;
+                v1 *= rs;
+            }
+            if (p.bias) {
+                v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
+                v1 += to_f32<ACT>((uint16_t)(bi[j] >> 16));
+            }
+            packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
+        }
+        uint16_t* dst = p.C + (size_t)row * p.n + nc;
+        if (p.c_v8) {  // two 32-byte stores: whole sectors
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+                st_global_v8(dst + 16 * w, &packed[8 * w]);
+        } else {
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                reinterpret_cast<uint4*>(dst)[w] =
+                    make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
+        }
+    };
+    // TMEM -> C for the chunks x = part, part + nparts, ... of unit `it`'s
+    // accumulator (x walks the MS sub-tiles' 32-column chunks), rows of this
+    // warp's TMEM lane quadrant; stage_cols(n0) of the tile came first
+    auto drain = [&](int it, int part, int nparts) {
+        const int acc = it % Cfg::NACC, qd = warp & 3;
+        int m0, n0;
+        tile_coords(p, ((int)blockIdx.x + it * (int)gridDim.x) / splits, TM, BN, m0, n0);
+#pragma unroll 1
+        for (int x = part; x < MS * (BN / 32); x += nparts) {
+            const int h = x / (BN / 32), cc = x % (BN / 32);
+            const int nc = n0 + cc * 32;
+            if (nc >= p.n)
+                continue;
+            const int row = m0 + h * BM + qd * 32 + lane;
+            const float rs = (p.rowscale && row < p.m) ? p.rowscale[row] : 1.f;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)((acc * MS + h) * BN + cc * 32),
+                               r);
+            tmem_ld_wait();
+            uint32_t sc[16], bi[16];
+            gather(cc, sc, bi);
+            if (row < p.m) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __uint_as_float(r[j]);
+                finish(row, nc, rs, v, sc, bi);
+            }
+        }
+    };
+
 
     if (warp == 0 || warp == 2) {
         if (lane == 0) {
@@ -389,36 +469,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
         // ---- epilogue: TMEM lane quadrant q = warp % 4 ----
         const int q = warp - kEpilogueWarp0;
-        // scale (8-bit) or row scale (4-bit), bias, one rounding: 32 values of
-        // row `row`, columns nc..nc+31
-        auto finish = [&](int row, int nc, float rs, const float (&v)[32]) {
-            uint32_t sc[16], bi[16];
-            if constexpr (BITS == 8)
-                load32_u16(p.scales + nc, p.vec_ok != 0, sc);
-            if (p.bias)
-                load32_u16(p.bias + nc, p.vec_ok != 0, bi);
-            uint32_t packed[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float v0 = v[2 * j], v1 = v[2 * j + 1];
-                if constexpr (BITS == 8) {
-                    v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
-                    v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
-                } else {
-                    v0 *= rs;
-                    v1 *= rs;
-                }
-                if (p.bias) {
-                    v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
-                    v1 += to_f32<ACT>((uint16_t)(bi[j] >> 16));
-                }
-                packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(p.C + (size_t)row * p.n + nc);
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-                dst[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
-        };
         volatile int* is_last = &bars->is_last;
         for (int it = 0; it < my_tiles; ++it) {
             const int u = (int)blockIdx.x + it * (int)gridDim.x;
@@ -426,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = it % Cfg::NACC, use = it / Cfg::NACC;
             int m0, n0;
             tile_coords(p, tile, TM, BN, m0, n0);
+            stage_cols(n0);
             const bool got = mbar_wait_bounded(&bars->tfull[acc], use & 1, abort, p.err, 6,
                                                kWaitLimitNs);
             const bool live = __all_sync(0xffffffffu, got && !*abort);  // tcgen05.ld: whole warp
@@ -433,29 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!live)
                     break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int h = 0; h < MS; ++h) {
-                    const int row = m0 + h * BM + q * 32 + lane;
-                    const float rs = (p.rowscale && row < p.m) ? p.rowscale[row] : 1.f;
-#pragma unroll 1
-                    for (int cc = 0; cc < BN / 32; ++cc) {
-                        const int nc = n0 + cc * 32;
-                        if (nc >= p.n)
-                            break;
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) +
-                                               (uint32_t)((acc * MS + h) * BN + cc * 32),
-                                           r);
-                        tmem_ld_wait();
-                        if (row < p.m) {
-                            float v[32];
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                v[j] = __uint_as_float(r[j]);
-                            finish(row, nc, rs, v);
-                        }
-                    }
-                }
+                drain(it, 0, helpers ? 3 : 1);
                 tc_fence_before();
                 mbar_arrive(&bars->tempty[acc]);
                 continue;
@@ -529,8 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 v[4 * w + 3] += x.w;
                             }
                         }
+                        uint32_t sc[16], bi[16];
+                        gather(cc, sc, bi);
                         if (row < p.m)
-                            finish(row, nc, rs, v);
+                            finish(row, nc, rs, v, sc, bi);
                     }
                 }
                 if (warp == kEpilogueWarp0 && lane == 0)
@@ -557,8 +588,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j < total)
                     load_scales<BITS, BN>(p, n0_of(j), kb_of(j), dw, lane, buf[j]);
         }
+        // drain part 1 + dw / 4 of three of unit t's accumulator (helpers)
+        auto help = [&](int t) {
+            int m0, n0;
+            tile_coords(p, ((int)blockIdx.x + t * (int)gridDim.x) / splits, TM, BN, m0, n0);
+            stage_cols(n0);
+            const bool got = mbar_wait_bounded(&bars->tfull[0], t & 1, abort, p.err, 13, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, got && !*abort))
+                return false;
+            tc_fence_after();
+            drain(t, 1 + dw / 4, 3);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->tempty[0]);
+            return true;
+        };
+        int nd = 0;  // next unit to help drain
         bool ok = true;
         for (int c0 = 0; c0 < total && ok; c0 += Cfg::PF) {
+            // unit nd's k blocks all dequantised (c0 >= B), and this group
+            // reaches block B + S2, whose operand stage only frees once the
+            // next unit's MMAs run, i.e. after unit nd's drain: help first
+            // (a group never holds both B - 1 and B + S2, as PF <= S2 + 1)
+            static_assert(Cfg::NACC == 2 || Cfg::PF <= Cfg::S2 + 1, "helper trigger");
+            while (helpers && ok && nd < my_tiles && c0 >= (nd + 1) * kps &&
+                   c0 + Cfg::PF - 1 >= (nd + 1) * kps + Cfg::S2)
+                ok = help(nd++);
 #pragma unroll
             for (int j = 0; j < Cfg::PF; ++j) {
                 const int c = c0 + j;
@@ -588,6 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        while (helpers && ok && nd < my_tiles)
+            ok = help(nd++);
     }
 
     tc_fence_before();
@@ -1053,8 +1111,7 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     tp.C = static_cast<uint16_t*>(a.C);
     tp.G = a.k / a.group;
     tp.group = a.group;
-    tp.vec_ok = (reinterpret_cast<uintptr_t>(a.scales) % 16 == 0) &&
-                (reinterpret_cast<uintptr_t>(a.bias) % 16 == 0);
+    tp.c_v8 = reinterpret_cast<uintptr_t>(a.C) % 32 == 0 && a.n % 16 == 0;
     tp.err = reinterpret_cast<unsigned*>(ws);
     tp.splits = plan.splits;
     tp.counters = reinterpret_cast<unsigned*>(ws + kWsHeader);

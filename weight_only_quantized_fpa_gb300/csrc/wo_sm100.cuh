@@ -140,6 +140,14 @@ __device__ __forceinline__ void cluster_wait()
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
+// 32 bytes (eight 32-bit words) to global memory; dst 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ TMA ----
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap)

@@ -67,9 +67,11 @@ SMALL = [
     (24, 256, 1024, 4, 128, inputs.F16, True, True),    # group 128, streaming kernel
     (200, 384, 512, 8, -1, inputs.BF16, False, True),   # tensor cores, ragged m and n tiles
     (300, 448, 1024, 4, 64, inputs.BF16, True, True),   # 4-bit, tensor cores, ragged
-    (300, 9792, 512, 4, 64, inputs.BF16, True, True),   # 4-bit 256 x 128 tiles, ragged m and n
-    (300, 19520, 512, 8, -1, inputs.F16, False, True),  # 256 x 256 tiles, ragged m and n
-    (260, 19584, 512, 4, 64, inputs.BF16, True, False), # 4-bit 256 x 256 tiles, ragged
+    (250, 12736, 512, 4, 64, inputs.BF16, True, True),  # 4-bit 256 x 128 tiles, ragged m and n
+    (300, 19520, 512, 8, -1, inputs.F16, False, True),  # 128 x 256 tiles, ragged m and n
+    (300, 15296, 512, 8, -1, inputs.F16, False, True),  # 256 x 256 tiles (drain helpers), ragged
+    (260, 19584, 512, 4, 64, inputs.BF16, True, False), # 4-bit 128 x 256 tiles, ragged
+    (300, 15296, 512, 4, 64, inputs.BF16, True, True),  # 4-bit 256 x 256 tiles, ragged
     (200, 320, 6144, 8, -1, inputs.BF16, False, True),  # k split in 2, ragged m and n
     (130, 448, 12288, 4, 64, inputs.BF16, True, True),  # 4-bit, k split in 4, ragged
 ]

@@ -9,9 +9,9 @@
 //
 // Persistent kernel: one CTA per SM walks output tiles of MS x 128 (m) by BN
 // (n) in the order tile_coords gives; tc_shape picks the shape (256 x 256
-// when the GPU stays full, so that every A and code byte fetched from L2
-// feeds the most FLOPs).  With MS = 2 two M=128 MMAs per k step share one
-// dequantised B tile.  Roles (16 warps):
+// unless narrower tiles fill the SMs in fewer waves, so that every A and
+// code byte fetched from L2 feeds the most FLOPs).  With MS = 2 two M=128
+// MMAs per k step share one dequantised B tile.  Roles (16 warps):
 //   warp 0       TMA producer of the packed code tiles (BN channels x 64 k)
 //                into the code ring;
 //   warp 2       TMA producer of the A tiles (128 x 64, 128-byte swizzle)
@@ -24,7 +24,9 @@
 //                lane quadrant per warp), apply scale[n] (8-bit) or the
 //                activation row scale (4-bit), add bias, round once, store C,
 //                and hand the accumulator back -- while the MMAs already run
-//                the next tile into the other accumulator;
+//                the next tile into the other accumulator; with one
+//                accumulator (256 x 256, 8-bit) the dequantisation warps,
+//                idle until it is handed back, drain two thirds of it;
 //   warps 8-15   dequantisation: code ring -> registers -> exact (q - 128)
 //                for 8-bit codes or fp16 round((q - 8) * s + z) for 4-bit
 //                group codes, written with stmatrix into the operand ring in
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = my_tiles * kps;  // k blocks this CTA runs, over all its units
     // one accumulator (its epilogue cannot overlap the next tile's MMAs): the
     // dequantisation warps, idle while it drains, drain two thirds of it
-    const bool helpers = Cfg::NACC == 1 && splits == 1;
+    const bool helpers = BITS == 8 && Cfg::NACC == 1 && splits == 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::SA; ++s) {
@@ -307,8 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int src = (cc * 16 + j) / CW;
             if constexpr (BITS == 8)  // 4-bit: the scales were applied to the codes
                 sc[j] = __shfl_sync(0xffffffffu, csc[j % CW], src);
-            if (p.bias)
-                bi[j] = __shfl_sync(0xffffffffu, cbi[j % CW], src);
+            bi[j] = __shfl_sync(0xffffffffu, cbi[j % CW], src);
         }
     };
     // scale (8-bit) or row scale (4-bit), bias, one rounding: 32 values of
@@ -351,6 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int acc = it % Cfg::NACC, qd = warp & 3;
         int m0, n0;
         tile_coords(p, ((int)blockIdx.x + it * (int)gridDim.x) / splits, TM, BN, m0, n0);
+        int rs_h = -1;  // sub-tile whose row scale rs holds
+        float rs = 1.f;
 #pragma unroll 1
         for (int x = part; x < MS * (BN / 32); x += nparts) {
             const int h = x / (BN / 32), cc = x % (BN / 32);
@@ -358,7 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nc >= p.n)
                 continue;
             const int row = m0 + h * BM + qd * 32 + lane;
-            const float rs = (p.rowscale && row < p.m) ? p.rowscale[row] : 1.f;
+            if (h != rs_h) {
+                rs = (p.rowscale && row < p.m) ? p.rowscale[row] : 1.f;
+                rs_h = h;
+            }
             uint32_t r[32];
             tmem_ld_32x32b_x32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)((acc * MS + h) * BN + cc * 32),
                                r);
@@ -698,28 +704,42 @@ __global__ void a_to_f16_kernel(const uint16_t* __restrict__ A, uint16_t* __rest
         rowscale[row] = ldexpf(1.f, E);
 }
 
-// Output tile shape: MS sub-tiles of 128 rows by BN columns.
-//   256 x 256 whenever those tiles still give every SM one: A and the codes
-//     are each fetched from L2 once per 256 columns / rows, the least traffic
-//     per FLOP (one accumulator: its 512 TMEM columns leave no room for a
-//     second, so the epilogue does not overlap the next tile);
-//   256 x 128 for 4-bit codes (their dequantisation costs the most per
-//     weight) when those tiles fill the GPU: two MMAs share each B tile;
-//   otherwise 128 x 256, or 128 x 128 when 256-wide tiles would fill at most
-//     half the SMs.
+// Output tile shape: MS sub-tiles of 128 rows by BN columns, the one whose
+// waves of tiles over the SMs take the least time.  A tile's time is its
+// shape's relative cost per k block, measured on GB300 with this kernel
+// (one 256 x 256 tile = 1): the 256 x 256 tiles fetch the fewest A and code
+// bytes per FLOP and dequantise each B tile for two MMAs, so they do the
+// most work per unit time; narrower tiles win when they fill more SMs.
+// 4-bit codes cost more to dequantise per weight, which weighs on the
+// shapes with one M=128 MMA per B tile (MS = 1).
 struct TcShape {
     int bn, ms;
 };
 
 TcShape tc_shape(int m, int n, int bits)
 {
-    const long long mt2 = (m + 2 * BM - 1) / (2 * BM);
-    if (m > BM && mt2 * ((n + 255) / 256) >= num_sms())
-        return {256, 2};
-    if (bits == 4 && m > BM && mt2 * ((n + 127) / 128) >= num_sms())
-        return {128, 2};
-    const long long tiles256 = (long long)((m + BM - 1) / BM) * ((n + 255) / 256);
-    return {2 * tiles256 <= num_sms() ? 128 : 256, 1};
+    struct Cand {
+        int bn, ms;
+        double cost;
+    };
+    // (8-bit 256 x 128 tiles, 0.66, never beat 128 x 256 ones at 0.61: the
+    // two shapes give nearly the same tile counts)
+    static constexpr Cand c8[3] = {{256, 2, 1.0}, {256, 1, 0.61}, {128, 1, 0.48}};
+    static constexpr Cand c4[4] = {{256, 2, 1.0}, {128, 2, 0.70}, {128, 1, 0.63}, {256, 1, 0.99}};
+    const Cand* cs = bits == 8 ? c8 : c4;
+    const int nc = bits == 8 ? 3 : 4;
+    TcShape best{cs[0].bn, cs[0].ms};
+    double best_t = 0.0;
+    for (int i = 0; i < nc; ++i) {
+        const long long tiles =
+            (long long)((m + BM * cs[i].ms - 1) / (BM * cs[i].ms)) * ((n + cs[i].bn - 1) / cs[i].bn);
+        const double t = (double)((tiles + num_sms() - 1) / num_sms()) * cs[i].cost;
+        if (i == 0 || t < best_t * 0.999) {
+            best = {cs[i].bn, cs[i].ms};
+            best_t = t;
+        }
+    }
+    return best;
 }
 
 template <int BITS, int OT, int ACT, int BN, int MS>
@@ -750,9 +770,12 @@ template <int BITS, int OT, int ACT>
 cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& tp, const TcPlan& sh,
                          cudaStream_t s)
 {
-    if (sh.ms == 2)
-        return sh.bn == 256 ? launch_tc_t<BITS, OT, ACT, 256, 2>(ma, B, tp, s)
-                            : launch_tc_t<BITS, OT, ACT, 128, 2>(ma, B, tp, s);
+    if (sh.ms == 2) {
+        if constexpr (BITS == 4)  // tc_shape gives 256 x 128 tiles for 4-bit codes only
+            if (sh.bn == 128)
+                return launch_tc_t<BITS, OT, ACT, 128, 2>(ma, B, tp, s);
+        return launch_tc_t<BITS, OT, ACT, 256, 2>(ma, B, tp, s);
+    }
     return sh.bn == 128 ? launch_tc_t<BITS, OT, ACT, 128, 1>(ma, B, tp, s)
                         : launch_tc_t<BITS, OT, ACT, 256, 1>(ma, B, tp, s);
 }

@@ -426,27 +426,51 @@ def run_moe(args, ws, rank, local):
     secs = total_ms / 1e3
     value = bytes_per_step * args.steps * ws / secs / 1e9
 
+    # end to end: every step copies its activations and gating logits in from
+    # pinned host memory and its output out, on two copy streams with two
+    # buffer sets (overlapping the neighbouring steps' kernels, as a serving
+    # loop would); events order every buffer's reuse
     hA = torch.empty(A.shape, dtype=dt, pin_memory=True)
     hA.copy_(A.cpu())
     hL = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
     hL.copy_(logits.cpu())
-    hO = torch.empty(out.shape, dtype=dt, pin_memory=True)
+    hO = [torch.empty(out.shape, dtype=dt, pin_memory=True) for _ in range(2)]
+    dA = [torch.empty_like(A) for _ in range(2)]
+    dL = [torch.empty_like(logits) for _ in range(2)]
+    dO = [torch.empty_like(out) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_k = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
     e2e_steps = max(1, min(args.steps, 30))
 
-    def e2e_step():
+    def e2e_step(i):
+        b = i % 2
+        if used[b]:
+            s_in.wait_event(ev_k[b])
+            stream.wait_event(ev_out[b])
+        used[b] = True
+        with torch.cuda.stream(s_in):
+            dA[b].copy_(hA, non_blocking=True)
+            dL[b].copy_(hL, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
         with torch.cuda.stream(stream):
-            A.copy_(hA, non_blocking=True)
-            logits.copy_(hL, non_blocking=True)
-            wo.moe_ffn(A, logits, fc1, s1, fc2, s2, c.H, c.I, c.E, c.topk, out=out,
+            wo.moe_ffn(dA[b], dL[b], fc1, s1, fc2, s2, c.H, c.I, c.E, c.topk, out=dO[b],
                        workspace=workspace, stream=stream)
-            hO.copy_(out, non_blocking=True)
-    for _ in range(3):
-        e2e_step()
+            ev_k[b].record(stream)
+        s_out.wait_event(ev_k[b])
+        with torch.cuda.stream(s_out):
+            hO[b].copy_(dO[b], non_blocking=True)
+            ev_out[b].record(s_out)
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    stream.synchronize()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
     e2e_s = max_over_ranks(ws, time.perf_counter() - t0)
     if rank != 0:
         return 0
@@ -472,7 +496,10 @@ def run_moe(args, ws, rank, local):
                      "algorithmic_bytes_per_launch": bytes_per_step},
         "e2e": {"value": bytes_per_step * e2e_steps * ws / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": hA.numel() * 2 + hL.numel() * 4,
-                "d2h_bytes_per_step": hO.numel() * 2},
+                "d2h_bytes_per_step": hO[0].numel() * 2,
+                "copies": "every step: pinned H2D of its activations and logits, D2H of its "
+                          "output, on two copy streams with two buffer sets (overlapping the "
+                          "neighbouring steps' kernels)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -600,42 +627,64 @@ def run_ours(args, ws, rank, local):
 
     # ---- end to end through the public API with host buffers ----
     # every step: one pinned host -> device copy of all the cases' activations,
-    # one wo.gemm per case, one device -> host copy of all the outputs
+    # one wo.gemm per case, one device -> host copy of all the outputs.  As in
+    # a serving loop the copies run on their own streams with two buffer sets:
+    # step i's input copy overlaps step i - 1's kernels and step i's output
+    # copy step i + 1's kernels; events order every buffer's reuse.
     a_sizes = [d["A"].numel() for d in dev_cases]
     c_sizes = [d["C"].numel() for d in dev_cases]
     a_dt, c_dt = dev_cases[0]["A"].dtype, dev_cases[0]["C"].dtype
     host_A = torch.empty(sum(a_sizes), dtype=a_dt, pin_memory=True)
-    host_C = torch.empty(sum(c_sizes), dtype=c_dt, pin_memory=True)
-    dev_A = torch.empty(sum(a_sizes), dtype=a_dt, device=dev)
-    dev_C = torch.empty(sum(c_sizes), dtype=c_dt, device=dev)
-    a_views, c_views, off_a, off_c = [], [], 0, 0
+    host_C = [torch.empty(sum(c_sizes), dtype=c_dt, pin_memory=True) for _ in range(2)]
+    dev_A = [torch.empty(sum(a_sizes), dtype=a_dt, device=dev) for _ in range(2)]
+    dev_C = [torch.empty(sum(c_sizes), dtype=c_dt, device=dev) for _ in range(2)]
+    a_views, c_views = [[], []], [[], []]
+    off_a = off_c = 0
     for d, na, nc in zip(dev_cases, a_sizes, c_sizes):
         host_A[off_a:off_a + na].copy_(d["A"].reshape(-1).cpu())
-        a_views.append(dev_A[off_a:off_a + na].view(d["A"].shape))
-        c_views.append(dev_C[off_c:off_c + nc].view(d["C"].shape))
+        for b in range(2):
+            a_views[b].append(dev_A[b][off_a:off_a + na].view(d["A"].shape))
+            c_views[b].append(dev_C[b][off_c:off_c + nc].view(d["C"].shape))
         off_a += na
         off_c += nc
     h2d = host_A.numel() * host_A.element_size()
-    d2h = host_C.numel() * host_C.element_size()
+    d2h = host_C[0].numel() * host_C[0].element_size()
     e2e_steps = max(1, min(args.steps, 50))
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]   # set b's input copy done
+    ev_k = [torch.cuda.Event() for _ in range(2)]    # set b's kernels done
+    ev_out = [torch.cuda.Event() for _ in range(2)]  # set b's output copy done
+    used = [False, False]
 
-    def e2e_step():
+    def e2e_step(i):
+        b = i % 2
+        if used[b]:
+            s_in.wait_event(ev_k[b])      # the kernels two steps back read dev_A[b]
+            stream.wait_event(ev_out[b])  # and their outputs left dev_C[b]
+        used[b] = True
+        with torch.cuda.stream(s_in):
+            dev_A[b].copy_(host_A, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
         with torch.cuda.stream(stream):
-            dev_A.copy_(host_A, non_blocking=True)
-            for d, Av, Cv in zip(dev_cases, a_views, c_views):
+            for d, Av, Cv in zip(dev_cases, a_views[b], c_views[b]):
                 c = d["c"]
                 wo.gemm(Av, d["B"], d["s"], c.n, c.k, c.bits, group_size=c.group_size,
                         zeros=d["z"], bias=d["b"], out=Cv, workspace=workspace,
                         stream=stream)
-            host_C.copy_(dev_C, non_blocking=True)
-    for _ in range(min(3, e2e_steps)):
-        e2e_step()
+            ev_k[b].record(stream)
+        s_out.wait_event(ev_k[b])
+        with torch.cuda.stream(s_out):
+            host_C[b].copy_(dev_C[b], non_blocking=True)
+            ev_out[b].record(s_out)
+    for i in range(min(3, e2e_steps)):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(ws)
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    stream.synchronize()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
     e2e_s = max_over_ranks(ws, time.perf_counter() - t0)
     if w["unit"] == "GB/s":
         e2e_val = bytes_per_step * e2e_steps * ws / e2e_s / 1e9
@@ -696,7 +745,10 @@ def run_ours(args, ws, rank, local):
                        else case_flops(c) / (ms / 1e3) / 1e12}
                   for c, ms in zip(cases, per_case_ms)],
         "e2e": {"value": e2e_val, "unit": w["unit"], "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "copies": "every step: one pinned H2D of its inputs, one D2H of its outputs, on "
+                          "two copy streams with two buffer sets (overlapping the neighbouring "
+                          "steps' kernels)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }

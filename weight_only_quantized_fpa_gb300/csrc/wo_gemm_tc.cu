@@ -67,8 +67,13 @@ struct TcCfg {
     static constexpr int A_BYTES = MS * A_SUB;
     static constexpr int C_BYTES = BN * BK * BITS / 8;           // packed codes of a k block
     static constexpr int B_BYTES = BN * BK * 2;                  // dequantised operand
-    static constexpr int SA = MS == 2 ? (BN == 256 ? 3 : BITS == 4 ? 4 : 3) : BN == 256 ? 4 : 6;  // A ring
-    static constexpr int SC = MS == 2 ? (BN == 256 ? 3 : 6) : (BITS == 8 ? 4 : 6) + (BN == 256 ? 0 : 2);  // codes
+    // 256 x 256 8-bit tiles: the A tiles' TMA round trip paces the MMAs, so
+    // the A ring gets four stages and the code ring, whose 16 KiB stages
+    // arrive early enough, two.  4-bit tiles keep three and three: their
+    // dequantisation reads the group scales through L1, which a fuller
+    // shared memory would shrink.
+    static constexpr int SA = MS == 2 ? (BN == 256 ? (BITS == 8 ? 4 : 3) : BITS == 4 ? 4 : 3) : BN == 256 ? 4 : 6;  // A ring
+    static constexpr int SC = MS == 2 ? (BN == 256 ? (BITS == 8 ? 2 : 3) : 6) : (BITS == 8 ? 4 : 6) + (BN == 256 ? 0 : 2);  // codes
     static constexpr int S2 = MS == 2 && BN == 256 ? 2 : BN == 256 ? 3 : 4;  // operand ring stages
     static constexpr int TPN = BK / Geom<BITS>::KT;              // packed tiles per 16 rows
     static constexpr int NT = (BN / 16) * TPN;                   // packed tiles per k block

@@ -226,6 +226,39 @@ __device__ __forceinline__ void dequant_stage(uint32_t c_s, const DqScales<BITS,
     }
 }
 
+// Sum of `splits` partial blocks (4 KB each: 32 rows x 32 fp32, block sp at
+// blk0 + sp * stride floats) into this lane's row v[32], in split order.  Up
+// to four blocks at a time are staged in shared memory at `stg` (16 KB) with
+// cp.async, their 16-byte pieces swizzled by row so that each lane reads its
+// row without bank conflicts.  Kept out of line: it is the cold k-split path
+// and stays out of the register allocation of the main loop.
+__device__ __noinline__ void split_sum(const float* blk0, size_t stride, int splits, uint32_t stg, int lane,
+                                       float (&v)[32])
+{
+    for (int sp0 = 0; sp0 < splits; sp0 += 4) {
+        const int nb = splits - sp0 < 4 ? splits - sp0 : 4;
+        for (int b = 0; b < nb; ++b)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int pc = i * 32 + lane, r = pc >> 3, w = pc & 7;
+                cp_async_16(stg + (uint32_t)(b * 4096 + r * 128 + ((w ^ (r & 7)) << 4)),
+                            blk0 + (size_t)(sp0 + b) * stride + pc * 4);
+            }
+        cp_async_wait_all();
+        __syncwarp();
+        for (int b = 0; b < nb; ++b)
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const uint4 u = lds128(stg + (uint32_t)(b * 4096 + lane * 128 + ((w ^ (lane & 7)) << 4)));
+                v[4 * w] += __uint_as_float(u.x);
+                v[4 * w + 1] += __uint_as_float(u.y);
+                v[4 * w + 2] += __uint_as_float(u.z);
+                v[4 * w + 3] += __uint_as_float(u.w);
+            }
+        __syncwarp();  // reads done before the next batch lands
+    }
+}
+
 template <int BITS, int OT, int ACT, int BN, int MS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
@@ -543,6 +576,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;  // every epilogue warp read the same value
             if (last) {
                 __threadfence();
+                // A split plan gives every CTA one unit (launch_tc_t checks), so
+                // here the A ring is idle: split_sum stages the partials in it
+                // (up to four splits, 16 KB per warp, in flight at once instead
+                // of 128 bytes per lane).
+                static_assert(Cfg::SA * Cfg::A_BYTES >= 4 * 16384, "partial staging");
+                const uint32_t stg = smem_addr(ringA) + (uint32_t)(q * 16384);
 #pragma unroll 1
                 for (int h = 0; h < MS; ++h) {
                     const int row = m0 + h * BM + q * 32 + lane;
@@ -556,19 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             v[j] = 0.f;
-                        for (int sp = 0; sp < splits; ++sp) {
-                            const float4* src = reinterpret_cast<const float4*>(
-                                p.partial + (size_t)(tile * splits + sp) * TM * BN +
-                                ((size_t)(h * (BN / 32) + cc) * BM + q * 32 + lane) * 32);
-#pragma unroll
-                            for (int w = 0; w < 8; ++w) {
-                                const float4 x = __ldcg(src + w);
-                                v[4 * w] += x.x;
-                                v[4 * w + 1] += x.y;
-                                v[4 * w + 2] += x.z;
-                                v[4 * w + 3] += x.w;
-                            }
-                        }
+                        // split 0's block: this warp's 32 rows x 32 floats, 4 KB
+                        split_sum(p.partial + (size_t)tile * splits * TM * BN +
+                                      ((size_t)(h * (BN / 32) + cc) * BM + q * 32) * 32,
+                                  (size_t)TM * BN, splits, stg, lane, v);
                         uint32_t sc[16], bi[16];
                         gather(cc, sc, bi);
                         if (row < p.m)
@@ -759,6 +789,8 @@ cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaS
     tp.m_tiles = (tp.m + BM * MS - 1) / (BM * MS);
     tp.n_tiles = (tp.n + BN - 1) / BN;
     const long long units = (long long)tp.m_tiles * tp.n_tiles * tp.splits;
+    if (tp.splits > 1 && units > num_sms())
+        return cudaErrorInvalidConfiguration;  // the split reduction stages in the A ring of a one-unit CTA
     const int grid = (int)(units < num_sms() ? units : num_sms());
     // packed codes viewed as [n/16 rows] x [bytes per 16-channel row / 4] words;
     // one box = BN/16 rows x one k block

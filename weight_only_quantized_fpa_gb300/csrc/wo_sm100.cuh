@@ -148,6 +148,18 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w)
                  : "memory");
 }
 
+// 16 bytes global -> shared without registers (L2 only); complete with
+// cp_async_wait_all.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA ----
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap)

@@ -74,6 +74,8 @@ SMALL = [
     (300, 15296, 512, 4, 64, inputs.BF16, True, True),  # 4-bit 256 x 256 tiles, ragged
     (200, 320, 6144, 8, -1, inputs.BF16, False, True),  # k split in 2, ragged m and n
     (130, 448, 12288, 4, 64, inputs.BF16, True, True),  # 4-bit, k split in 4, ragged
+    (200, 384, 3584, 8, -1, inputs.F16, False, True),   # 128 x 128 tiles, k split in 2, ragged
+    (130, 320, 4096, 4, 64, inputs.BF16, True, False),  # 4-bit 128 x 128 tiles, k split in 2
 ]
 
 

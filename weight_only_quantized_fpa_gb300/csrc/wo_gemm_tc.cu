@@ -1149,10 +1149,19 @@ TcPlan plan_tc(int m, int n, int k, int bits, int act, bool allow_split)
                 p.splits = sp;
                 break;
             }
+        // 128 x 128 tiles that fill at most half the SMs: split k in two when
+        // each half keeps at least 24 k blocks (the partial round trip of a
+        // 128 x 128 tile is a quarter of a 128 x 256 one's with four splits)
+        const long long tiles128 = (long long)((m + BM - 1) / BM) * ((n + 127) / 128);
+        if (p.splits == 1 && sh.bn == 128 && num_kb % 2 == 0 && num_kb / 2 >= 24 &&
+            tiles128 * 2 <= num_sms() && tiles128 <= (long long)kWsCounters)
+            p.splits = 2;
     }
+    const long long tiles = (long long)((m + BM * p.ms - 1) / (BM * p.ms)) * ((n + p.bn - 1) / p.bn);
     p.a16_bytes = (bits == 4 && act == WO_BF16) ? align_up((size_t)m * k * 2, 256) : 0;
     p.rowscale_bytes = p.a16_bytes ? align_up((size_t)m * 4, 256) : 0;
-    p.partial_bytes = p.splits > 1 ? align_up((size_t)tiles256 * p.splits * BM * 256 * 4, 256) : 0;
+    p.partial_bytes =
+        p.splits > 1 ? align_up((size_t)tiles * p.splits * BM * p.ms * p.bn * 4, 256) : 0;
     p.ws_bytes = kWsScratch + p.a16_bytes + p.rowscale_bytes + p.partial_bytes;
     return p;
 }

@@ -701,26 +701,67 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 2^-E (E chosen so max |a| * 2^-E lies in [2^14, 2^15)), which is exact,
 // then rounded to fp16, which is exact for bf16 values whose scaled
 // magnitude is at least 2^-14; rowscale[r] = 2^E undoes it in the epilogue.
-__global__ void a_to_f16_kernel(const uint16_t* __restrict__ A, uint16_t* __restrict__ A16,
-                                float* __restrict__ rowscale, int m, int k)
+// One CTA per row, 16-byte loads and stores (k % 64 == 0 and A 16-byte
+// aligned on this path); up to kA16Cache chunks of 8 values per thread stay
+// in registers between the max and the conversion, so rows up to 16384
+// values are read once.
+constexpr int kA16Threads = 256, kA16Cache = 8;
+
+__device__ __forceinline__ float absmax_bf16x8(const uint4& v)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        mx = fmaxf(mx, fabsf(to_f32<ACT_BF16>((uint16_t)(w[i] & 0xFFFFu))));
+        mx = fmaxf(mx, fabsf(to_f32<ACT_BF16>((uint16_t)(w[i] >> 16))));
+    }
+    return mx;
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v, float inv)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o[i] = (uint32_t)from_f32<ACT_F16>(to_f32<ACT_BF16>((uint16_t)(w[i] & 0xFFFFu)) * inv) |
+               ((uint32_t)from_f32<ACT_F16>(to_f32<ACT_BF16>((uint16_t)(w[i] >> 16)) * inv) << 16);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void __launch_bounds__(kA16Threads) a_to_f16_kernel(const uint16_t* __restrict__ A,
+                                                               uint16_t* __restrict__ A16,
+                                                               float* __restrict__ rowscale, int m, int k)
 {
     const int row = blockIdx.x;
     if (row >= m)
         return;
-    const uint16_t* a = A + (size_t)row * k;
+    const uint4* a = reinterpret_cast<const uint4*>(A + (size_t)row * k);
+    uint4* o = reinterpret_cast<uint4*>(A16 + (size_t)row * k);
+    const int nch = k >> 3;  // chunks of 8 values
+    uint4 c[kA16Cache];
     float mx = 0.f;
-    for (int c = threadIdx.x; c < k; c += blockDim.x)
-        mx = fmaxf(mx, fabsf(to_f32<ACT_BF16>(a[c])));
+#pragma unroll
+    for (int i = 0; i < kA16Cache; ++i) {
+        const int j = (int)threadIdx.x + i * kA16Threads;
+        if (j < nch) {
+            c[i] = __ldg(a + j);
+            mx = fmaxf(mx, absmax_bf16x8(c[i]));
+        }
+    }
+    for (int j = (int)threadIdx.x + kA16Cache * kA16Threads; j < nch; j += kA16Threads)
+        mx = fmaxf(mx, absmax_bf16x8(__ldg(a + j)));
     __shared__ float red[32];
-    for (int o = 16; o > 0; o >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int s = 16; s > 0; s >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
     if ((threadIdx.x & 31) == 0)
         red[threadIdx.x >> 5] = mx;
     __syncthreads();
     if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-        for (int o = 16; o > 0; o >>= 1)
-            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        float v = threadIdx.x < (kA16Threads >> 5) ? red[threadIdx.x] : 0.f;
+        for (int s = 16; s > 0; s >>= 1)
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, s));
         if (threadIdx.x == 0)
             red[0] = v;
     }
@@ -733,8 +774,14 @@ __global__ void a_to_f16_kernel(const uint16_t* __restrict__ A, uint16_t* __rest
         E = e2 - 15;      // mx * 2^-E in [2^14, 2^15)
     }
     const float inv = ldexpf(1.f, -E);
-    for (int c = threadIdx.x; c < k; c += blockDim.x)
-        A16[(size_t)row * k + c] = from_f32<ACT_F16>(to_f32<ACT_BF16>(a[c]) * inv);
+#pragma unroll
+    for (int i = 0; i < kA16Cache; ++i) {
+        const int j = (int)threadIdx.x + i * kA16Threads;
+        if (j < nch)
+            o[j] = bf16x8_to_f16x8(c[i], inv);
+    }
+    for (int j = (int)threadIdx.x + kA16Cache * kA16Threads; j < nch; j += kA16Threads)
+        o[j] = bf16x8_to_f16x8(__ldg(a + j), inv);
     if (threadIdx.x == 0)
         rowscale[row] = ldexpf(1.f, E);
 }
@@ -1194,7 +1241,7 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     if (plan.a16_bytes) {
         uint16_t* A16 = reinterpret_cast<uint16_t*>(ws + kWsScratch);
         float* rsc = reinterpret_cast<float*>(ws + kWsScratch + plan.a16_bytes);
-        a_to_f16_kernel<<<a.m, 256, 0, s>>>(static_cast<const uint16_t*>(a.A), A16, rsc, a.m, a.k);
+        a_to_f16_kernel<<<a.m, kA16Threads, 0, s>>>(static_cast<const uint16_t*>(a.A), A16, rsc, a.m, a.k);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;

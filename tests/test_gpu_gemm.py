@@ -88,6 +88,18 @@ def test_small_shapes(wo, m, n, k, bits, group, act, zeros, bias):
     _check_full(DeviceCase(c), f"m{m} n{n} k{k} w{bits} g{group}")
 
 
+@pytest.mark.parametrize("m,n,k,group", [(1, 128, 16384, -1), (4, 256, 16384, 64), (2, 128, 8192, -1)])
+def test_w4_nonnegative_activations_long_groups(wo, m, n, k, group):
+    # 4-bit codes with bf16 activations that are all >= 0 (as after a gated
+    # activation): the decode kernel's group sums then carry the largest
+    # activation sums next to the smallest results, per-channel groups span
+    # the whole k
+    c = inputs.make_gemm_case(8, 400 + m, m, n, k, bits=4, group_size=group, act_dtype=inputs.BF16,
+                              scale_lo=0.005, scale_hi=0.02, with_zeros=True, with_bias=True)
+    c.A = (c.A & np.uint16(0x7FFF)).astype(c.A.dtype)  # |a|: clear the bf16 sign bits
+    _check_full(DeviceCase(c), f"w4 |a| m{m} k{k} g{group}")
+
+
 def test_split_k_long_reduction(wo):
     # few channels and a long k: the k range is split across a cluster of CTAs
     c = inputs.make_gemm_case(8, 77, 4, 64, 18944, bits=8, group_size=-1, act_dtype=inputs.F16,

@@ -882,25 +882,27 @@ cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& t
 
 constexpr int kMoeNT = 64;  // token rows per chunk (the MMA's N)
 
-template <bool GATED>
+// TWO: an item carries two 128-row weight halves that share each token tile
+// (the gated fc1's gate and up rows, or 256 consecutive fc2 channels).
+template <bool TWO>
 struct MoeCfg {
-    static constexpr int WR = GATED ? 256 : 128;         // weight rows per item
+    static constexpr int WR = TWO ? 256 : 128;           // weight rows per item
     static constexpr int A_BYTES = kMoeNT * BK * 2;       // 8 KiB of token rows
     static constexpr int C_BYTES = WR * BK;               // packed codes of a k block
     static constexpr int B_BYTES = WR * BK * 2;           // dequantised operand
     // The codes stream from HBM: their ring holds 128 KiB, the bytes in flight
     // one SM needs at HBM rate under load; token rows come from L2 and the
     // operand ring only covers the dequant -> MMA hand-off.
-    static constexpr int SA = 4, SC = GATED ? 8 : 16, S2 = GATED ? 2 : 3;
+    static constexpr int SA = 4, SC = TWO ? 8 : 16, S2 = TWO ? 2 : 3;
     static_assert(SC <= 16 && S2 <= 4 && SA <= 8, "barrier arrays");
-    static constexpr int COLS = (GATED ? 2 : 1) * kMoeNT; // TMEM columns per accumulator
+    static constexpr int COLS = (TWO ? 2 : 1) * kMoeNT;   // TMEM columns per accumulator
     static constexpr uint32_t TMEM_COLS = 2 * COLS;
     static constexpr int SMEM = SA * A_BYTES + SC * C_BYTES + S2 * B_BYTES;
 };
 
 struct MoeTcParams {
     const int* offsets;      // [E + 1] row ranges of the experts (rows in expert order)
-    int E, nb;               // experts, 128-channel blocks per expert
+    int E, nb;               // experts, items (128 or 256 channels) per expert
     int num_kb;              // K / BK
     int inter;               // gated: channel distance gate -> up (and h row length)
     int n_out;               // plain: output row length (hidden)
@@ -919,12 +921,14 @@ __device__ __forceinline__ void moe_rows(const MoeTcParams& p, int e, int& r0, i
     chunks = cnt > 0 ? (cnt + kMoeNT - 1) / kMoeNT : 0;
 }
 
-template <bool GATED, int ACT>
+template <bool GATED, bool WIDE, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
                   const MoeTcParams p)
 {
-    using Cfg = MoeCfg<GATED>;
+    constexpr bool TWO = GATED || WIDE;
+    constexpr int CH = WIDE ? 256 : 128;  // output channels per item
+    using Cfg = MoeCfg<TWO>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -983,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int e = it / p.nb, nb = it % p.nb;
                 int r0, cnt, chunks;
                 moe_rows(p, e, r0, cnt, chunks);
-                const int wrow = (e * p.rows_per_expert_w + nb * 128) / 16;  // 16-channel block row
+                const int wrow = (e * p.rows_per_expert_w + nb * CH) / 16;  // 16-channel block row
                 for (int ch = 0; ch < chunks && ok; ++ch) {
                     for (int kb = 0; kb < num_kb; ++kb, ++c) {
                         const int s = c % S;
@@ -996,9 +1000,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive_expect_tx(&full[s], Cfg::C_BYTES);
                             uint8_t* dst = ringC + s * Cfg::C_BYTES;
                             tma_load_2d(dst, &tmC, &full[s], kb * (BK * 16 / 4), wrow);
-                            if constexpr (GATED)  // the matching up channels, inter rows further
+                            if constexpr (TWO)  // the matching up channels, inter rows further,
+                                                // or the next 128 channels
                                 tma_load_2d(dst + 128 * BK, &tmC, &full[s], kb * (BK * 16 / 4),
-                                            wrow + p.inter / 16);
+                                            wrow + (GATED ? p.inter / 16 : 8));
                         } else {
                             mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES);
                             tma_load_2d(ringA + s * Cfg::A_BYTES, &tmA, &full[s], kb * BK,
@@ -1048,7 +1053,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < BK / 16; ++j) {
                             mma_f16(d, wd + (uint64_t)(2 * j), xd + (uint64_t)(2 * j), idesc,
                                     (kb > 0 || j > 0) ? 1u : 0u);
-                            if constexpr (GATED)  // up rows: operand rows 128..255, 16 KiB on
+                            if constexpr (TWO)  // second half: operand rows 128..255, 16 KiB on
                                 mma_f16(d + kMoeNT, desc_sw128(w_s + 128 * 128) + (uint64_t)(2 * j),
                                         xd + (uint64_t)(2 * j), idesc, (kb > 0 || j > 0) ? 1u : 0u);
                         }
@@ -1072,10 +1077,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int e = it / p.nb, nb = it % p.nb;
             int r0, cnt, chunks;
             moe_rows(p, e, r0, cnt, chunks);
-            const int chl = nb * 128 + q * 32 + lane;  // output channel within the expert
+            const int chl = nb * CH + q * 32 + lane;  // output channel within the expert
             const uint16_t* se = p.scales + (size_t)e * p.rows_per_expert_w;
             const float s0 = to_f32<ACT>(ld_nc_u16(se + chl));
-            const float s1 = GATED ? to_f32<ACT>(ld_nc_u16(se + p.inter + chl)) : 0.f;
+            const float s1 = TWO ? to_f32<ACT>(ld_nc_u16(se + (GATED ? p.inter : 128) + chl)) : 0.f;
             bool ok = true;
             for (int ch = 0; ch < chunks; ++ch, ++t) {
                 const int acc = t & 1;
@@ -1094,7 +1099,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;  // warp-uniform
                     uint32_t r[32], u[32];
                     tmem_ld_32x32b_x32(tbase + (uint32_t)(cc * 32), r);
-                    if constexpr (GATED)
+                    if constexpr (TWO)
                         tmem_ld_32x32b_x32(tbase + (uint32_t)(kMoeNT + cc * 32), u);
                     tmem_ld_wait();
 #pragma unroll
@@ -1107,6 +1112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 p.H[row * p.inter + chl] = from_f32<ACT>(g / (1.f + expf(-g)) * up);
                             } else {
                                 p.Y[row * p.n_out + chl] = g;
+                                if constexpr (WIDE)
+                                    p.Y[row * p.n_out + chl + 128] = __uint_as_float(u[j]) * s1;
                             }
                         }
                     }
@@ -1157,13 +1164,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool GATED, int ACT>
+template <bool GATED, bool WIDE, int ACT>
 cudaError_t launch_moe_tc_t(const CUtensorMap& ma, const CUtensorMap& mc, const MoeTcParams& mp,
                             cudaStream_t s)
 {
-    constexpr int smem = MoeCfg<GATED>::SMEM + (int)sizeof(Barriers) + 1024;
+    constexpr int smem = MoeCfg<GATED || WIDE>::SMEM + (int)sizeof(Barriers) + 1024;
     static_assert(smem <= 232448, "shared memory per CTA");
-    auto kern = moe_tc_kernel<GATED, ACT>;
+    auto kern = moe_tc_kernel<GATED, WIDE, ACT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
@@ -1274,7 +1281,10 @@ cudaError_t launch_moe_tc(bool gated, int act, const void* rows, int total_rows,
     MoeTcParams mp{};
     mp.offsets = offsets;
     mp.E = experts;
-    mp.nb = (gated ? inter : n_out) / 128;
+    // fc2 items of 256 channels when they tile the output (two MMAs per token
+    // tile, half the token-row copies per weight byte), else 128
+    const bool wide = !gated && n_out % 256 == 0;
+    mp.nb = gated ? inter / 128 : n_out / (wide ? 256 : 128);
     mp.num_kb = k / BK;
     mp.inter = inter;
     mp.n_out = n_out;
@@ -1296,10 +1306,13 @@ cudaError_t launch_moe_tc(bool gated, int act, const void* rows, int total_rows,
                       BK * 16 / 4, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     if (gated)
-        return act == WO_F16 ? launch_moe_tc_t<true, ACT_F16>(ma, mc, mp, s)
-                             : launch_moe_tc_t<true, ACT_BF16>(ma, mc, mp, s);
-    return act == WO_F16 ? launch_moe_tc_t<false, ACT_F16>(ma, mc, mp, s)
-                         : launch_moe_tc_t<false, ACT_BF16>(ma, mc, mp, s);
+        return act == WO_F16 ? launch_moe_tc_t<true, false, ACT_F16>(ma, mc, mp, s)
+                             : launch_moe_tc_t<true, false, ACT_BF16>(ma, mc, mp, s);
+    if (wide)
+        return act == WO_F16 ? launch_moe_tc_t<false, true, ACT_F16>(ma, mc, mp, s)
+                             : launch_moe_tc_t<false, true, ACT_BF16>(ma, mc, mp, s);
+    return act == WO_F16 ? launch_moe_tc_t<false, false, ACT_F16>(ma, mc, mp, s)
+                         : launch_moe_tc_t<false, false, ACT_BF16>(ma, mc, mp, s);
 }
 
 }  // namespace wo

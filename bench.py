@@ -477,10 +477,10 @@ def run_moe(args, ws, rank, local):
     hbm_gbs, _, peak_src = measured_peaks()
     achieved = bytes_per_step / (total_ms / args.steps / 1e3) / 1e9
     try:
-        sh = kernel_source_hash(["wo_moe.cu", "wo_common.cuh"])
+        sh = kernel_source_hash(["wo_moe.cu", "wo_gemm_tc.cu", "wo_common.cuh", "wo_sm100.cuh"])
     except OSError:
         sh = None
-    tr = traffic_from_profile("expert_gemv_kernel", sh) if sh else None
+    tr = traffic_from_profile("moe_ffn", sh) if sh else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,

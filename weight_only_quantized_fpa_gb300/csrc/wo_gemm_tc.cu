@@ -873,9 +873,12 @@ cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& t
 // channels), and the expert's token rows (in expert order, a chunk of up to
 // kMoeNT at a time) are its N operand, so an expert's few dozen rows still
 // fill the tensor pipe while its weights stream from HBM once per chunk.
-// Work items: (expert, block of 128 output channels); for the gated fc1 an
-// item carries the 128 gate channels and the matching 128 up channels
-// (inter apart) so the epilogue can form h = silu(gate) * up.  Roles as in
+// Work items: (expert, block of output channels).  For the gated fc1 an item
+// carries the 128 gate channels and the matching 128 up channels (inter
+// apart) so the epilogue can form h = silu(gate) * up; for fc2 it carries
+// 256 consecutive output channels when they tile the output (else 128).
+// An item's two 128-row weight halves are two MMAs on the same staged token
+// tile: the token rows are copied once per 256 weight rows.  Roles as in
 // gemm_tc_kernel: warp 0 codes TMA, warp 2 activation TMA, warp 1 MMA,
 // warps 4-7 epilogue (TMEM lanes are channels, columns are tokens), warps
 // 8-15 dequantisation.

@@ -124,6 +124,26 @@ WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* sca
                   size_t workspace_bytes, void* stream);
 
 /*
+ * Rows of a quantised embedding (vocab) table, dequantised (vLLM-Omni
+ * "cpu_int4.py", CPUInt4EmbeddingMethod.embedding: the rows of the token ids,
+ * w = (q - offset) * scale (+ zero) in fp32, rounded once to the activation
+ * dtype).  The table is the same packed weight wo_gemm reads as [n, k] =
+ * [vocab, hidden] (tied lm_head and embedding share one copy): rows are read
+ * straight from the packed tiles.
+ *   ids:      int32 [T] device array of token ids; an id outside [0, vocab)
+ *             gives a row of zeros.
+ *   B_packed: output of wo_pack for (vocab, hidden, bits).
+ *   scales, zeros, group_size, bits: as for wo_gemm (n = vocab, k = hidden).
+ *   out:      act_dtype [T, hidden], row-major.
+ * Requires vocab % 64 == 0, hidden % 64 == 0; T == 0 is a no-op.  Pointers:
+ * ids 4-byte, B_packed 16-byte, scales, zeros and out 2-byte aligned.
+ * Bit-identical to rounding the oracle's fp32 dequantised rows.
+ */
+WO_API wo_status wo_embed(const int32_t* ids, int T, const uint8_t* B_packed, const void* scales,
+                          const void* zeros, void* out, int vocab, int hidden, int group_size,
+                          int bits, wo_dtype act_dtype, void* stream);
+
+/*
  * Workspace bytes for wo_moe_ffn with T tokens, the given sizes and top-k.
  * Same zero-fill rule as wo_workspace_size.
  */

@@ -16,6 +16,8 @@ Functions and the page passages they follow:
   int8 scale; group-wise int4 scale and zero).
 * ``gemm`` -- acext User Guide 1.2.1 (fpA_intB runner ``gemm`` with scales,
   zero points, biases and group_size).
+* ``embed`` -- vLLM-Omni ``cpu_int4.py`` ``CPUInt4EmbeddingMethod.embedding``
+  (rows of the token ids, dequantised in fp32, cast to the activation dtype).
 * ``moe_route`` / ``moe_ffn`` -- acext User Guide 1.2.3 (MoE runner: gating
   output, top-k, fc1, activation, fc2, routing-weighted combine).
 * ``to_half_bits`` / ``to_bf16_bits`` / ``decode`` -- IEEE binary16 and
@@ -201,6 +203,18 @@ def gemm(A, act_dtype, B, scales, zeros, bias, m, n, k, group_size, bits,
     _check(_load().oracle_gemm(_ptr(Ac), act_dtype, _ptr(Bc), _ptr(s), _ptr(z), _ptr(b),
                                m, n, k, group_size, bits, nt, _ptr(C)), "gemm")
     return C
+
+
+def embed(ids, B, scales, zeros, vocab, hidden, group_size, bits, act_dtype) -> np.ndarray:
+    """Embedding rows: act_dtype bit patterns [T, hidden], row t = the fp32
+    dequantised weight row ids[t] rounded once (a zero row for an id outside
+    [0, vocab))."""
+    w = dequant(B, scales, zeros, vocab, hidden, group_size, bits, act_dtype)
+    idx = np.asarray(ids, dtype=np.int64).reshape(-1)
+    rows = np.zeros((idx.size, hidden), dtype=np.float64)
+    ok = (idx >= 0) & (idx < vocab)
+    rows[ok] = w[idx[ok]]
+    return round_to(rows, act_dtype)
 
 
 # -- MoE -------------------------------------------------------------------

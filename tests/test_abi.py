@@ -28,7 +28,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["wo_pack", "wo_unpack", "wo_packed_bytes", "wo_workspace_size", "wo_gemm",
               "wo_moe_workspace_size", "wo_moe_ffn", "wo_status_string", "wo_check_workspace",
-              "wo_selftest_wait_timeout"]:
+              "wo_selftest_wait_timeout", "wo_embed"]:
         assert n in names
 
 
@@ -141,3 +141,24 @@ def test_selftest_rejects_bad_arguments_without_launching(lib):
     assert f(addr + 8, 256, 1000, None) == 1      # not 256-byte aligned
     assert f(addr, 256, 0, None) == 1             # limit out of range
     assert f(addr, 256, 2000000, None) == 1
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(), 0),                                   # T == 0: nothing to do
+    (dict(T=4, bits=3), 1),                        # bad bits
+    (dict(T=4, vocab=100), 1),                     # vocab % 64
+    (dict(T=4, hidden=96), 1),                     # hidden % 64
+    (dict(T=4, bits=8, group=64), 2),              # 8-bit tables are per channel
+    (dict(T=4, bits=8, group=-1, zeros=64), 2),    # 8-bit tables have no zeros
+    (dict(T=4, ids=4098), 1),                      # ids not 4-byte aligned
+    (dict(T=4, B=4104), 1),                        # packed table not 16-byte aligned
+    (dict(T=4, act=7), 1),                         # bad activation dtype
+    (dict(T=-1), 1),
+])
+def test_embed_rejects_bad_arguments_before_launch(lib, kw, expect):
+    a = dict(ids=4096, T=0, B=8192, s=64, zeros=None, out=16384, vocab=256, hidden=512, group=64,
+             bits=4, act=1)
+    a.update(kw)
+    st = lib.wo_embed(a["ids"], a["T"], a["B"], a["s"], a["zeros"], a["out"], a["vocab"],
+                      a["hidden"], a["group"], a["bits"], a["act"], None)
+    assert st == expect

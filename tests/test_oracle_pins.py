@@ -358,6 +358,27 @@ def test_gemm_one_hot_rows_pick_weight_columns(bits):
         assert np.array_equal(C[i], w.astype(np.float64))
 
 
+@pytest.mark.parametrize("bits,group,dtype", [(4, 64, BF16), (8, -1, F16), (4, -1, F16)])
+def test_embed_rows_are_identity_gemm_columns(bits, group, dtype):
+    # A = I_k gives C[i, j] = w[j][i]: column id of that product, rounded
+    # once, is embedding row id; ids out of range give zero rows
+    vocab, k = 64, 128
+    c = inputs.make_gemm_case(9, 50 + bits, 1, vocab, k, bits=bits, group_size=group,
+                              act_dtype=dtype, scale_lo=0.005, scale_hi=0.02,
+                              with_zeros=bits == 4, with_bias=False)
+    one = inputs.to_bits(np.array([1.0]), dtype)[0]
+    eye = np.zeros((k, k), dtype=np.uint16)
+    eye[np.arange(k), np.arange(k)] = one
+    C = oracle.gemm(eye, dtype, c.B, c.scales, c.zeros, None, k, vocab, k, group, bits)
+    ids = np.array([0, 5, 15, 16, 63, -1, 64, 17], dtype=np.int32)
+    got = oracle.embed(ids, c.B, c.scales, c.zeros, vocab, k, group, bits, dtype)
+    for t, i in enumerate(ids):
+        if 0 <= i < vocab:
+            assert np.array_equal(got[t], oracle.round_to(C[:, i], dtype))
+        else:
+            assert not got[t].any()
+
+
 def test_gemm_integer_exact():
     # integer A in -2..2, int8 codes 126..130 (q - 128 in -2..2), scale 1:
     # every partial sum is a small integer, so C equals the integer matmul

@@ -78,6 +78,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.wo_moe_workspace_size.restype = S
         lib.wo_moe_ffn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
         lib.wo_moe_ffn.restype = I
+        lib.wo_embed.argtypes = [P, I, P, P, P, P, I, I, I, I, I, P]
+        lib.wo_embed.restype = I
         lib.wo_check_workspace.argtypes = [P, S, P]
         lib.wo_check_workspace.restype = I
         lib.wo_gemm_tc_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
@@ -158,6 +160,13 @@ def wo_gemm(A, B_packed, scales, zeros, bias, C, m: int, n: int, k: int, group_s
                                   _ptr(bias), _ptr(C), m, n, k, group_size, bits, act_dtype,
                                   _ptr(workspace), workspace_bytes, _stream_ptr(stream)),
            "wo_gemm")
+
+
+def wo_embed(ids, T: int, B_packed, scales, zeros, out, vocab: int, hidden: int, group_size: int,
+             bits: int, act_dtype: int, stream=None) -> None:
+    _raise(load_library().wo_embed(_ptr(ids), T, _ptr(B_packed), _ptr(scales), _ptr(zeros),
+                                   _ptr(out), vocab, hidden, group_size, bits, act_dtype,
+                                   _stream_ptr(stream)), "wo_embed")
 
 
 def wo_moe_workspace_size(T: int, hidden: int, inter: int, experts: int, topk: int) -> int:
@@ -279,6 +288,19 @@ def gemm(A, B_packed, scales, n: int, k: int, bits: int, group_size: int = -1, z
         ws, ws_bytes = workspace, workspace.numel()
     wo_gemm(A, B_packed, scales, zeros, bias, out, m, n, k, group_size, bits, act, ws, ws_bytes,
             stream)
+    return out
+
+
+def embed(ids, B_packed, scales, vocab: int, hidden: int, bits: int, group_size: int = -1,
+          zeros=None, out=None, stream=None):
+    """Rows ids of a packed [vocab, hidden] table, dequantised to the scales'
+    dtype through wo_embed; returns [len(ids), hidden]."""
+    import torch
+    T = ids.numel()
+    act = _dtype_code(scales)
+    if out is None:
+        out = torch.empty((T, hidden), dtype=scales.dtype, device=scales.device)
+    wo_embed(ids, T, B_packed, scales, zeros, out, vocab, hidden, group_size, bits, act, stream)
     return out
 
 

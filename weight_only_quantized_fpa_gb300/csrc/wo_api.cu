@@ -173,6 +173,34 @@ wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, co
     return cuda_status(launch_stream_gemm(a, s));
 }
 
+wo_status wo_embed(const int32_t* ids, int T, const uint8_t* B_packed, const void* scales,
+                   const void* zeros, void* out, int vocab, int hidden, int group_size, int bits,
+                   wo_dtype act_dtype, void* stream)
+{
+    // the table's shape rules are wo_gemm's with n = vocab, k = hidden
+    if (T < 0 || vocab < 0 || hidden <= 0 || (bits != 4 && bits != 8) || vocab % 64 != 0 ||
+        hidden % 64 != 0)
+        return WO_ERR_INVALID_ARG;
+    const int g = norm_group(group_size, hidden);
+    if (g <= 0 || hidden % g != 0)
+        return WO_ERR_INVALID_ARG;
+    if ((bits == 8 && g != hidden) || (bits == 4 && g != hidden && g % 64 != 0))
+        return WO_ERR_UNSUPPORTED;
+    if (act_dtype != WO_F16 && act_dtype != WO_BF16)
+        return WO_ERR_INVALID_ARG;
+    if (bits == 8 && zeros)
+        return WO_ERR_UNSUPPORTED;  // 8-bit weights are scale-only
+    if (T == 0 || vocab == 0)
+        return WO_OK;
+    if (!ids || !B_packed || !scales || !out)
+        return WO_ERR_INVALID_ARG;
+    if (!aligned(ids, 4) || !aligned(B_packed, 16) || !aligned(scales, 2) || !aligned(out, 2) ||
+        (zeros && !aligned(zeros, 2)))
+        return WO_ERR_INVALID_ARG;
+    return cuda_status(launch_embed(ids, T, B_packed, scales, zeros, out, vocab, hidden, g, bits,
+                                    act_dtype, static_cast<cudaStream_t>(stream)));
+}
+
 wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, void* stream)
 {
     const cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -29,6 +29,10 @@ int num_sms();  // SM count of the current device (152 when none is visible)
 // ---- pack -----------------------------------------------------------------
 cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,
                         cudaStream_t s);
+// rows ids[0..T) of a packed [vocab, hidden] table, dequantised (wo_embed)
+cudaError_t launch_embed(const int32_t* ids, int T, const uint8_t* B, const void* scales,
+                         const void* zeros, void* out, int vocab, int hidden, int group, int bits,
+                         int act, cudaStream_t s);
 
 struct GemmArgs {
     const void* A;

@@ -119,7 +119,101 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
     }
 }
 
+// Embedding rows straight from the packed table (vLLM-Omni "cpu_int4.py",
+// CPUInt4EmbeddingMethod.embedding: gather the rows of the token ids,
+// dequantise w = (q - offset) * scale (+ zero) in fp32, round once to the
+// activation dtype).  Row r of a 16-row block lives in lanes 4 (r % 8) + t,
+// t = 0..3, of each of its block's tiles, so one thread per (token, k tile,
+// t) reads one 16-byte lane chunk and writes the codes of that chunk that
+// belong to the row; ids outside [0, vocab) give a zero row.
+template <int BITS, int ACT>
+__global__ void embed_kernel(const int32_t* __restrict__ ids, int T, const uint8_t* __restrict__ B,
+                             const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
+                             uint16_t* __restrict__ out, int vocab, int hidden, int G, int group)
+{
+    constexpr int KT = Geom<BITS>::KT;
+    const int ktiles = hidden / KT;
+    const long long total = (long long)T * ktiles * 4;
+    for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < total;
+         c += (long long)gridDim.x * blockDim.x) {
+        const int t4 = (int)(c & 3);
+        const int kt = (int)((c >> 2) % ktiles);
+        const int tok = (int)((c >> 2) / ktiles);
+        const int id = ids[tok];
+        const bool valid = id >= 0 && id < vocab;
+        const int r = valid ? id % 16 : 0;  // an invalid id writes row 0's positions with zeros
+        const int g = r & 7;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid)
+            v = *reinterpret_cast<const uint4*>(B + ((((size_t)(id / 16) * ktiles + kt) * 32 + 4 * g + t4) * 16));
+        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint16_t* orow = out + (size_t)tok * hidden + (size_t)kt * KT;
+        auto put = [&](int kk, int q) {
+            float w = 0.f;
+            if (valid) {
+                const int kg = kt * KT + kk;
+                const size_t gi = (size_t)id * G + kg / group;
+                w = (float)(q - (BITS == 8 ? 128 : 8)) * to_f32<ACT>(scales[gi]);
+                if (zeros)
+                    w += to_f32<ACT>(zeros[gi]);
+            }
+            orow[kk] = from_f32<ACT>(w);
+        };
+        if constexpr (BITS == 8) {
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+                int row, kk;
+                u8_coord(b, g, t4, row, kk);
+                if (row == r)
+                    put(kk, (int)((words[b >> 2] >> (8 * (b & 3))) & 0xFFu));
+            }
+        } else {
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+                for (int p4 = 0; p4 < 8; ++p4) {
+                    int row, kk;
+                    u4_coord(s4, p4, g, t4, row, kk);
+                    if (row == r)
+                        put(kk, (int)((words[s4] >> (4 * p4)) & 0xFu));
+                }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_embed(const int32_t* ids, int T, const uint8_t* B, const void* scales,
+                         const void* zeros, void* out, int vocab, int hidden, int group, int bits,
+                         int act, cudaStream_t s)
+{
+    const int KT = bits == 8 ? 32 : 64;
+    const long long total = (long long)T * (hidden / KT) * 4;
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    const long long cap = (long long)num_sms() * 16;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    const int G = hidden / group;
+    const auto* sc = static_cast<const uint16_t*>(scales);
+    const auto* zc = static_cast<const uint16_t*>(zeros);
+    auto* o = static_cast<uint16_t*>(out);
+    const unsigned nb = (unsigned)blocks;
+    if (bits == 8) {
+        if (act == WO_F16)
+            embed_kernel<8, ACT_F16><<<nb, threads, 0, s>>>(ids, T, B, sc, zc, o, vocab, hidden, G, group);
+        else
+            embed_kernel<8, ACT_BF16><<<nb, threads, 0, s>>>(ids, T, B, sc, zc, o, vocab, hidden, G, group);
+    } else {
+        if (act == WO_F16)
+            embed_kernel<4, ACT_F16><<<nb, threads, 0, s>>>(ids, T, B, sc, zc, o, vocab, hidden, G, group);
+        else
+            embed_kernel<4, ACT_BF16><<<nb, threads, 0, s>>>(ids, T, B, sc, zc, o, vocab, hidden, G, group);
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,
                         cudaStream_t s)

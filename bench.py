@@ -63,7 +63,13 @@ WORKLOADS = {
                      "of fp32 logits ~N(0,1); hidden 4096, inter 1408; per expert fc1 "
                      "[2816,4096] and fc2 [4096,1408] int8 per-channel, bf16 scales "
                      "~U(0.001,0.01); SiLU-gated fc1, fc2, routing-weighted sum; A bf16 ~N(0,1)"),
+    "embed": dict(config=4, unit="GB/s", dtype="bf16",
+                  desc="Packed-embedding row gather (wo_embed): 16384 token ids ~U[0,131072) per "
+                       "call, 4 id sets rotated so the gathered rows exceed L2 across calls; the "
+                       "table is the w4_g64 head (131072 x 2048, 4-bit group 64, bf16 scales and "
+                       "zeros); bytes = the rows' codes, scales and zeros + the bf16 output"),
 }
+EMBED_T, EMBED_SETS = 16384, 4
 
 HBM_FALLBACK_GBS = 6800.0
 BF16_FALLBACK_TFLOPS = 1900.0
@@ -326,11 +332,177 @@ def run_reference_moe(args):
     return 0
 
 
+def embed_bytes_per_row(c) -> int:
+    G = c.k // 64
+    return c.k // 2 + 2 * G * 2 + c.k * 2  # codes, scales and zeros, bf16 output
+
+
+def run_reference_embed(args):
+    import oracle
+    oracle.build()
+    w = WORKLOADS["embed"]
+    c = inputs.workload_case(4, 3)
+    rng = np.random.default_rng(1234)
+    per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+
+    def one(nids):
+        ids = rng.integers(0, c.n, size=nids, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.embed(ids, c.B, c.scales, c.zeros, c.n, c.k, c.group_size, c.bits, c.act_dtype)
+        return time.perf_counter() - t0
+
+    dt = one(64)
+    nids = max(64, min(EMBED_T, int(64 * per_step_budget / max(dt, 1e-4))))
+    for _ in range(args.warmup):
+        one(nids)
+    tot = sum(one(nids) for _ in range(args.steps))
+    value = nids * args.steps * embed_bytes_per_row(c) / tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["desc"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {nids} random ids of the table"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def embed_traffic():
+    try:
+        sh = kernel_source_hash(["wo_pack.cu", "wo_common.cuh"])
+    except OSError:
+        return None
+    tr = traffic_from_profile("embed_kernel", sh)
+    return tr["dram_bytes_per_launch"] if tr else None
+
+
+def run_embed(args, ws, rank, local):
+    import torch
+
+    import weight_only_quantized_fpa_gb300 as wo
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wo.load_library()
+    w = WORKLOADS["embed"]
+    c = inputs.workload_case(4, 3)
+    dt = torch.bfloat16
+
+    def up16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt)
+
+    B = wo.pack(torch.from_numpy(c.B).to(dev), c.n, c.k, c.bits)
+    s, z = up16(c.scales), up16(c.zeros)
+    rng = np.random.default_rng(1234 + rank)
+    ids_h = [rng.integers(0, c.n, size=EMBED_T, dtype=np.int32) for _ in range(EMBED_SETS)]
+    ids_d = [torch.from_numpy(x).to(dev) for x in ids_h]
+    out = torch.empty((EMBED_T, c.k), dtype=dt, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(ids, o):
+        wo.wo_embed(ids, EMBED_T, B, s, z, o, c.n, c.k, c.group_size, c.bits, inputs.BF16, stream)
+
+    with torch.cuda.stream(stream):
+        call(ids_d[0], out)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()  # one replay = one call per id set
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(EMBED_SETS):
+                call(ids_d[i], out)
+    torch.cuda.synchronize()
+    bytes_per_call = EMBED_T * embed_bytes_per_row(c)
+    sampler = ClockSampler(local)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(ws, start.elapsed_time(end))
+    calls = args.steps * EMBED_SETS
+    value = bytes_per_call * calls * ws / (total_ms / 1e3) / 1e9
+
+    # end to end: every call copies its ids in from pinned host memory and its
+    # rows out, serially on one stream
+    hI = [torch.from_numpy(x).pin_memory() for x in ids_h]
+    hO = torch.empty((EMBED_T, c.k), dtype=dt, pin_memory=True)
+    dI = torch.empty(EMBED_T, dtype=torch.int32, device=dev)
+    e2e_calls = max(1, min(calls, 40))
+
+    def e2e_call(i):
+        with torch.cuda.stream(stream):
+            dI.copy_(hI[i % EMBED_SETS], non_blocking=True)
+            wo.embed(dI, B, s, c.n, c.k, c.bits, group_size=c.group_size, zeros=z, out=out,
+                     stream=stream)
+            hO.copy_(out, non_blocking=True)
+    for i in range(3):
+        e2e_call(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_calls):
+        e2e_call(i)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(ws, time.perf_counter() - t0)
+    if rank != 0:
+        return 0
+    hbm_gbs, _, peak_src = measured_peaks()
+    achieved = bytes_per_call / (total_ms / calls / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w["desc"], "calls_per_step": EMBED_SETS,
+                   "bytes_per_call": bytes_per_call,
+                   "l2": "the 4 id sets gather 344 MB of rows and output per step: larger than L2",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "peak_source": f"hbm_gbs ({peak_src})",
+                     "traffic": embed_traffic(), "kernel": "embed_kernel",
+                     "algorithmic_bytes_per_launch": bytes_per_call,
+                     "timing": f"{EMBED_SETS} launches per step in one CUDA graph"},
+        "e2e": {"value": bytes_per_call * e2e_calls * ws / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": EMBED_T * 4, "d2h_bytes_per_step": EMBED_T * c.k * 2,
+                "copies": "every call: pinned H2D of its ids, D2H of its rows, one stream"},
+        "gpu_launches": calls,
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        nids = 2048
+        t0 = time.perf_counter()
+        oracle.embed(ids_h[0][:nids], c.B, c.scales, c.zeros, c.n, c.k, c.group_size, c.bits,
+                     c.act_dtype)
+        dtc = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": nids * embed_bytes_per_row(c) / dtc / 1e9, "unit": "GB/s",
+                                "cores": 1, "kind": "oracle",
+                                "sample": f"{nids} of the ids, {dtc:.2f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
     if args.workload == "moe":
         return run_reference_moe(args)
+    if args.workload == "embed":
+        return run_reference_embed(args)
     w = WORKLOADS[args.workload]
     cases = workload_cases(args.workload)
     import oracle
@@ -767,6 +939,8 @@ def main():
         rc = run_reference(args, ws, rank)
     elif args.workload == "moe":
         rc = run_moe(args, ws, rank, local)
+    elif args.workload == "embed":
+        rc = run_embed(args, ws, rank, local)
     else:
         rc = run_ours(args, ws, rank, local)
     if ws > 1:

@@ -136,7 +136,7 @@ WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* sca
  *   scales, zeros, group_size, bits: as for wo_gemm (n = vocab, k = hidden).
  *   out:      act_dtype [T, hidden], row-major.
  * Requires vocab % 64 == 0, hidden % 64 == 0; T == 0 is a no-op.  Pointers:
- * ids 4-byte, B_packed 16-byte, scales, zeros and out 2-byte aligned.
+ * ids 4-byte, B_packed and out 16-byte, scales and zeros 2-byte aligned.
  * Bit-identical to rounding the oracle's fp32 dequantised rows.
  */
 WO_API wo_status wo_embed(const int32_t* ids, int T, const uint8_t* B_packed, const void* scales,

@@ -209,11 +209,17 @@ def embed(ids, B, scales, zeros, vocab, hidden, group_size, bits, act_dtype) -> 
     """Embedding rows: act_dtype bit patterns [T, hidden], row t = the fp32
     dequantised weight row ids[t] rounded once (a zero row for an id outside
     [0, vocab))."""
-    w = dequant(B, scales, zeros, vocab, hidden, group_size, bits, act_dtype)
     idx = np.asarray(ids, dtype=np.int64).reshape(-1)
-    rows = np.zeros((idx.size, hidden), dtype=np.float64)
     ok = (idx >= 0) & (idx < vocab)
-    rows[ok] = w[idx[ok]]
+    sel = idx[ok]
+    G = 1 if group_size in (-1, hidden) else hidden // group_size
+    # the selected rows' codes, scales and zeros, dequantised as a table of their own
+    Bs = np.asarray(B).reshape(vocab, -1)[sel]
+    ss = np.asarray(scales).reshape(vocab, G)[sel]
+    zs = None if zeros is None else np.asarray(zeros).reshape(vocab, G)[sel]
+    rows = np.zeros((idx.size, hidden), dtype=np.float64)
+    if sel.size:
+        rows[ok] = dequant(Bs, ss, zs, sel.size, hidden, group_size, bits, act_dtype)
     return round_to(rows, act_dtype)
 
 

@@ -152,6 +152,7 @@ def test_selftest_rejects_bad_arguments_without_launching(lib):
     (dict(T=4, bits=8, group=-1, zeros=64), 2),    # 8-bit tables have no zeros
     (dict(T=4, ids=4098), 1),                      # ids not 4-byte aligned
     (dict(T=4, B=4104), 1),                        # packed table not 16-byte aligned
+    (dict(T=4, out=16392), 1),                     # output not 16-byte aligned
     (dict(T=4, act=7), 1),                         # bad activation dtype
     (dict(T=-1), 1),
 ])

@@ -194,7 +194,7 @@ wo_status wo_embed(const int32_t* ids, int T, const uint8_t* B_packed, const voi
         return WO_OK;
     if (!ids || !B_packed || !scales || !out)
         return WO_ERR_INVALID_ARG;
-    if (!aligned(ids, 4) || !aligned(B_packed, 16) || !aligned(scales, 2) || !aligned(out, 2) ||
+    if (!aligned(ids, 4) || !aligned(B_packed, 16) || !aligned(scales, 2) || !aligned(out, 16) ||
         (zeros && !aligned(zeros, 2)))
         return WO_ERR_INVALID_ARG;
     return cuda_status(launch_embed(ids, T, B_packed, scales, zeros, out, vocab, hidden, g, bits,

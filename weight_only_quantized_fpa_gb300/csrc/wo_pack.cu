@@ -123,61 +123,98 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
 // CPUInt4EmbeddingMethod.embedding: gather the rows of the token ids,
 // dequantise w = (q - offset) * scale (+ zero) in fp32, round once to the
 // activation dtype).  Row r of a 16-row block lives in lanes 4 (r % 8) + t,
-// t = 0..3, of each of its block's tiles, so one thread per (token, k tile,
-// t) reads one 16-byte lane chunk and writes the codes of that chunk that
-// belong to the row; ids outside [0, vocab) give a zero row.
+// t = 0..3, of each of its block's tiles.  A warp takes one token and
+// kEmbedTiles consecutive k tiles: lane L reads the 16-byte chunk t = L % 4
+// of tile L / 4, writes the codes of its row into a shared-memory copy of
+// the row segment, and the warp then stores the segment with 16-byte
+// stores (one tile per lane measured faster than two, at more warps of
+// work).  Ids outside [0, vocab) give a zero row.
+constexpr int kEmbedTiles = 8;
+constexpr int kEmbedPerLane = kEmbedTiles / 8;
+constexpr int kEmbedWarps = 8;
+
 template <int BITS, int ACT>
-__global__ void embed_kernel(const int32_t* __restrict__ ids, int T, const uint8_t* __restrict__ B,
-                             const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
-                             uint16_t* __restrict__ out, int vocab, int hidden, int G, int group)
+__global__ void __launch_bounds__(kEmbedWarps * 32)
+    embed_kernel(const int32_t* __restrict__ ids, int T, const uint8_t* __restrict__ B,
+                 const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
+                 uint16_t* __restrict__ out, int vocab, int hidden, int G, int group)
 {
     constexpr int KT = Geom<BITS>::KT;
+    constexpr int SEG = kEmbedTiles * KT;  // values of a warp's row segment
+    __shared__ __align__(16) uint16_t seg_sm[kEmbedWarps][SEG];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint16_t* seg = seg_sm[warp];
     const int ktiles = hidden / KT;
-    const long long total = (long long)T * ktiles * 4;
-    for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < total;
-         c += (long long)gridDim.x * blockDim.x) {
-        const int t4 = (int)(c & 3);
-        const int kt = (int)((c >> 2) % ktiles);
-        const int tok = (int)((c >> 2) / ktiles);
+    const int segs = (ktiles + kEmbedTiles - 1) / kEmbedTiles;  // segments per row
+    const long long total = (long long)T * segs;
+    for (long long w = (long long)blockIdx.x * kEmbedWarps + warp; w < total;
+         w += (long long)gridDim.x * kEmbedWarps) {
+        const int tok = (int)(w / segs), sg = (int)(w % segs);
         const int id = ids[tok];
         const bool valid = id >= 0 && id < vocab;
-        const int r = valid ? id % 16 : 0;  // an invalid id writes row 0's positions with zeros
-        const int g = r & 7;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid)
-            v = *reinterpret_cast<const uint4*>(B + ((((size_t)(id / 16) * ktiles + kt) * 32 + 4 * g + t4) * 16));
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-        uint16_t* orow = out + (size_t)tok * hidden + (size_t)kt * KT;
-        auto put = [&](int kk, int q) {
-            float w = 0.f;
-            if (valid) {
-                const int kg = kt * KT + kk;
-                const size_t gi = (size_t)id * G + kg / group;
-                w = (float)(q - (BITS == 8 ? 128 : 8)) * to_f32<ACT>(scales[gi]);
-                if (zeros)
-                    w += to_f32<ACT>(zeros[gi]);
+        const int r = valid ? id % 16 : 0;
+        const int g = r & 7, t4 = lane & 3;
+        uint4 vj[kEmbedPerLane];
+        float scj[kEmbedPerLane], zcj[kEmbedPerLane];
+#pragma unroll
+        for (int j = 0; j < kEmbedPerLane; ++j) {
+            const int kt = sg * kEmbedTiles + (lane >> 2) + 8 * j;
+            vj[j] = make_uint4(0u, 0u, 0u, 0u);
+            scj[j] = zcj[j] = 0.f;
+            if (valid && kt < ktiles) {
+                vj[j] = *reinterpret_cast<const uint4*>(
+                    B + ((((size_t)(id / 16) * ktiles + kt) * 32 + 4 * g + t4) * 16));
+                // one scale (and zero) per k tile: groups are whole tiles or more
+                const size_t gi = (size_t)id * G + (size_t)(kt * KT) / group;
+                scj[j] = to_f32<ACT>(scales[gi]);
+                zcj[j] = zeros ? to_f32<ACT>(zeros[gi]) : 0.f;
             }
-            orow[kk] = from_f32<ACT>(w);
-        };
-        if constexpr (BITS == 8) {
-#pragma unroll
-            for (int b = 0; b < 16; ++b) {
-                int row, kk;
-                u8_coord(b, g, t4, row, kk);
-                if (row == r)
-                    put(kk, (int)((words[b >> 2] >> (8 * (b & 3))) & 0xFFu));
-            }
-        } else {
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4)
-#pragma unroll
-                for (int p4 = 0; p4 < 8; ++p4) {
-                    int row, kk;
-                    u4_coord(s4, p4, g, t4, row, kk);
-                    if (row == r)
-                        put(kk, (int)((words[s4] >> (4 * p4)) & 0xFu));
-                }
         }
+#pragma unroll
+        for (int j = 0; j < kEmbedPerLane; ++j) {
+          const int tl = (lane >> 2) + 8 * j;
+          const int kt = sg * kEmbedTiles + tl;
+          if (kt < ktiles) {
+            const uint32_t words[4] = {vj[j].x, vj[j].y, vj[j].z, vj[j].w};
+            const float sc = scj[j], zc = zcj[j];
+            auto put = [&](int kk, int q) {
+                float x = 0.f;
+                if (valid) {
+                    x = (float)(q - (BITS == 8 ? 128 : 8)) * sc;
+                    if (zeros)
+                        x += zc;
+                }
+                seg[tl * KT + kk] = from_f32<ACT>(x);
+            };
+            if constexpr (BITS == 8) {
+#pragma unroll
+                for (int b = 0; b < 16; ++b) {
+                    int row, kk;
+                    u8_coord(b, g, t4, row, kk);
+                    if (row == r)
+                        put(kk, (int)((words[b >> 2] >> (8 * (b & 3))) & 0xFFu));
+                }
+            } else {
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+                    for (int p4 = 0; p4 < 8; ++p4) {
+                        int row, kk;
+                        u4_coord(s4, p4, g, t4, row, kk);
+                        if (row == r)
+                            put(kk, (int)((words[s4] >> (4 * p4)) & 0xFu));
+                    }
+            }
+          }
+        }
+        __syncwarp();
+        // the segment's valid part: 16-byte stores, consecutive lanes
+        const int nvals = (ktiles - sg * kEmbedTiles < kEmbedTiles ? ktiles - sg * kEmbedTiles : kEmbedTiles) * KT;
+        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)tok * hidden + (size_t)sg * SEG);
+        const uint4* src = reinterpret_cast<const uint4*>(seg);
+        for (int i = lane; i < nvals / 8; i += 32)
+            dst[i] = src[i];
+        __syncwarp();
     }
 }
 
@@ -188,9 +225,10 @@ cudaError_t launch_embed(const int32_t* ids, int T, const uint8_t* B, const void
                          int act, cudaStream_t s)
 {
     const int KT = bits == 8 ? 32 : 64;
-    const long long total = (long long)T * (hidden / KT) * 4;
-    const int threads = 256;
-    long long blocks = (total + threads - 1) / threads;
+    const long long segs = (hidden / KT + kEmbedTiles - 1) / kEmbedTiles;
+    const long long total = (long long)T * segs;  // warps of work
+    const int threads = kEmbedWarps * 32;
+    long long blocks = (total + kEmbedWarps - 1) / kEmbedWarps;
     const long long cap = (long long)num_sms() * 16;
     if (blocks > cap)
         blocks = cap;

@@ -16,6 +16,10 @@ Functions and the page passages they follow:
   int8 scale; group-wise int4 scale and zero).
 * ``gemm`` -- acext User Guide 1.2.1 (fpA_intB runner ``gemm`` with scales,
   zero points, biases and group_size).
+* ``dequant_gidx`` / ``gemm_gidx`` -- the same with a GPTQ act-order group
+  index (``desc_act`` / ``has_g_idx`` in "[Misc][Kernel]: Add GPTQAllSpark
+  Quantization", the case its kernel leaves out): input channel c takes the
+  scale and zero of group ``g_idx[c]``; nothing is permuted.
 * ``embed`` -- vLLM-Omni ``cpu_int4.py`` ``CPUInt4EmbeddingMethod.embedding``
   (rows of the token ids, dequantised in fp32, cast to the activation dtype).
 * ``moe_route`` / ``moe_ffn`` -- acext User Guide 1.2.3 (MoE runner: gating
@@ -90,6 +94,11 @@ def _load():
         lib.oracle_dequant.restype = i32
         lib.oracle_gemm.argtypes = [P, i32, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
         lib.oracle_gemm.restype = i32
+        lib.oracle_dequant_gidx.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P]
+        lib.oracle_dequant_gidx.restype = i32
+        lib.oracle_gemm_gidx.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                         P]
+        lib.oracle_gemm_gidx.restype = i32
         lib.oracle_moe_route.argtypes = [P, i32, i32, i32, i32, P, P]
         lib.oracle_moe_route.restype = i32
         lib.oracle_moe_ffn.argtypes = [P, i32, P, P, P, P, P, i32, i32, i32, i32, i32,
@@ -202,6 +211,43 @@ def gemm(A, act_dtype, B, scales, zeros, bias, m, n, k, group_size, bits,
     nt = default_threads() if nthreads is None else nthreads
     _check(_load().oracle_gemm(_ptr(Ac), act_dtype, _ptr(Bc), _ptr(s), _ptr(z), _ptr(b),
                                m, n, k, group_size, bits, nt, _ptr(C)), "gemm")
+    return C
+
+
+def _gidx(g_idx, k) -> np.ndarray:
+    g = np.ascontiguousarray(g_idx, dtype=np.int32).reshape(-1)
+    if g.size != k:
+        raise ValueError("g_idx must have k entries")
+    return g
+
+
+def dequant_gidx(B, scales, zeros, g_idx, n, k, group_size, bits, sz_dtype) -> np.ndarray:
+    """fp32 [n, k] dequantised weights, channel c scaled by group g_idx[c]."""
+    Bc = _u8(B, "B")
+    s = _u16(scales, "scales")
+    z = None if zeros is None else _u16(zeros, "zeros")
+    g = _gidx(g_idx, k)
+    w = np.empty((n, k), dtype=np.float32)
+    _check(_load().oracle_dequant_gidx(_ptr(Bc), _ptr(s), _ptr(z), _ptr(g), n, k, group_size,
+                                       bits, sz_dtype, _ptr(w)), "dequant_gidx")
+    return w
+
+
+def gemm_gidx(A, act_dtype, B, scales, zeros, g_idx, bias, m, n, k, group_size, bits,
+              nthreads: int | None = None) -> np.ndarray:
+    """fp64 C [m, n] of an act-order checkpoint: input channel c takes the
+    scale and zero of group g_idx[c]; A, B and C in the original order."""
+    Ac = _u16(A, "A")
+    Bc = _u8(B, "B")
+    s = _u16(scales, "scales")
+    z = None if zeros is None else _u16(zeros, "zeros")
+    g = _gidx(g_idx, k)
+    b = None if bias is None else _u16(bias, "bias")
+    C = np.empty((m, n), dtype=np.float64)
+    nt = default_threads() if nthreads is None else nthreads
+    _check(_load().oracle_gemm_gidx(_ptr(Ac), act_dtype, _ptr(Bc), _ptr(s), _ptr(z), _ptr(g),
+                                    _ptr(b), m, n, k, group_size, bits, nt, _ptr(C)),
+           "gemm_gidx")
     return C
 
 

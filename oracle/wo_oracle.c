@@ -18,7 +18,10 @@
  *             byte j = w[2j] | w[2j+1] << 4; w = (q - 8) * scale + zero) and
  *             functions pack_nibbles / unpack_nibbles.
  *   [allspark] "[Misc][Kernel]: Add GPTQAllSpark Quantization": A16W8,
- *             group_size = -1 (per channel), no act-order.
+ *             group_size = -1 (per channel), no act-order; its kernel
+ *             choice names desc_act / has_g_idx (GPTQ act-order, a group
+ *             index per input channel) as the case it leaves out, which
+ *             oracle_gemm_gidx covers.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   - int8 codes are stored as uint8 0..255 and dequantise as (q - 128) * s
@@ -213,6 +216,7 @@ typedef struct {
     const uint8_t* B;       /* row-major codes, see oracle_unpack_codes */
     const uint16_t* scales; /* [n, G] (G = k / group) in sz_dtype        */
     const uint16_t* zeros;  /* [n, G] or NULL (= 0)                     */
+    const int32_t* g_idx;   /* [k] group of each input channel, or NULL  */
     int n, k, group, G, bits, sz_dtype;
 } wdesc;
 
@@ -230,6 +234,7 @@ static int make_wdesc(wdesc* d, const uint8_t* B, const uint16_t* scales,
     d->B = B;
     d->scales = scales;
     d->zeros = zeros;
+    d->g_idx = NULL;
     d->n = n;
     d->k = k;
     d->group = group;
@@ -241,11 +246,14 @@ static int make_wdesc(wdesc* d, const uint8_t* B, const uint16_t* scales,
 
 /*
  * One dequantised weight row w[r][0..k) in fp32:
- *   bits 4: w = (q - 8) * scale[r][c/group] + zero[r][c/group]
+ *   bits 4: w = (q - 8) * scale[r][g(c)] + zero[r][g(c)]
  *           ([cpu_int4] module docstring; [acext] 1.3.3 group-wise scales);
- *   bits 8: w = (q - 128) * scale[r][c/group] (+ zero when given)
+ *   bits 8: w = (q - 128) * scale[r][g(c)] (+ zero when given)
  *           ([acext] 1.3.1: one scale per output channel; the 128 offset is
  *           the uint8 storage of a symmetric int8 code).
+ * g(c) = c / group, or g_idx[c] when a GPTQ act-order group index is given
+ * ([allspark] names desc_act / has_g_idx as the case its kernel excludes:
+ * each input channel c carries its own group number instead of c / group).
  * The product and the sum are separate fp32 operations.
  */
 static void dequant_row(const wdesc* d, int r, float* w)
@@ -259,7 +267,8 @@ static void dequant_row(const wdesc* d, int r, float* w)
             uint8_t byte = d->B[(size_t)r * (d->k / 2) + c / 2];
             q = (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
         }
-        size_t gi = (size_t)r * d->G + (size_t)(c / d->group);
+        const int g = d->g_idx ? d->g_idx[c] : c / d->group;
+        size_t gi = (size_t)r * d->G + (size_t)g;
         float s = (float)decode_act(d->scales[gi], d->sz_dtype);
         float prod = (float)(q - off) * s;
         float z = d->zeros ? (float)decode_act(d->zeros[gi], d->sz_dtype) : 0.0f;
@@ -267,11 +276,37 @@ static void dequant_row(const wdesc* d, int r, float* w)
     }
 }
 
+/* Attach a per-channel group index: every entry must name a group. */
+static int set_g_idx(wdesc* d, const int32_t* g_idx)
+{
+    if (!g_idx)
+        return OR_OK;
+    for (int c = 0; c < d->k; ++c)
+        if (g_idx[c] < 0 || g_idx[c] >= d->G)
+            return OR_BAD;
+    d->g_idx = g_idx;
+    return OR_OK;
+}
+
 int oracle_dequant(const uint8_t* B, const uint16_t* scales, const uint16_t* zeros,
                    int n, int k, int group_size, int bits, int sz_dtype, float* w)
 {
     wdesc d;
     if (make_wdesc(&d, B, scales, zeros, n, k, group_size, bits, sz_dtype) != OR_OK)
+        return OR_BAD;
+    for (int r = 0; r < n; ++r)
+        dequant_row(&d, r, w + (size_t)r * k);
+    return OR_OK;
+}
+
+/* oracle_dequant with a GPTQ act-order group index g_idx[k] (see dequant_row). */
+int oracle_dequant_gidx(const uint8_t* B, const uint16_t* scales, const uint16_t* zeros,
+                        const int32_t* g_idx, int n, int k, int group_size, int bits,
+                        int sz_dtype, float* w)
+{
+    wdesc d;
+    if (make_wdesc(&d, B, scales, zeros, n, k, group_size, bits, sz_dtype) != OR_OK ||
+        set_g_idx(&d, g_idx) != OR_OK)
         return OR_BAD;
     for (int r = 0; r < n; ++r)
         dequant_row(&d, r, w + (size_t)r * k);
@@ -322,12 +357,14 @@ static void* gemm_worker(void* arg)
  * nthreads > 1 splits the output channels across threads; each element is
  * still one ascending-k sum, so the result does not depend on nthreads.
  */
-int oracle_gemm(const uint16_t* A, int act_dtype, const uint8_t* B,
-                const uint16_t* scales, const uint16_t* zeros, const uint16_t* bias,
-                int m, int n, int k, int group_size, int bits, int nthreads, double* C)
+static int gemm_common(const uint16_t* A, int act_dtype, const uint8_t* B,
+                       const uint16_t* scales, const uint16_t* zeros, const int32_t* g_idx,
+                       const uint16_t* bias, int m, int n, int k, int group_size, int bits,
+                       int nthreads, double* C)
 {
     gemm_job base;
-    if (make_wdesc(&base.d, B, scales, zeros, n, k, group_size, bits, act_dtype) != OR_OK)
+    if (make_wdesc(&base.d, B, scales, zeros, n, k, group_size, bits, act_dtype) != OR_OK ||
+        set_g_idx(&base.d, g_idx) != OR_OK)
         return OR_BAD;
     if (m < 0)
         return OR_BAD;
@@ -377,6 +414,31 @@ int oracle_gemm(const uint16_t* A, int act_dtype, const uint8_t* B,
     free(Ad);
     free(bd);
     return rc;
+}
+
+int oracle_gemm(const uint16_t* A, int act_dtype, const uint8_t* B,
+                const uint16_t* scales, const uint16_t* zeros, const uint16_t* bias,
+                int m, int n, int k, int group_size, int bits, int nthreads, double* C)
+{
+    return gemm_common(A, act_dtype, B, scales, zeros, NULL, bias, m, n, k, group_size, bits,
+                       nthreads, C);
+}
+
+/*
+ * The GEMM of a GPTQ act-order checkpoint ([allspark]: desc_act, has_g_idx):
+ * B, A and C keep the original input-channel order, and input channel c
+ * takes the scale and zero of group g_idx[c] (0 <= g_idx[c] < k / group).
+ * No permutation is applied anywhere: the sum still runs over c ascending.
+ */
+int oracle_gemm_gidx(const uint16_t* A, int act_dtype, const uint8_t* B,
+                     const uint16_t* scales, const uint16_t* zeros, const int32_t* g_idx,
+                     const uint16_t* bias, int m, int n, int k, int group_size, int bits,
+                     int nthreads, double* C)
+{
+    if (!g_idx)
+        return OR_BAD;
+    return gemm_common(A, act_dtype, B, scales, zeros, g_idx, bias, m, n, k, group_size, bits,
+                       nthreads, C);
 }
 
 /* ------------------------------------------------------------------------ */

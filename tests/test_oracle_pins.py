@@ -422,6 +422,119 @@ def test_gemm_rejects_bad_group():
         oracle.gemm(c.A, BF16, c.B, c.scales, c.zeros, None, c.m, c.n, c.k, 100, 4)
 
 
+# ------------------------------------------------- act-order (GPTQ g_idx) ---
+
+def _permute_codes(B, n, k, bits, perm):
+    """Row-major codes with input channel j taken from channel perm[j]."""
+    q = _test_unpack(B, n, k, bits)[:, perm]
+    if bits == 8:
+        return np.ascontiguousarray(q.astype(np.uint8))
+    q = q.astype(np.uint8)
+    return np.ascontiguousarray(q[:, 0::2] | (q[:, 1::2] << 4))
+
+
+def _gidx_case(seed, m, n, k, group, dtype=BF16, bias=False):
+    c = inputs.make_gemm_case(11, seed, m, n, k, bits=4, group_size=group, act_dtype=dtype,
+                              scale_lo=0.005, scale_hi=0.02, with_zeros=True, with_bias=bias)
+    g = inputs.act_order_g_idx(inputs.rng_for(11, seed, inputs.T_GIDX), k, group)
+    return c, g
+
+
+@pytest.mark.parametrize("group,dtype", [(64, BF16), (128, F16)])
+def test_gidx_in_order_equals_grouped_gemm(group, dtype):
+    # g_idx[c] = c // group (GPTQ without act-order, or static groups) is the
+    # plain group-wise GEMM, bit for bit
+    m, n, k = 3, 32, 512
+    c, _ = _gidx_case(1 + group, m, n, k, group, dtype, bias=True)
+    g = (np.arange(k) // group).astype(np.int32)
+    got = oracle.gemm_gidx(c.A, dtype, c.B, c.scales, c.zeros, g, c.bias, m, n, k, group, 4)
+    ref = oracle.gemm(c.A, dtype, c.B, c.scales, c.zeros, c.bias, m, n, k, group, 4)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(oracle.dequant_gidx(c.B, c.scales, c.zeros, g, n, k, group, 4, dtype),
+                          oracle.dequant(c.B, c.scales, c.zeros, n, k, group, 4, dtype))
+
+
+def test_gidx_brute_force():
+    m, n, k, group = 2, 8, 128, 64
+    c, g = _gidx_case(2, m, n, k, group, BF16, bias=True)
+    q = _test_unpack(c.B, n, k, 4).tolist()
+    A = _value(c.A, BF16).reshape(m, k).tolist()
+    S = _value(c.scales, BF16).reshape(n, -1).tolist()
+    Z = _value(c.zeros, BF16).reshape(n, -1).tolist()
+    bias = _value(c.bias, BF16).tolist()
+    ref = np.zeros((m, n))
+    for j in range(n):
+        w = [float(np.float32(np.float32(q[j][kk] - 8) * np.float32(S[j][g[kk]]))
+                   + np.float32(Z[j][g[kk]])) for kk in range(k)]
+        for i in range(m):
+            acc = 0.0
+            for kk in range(k):
+                acc += A[i][kk] * w[kk]
+            ref[i, j] = acc + bias[j]
+    got = oracle.gemm_gidx(c.A, BF16, c.B, c.scales, c.zeros, g, c.bias, m, n, k, group, 4)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_gidx_is_invariant_under_channel_permutation():
+    # reordering the input channels of A, B and g_idx together is the same
+    # sum in another order
+    m, n, k, group = 4, 48, 384, 64
+    c, g = _gidx_case(3, m, n, k, group, BF16)
+    pi = inputs.rng_for(11, 3, 12).permutation(k)
+    Ap = np.ascontiguousarray(c.A.reshape(m, k)[:, pi])
+    Bp = _permute_codes(c.B, n, k, 4, pi)
+    got = oracle.gemm_gidx(Ap, BF16, Bp, c.scales, c.zeros, g[pi], None, m, n, k, group, 4)
+    ref = oracle.gemm_gidx(c.A, BF16, c.B, c.scales, c.zeros, g, None, m, n, k, group, 4)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_gidx_sorted_by_group_is_grouped_gemm():
+    # sorting the channels by group (stable) makes every group contiguous, so
+    # the act-order GEMM becomes the plain group-wise GEMM of the sorted
+    # operands
+    m, n, k, group = 3, 32, 512, 128
+    c, g = _gidx_case(4, m, n, k, group, F16, bias=True)
+    sigma = np.argsort(g, kind="stable")
+    As = np.ascontiguousarray(c.A.reshape(m, k)[:, sigma])
+    Bs = _permute_codes(c.B, n, k, 4, sigma)
+    ref = oracle.gemm(As, F16, Bs, c.scales, c.zeros, c.bias, m, n, k, group, 4)
+    got = oracle.gemm_gidx(c.A, F16, c.B, c.scales, c.zeros, g, c.bias, m, n, k, group, 4)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_gidx_channel_reads_only_its_own_group():
+    # A = e_c: the output depends on the scale and zero of group g_idx[c]
+    # and on no other group's
+    m, n, k, group = 1, 16, 256, 64
+    c, g = _gidx_case(5, m, n, k, group, BF16)
+    G = k // group
+    one = inputs.to_bits(np.array([1.0]), BF16)[0]
+    two = inputs.to_bits(np.array([2.0]), BF16)[0]
+    for col in (0, 77, 255):
+        A = np.zeros((1, k), dtype=np.uint16)
+        A[0, col] = one
+        base = oracle.gemm_gidx(A, BF16, c.B, c.scales, c.zeros, g, None, 1, n, k, group, 4)
+        for gg in range(G):
+            s2 = c.scales.reshape(n, G).copy()
+            s2[:, gg] = two
+            z2 = c.zeros.reshape(n, G).copy()
+            z2[:, gg] = two
+            C2 = oracle.gemm_gidx(A, BF16, c.B, s2, z2, g, None, 1, n, k, group, 4)
+            assert np.array_equal(C2, base) == (gg != g[col])
+
+
+def test_gidx_rejects_out_of_range_group():
+    m, n, k, group = 1, 16, 128, 64
+    c, g = _gidx_case(6, m, n, k, group)
+    bad = g.copy()
+    bad[5] = k // group
+    with pytest.raises(ValueError):
+        oracle.gemm_gidx(c.A, BF16, c.B, c.scales, c.zeros, bad, None, m, n, k, group, 4)
+    bad[5] = -1
+    with pytest.raises(ValueError):
+        oracle.gemm_gidx(c.A, BF16, c.B, c.scales, c.zeros, bad, None, m, n, k, group, 4)
+
+
 # -------------------------------------------------------------------- MoE ---
 
 def test_route_ties_go_to_lower_expert():

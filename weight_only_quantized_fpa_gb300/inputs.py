@@ -16,10 +16,14 @@ Recipe (one numpy PCG64 stream per tensor, seed = 0x5EED0000 + 4096*config +
 * scales: uniform on [lo, hi) in fp64, rounded into the activation dtype;
 * zeros: normal with standard deviation 0.01; bias: normal with standard
   deviation 0.1 (the second parameter of N(mu, sigma) read as sigma);
-* gating logits: standard normal, fp32.
+* gating logits: standard normal, fp32;
+* act-order group index (GPTQ ``g_idx``): a uniformly random order of the k
+  input channels stands in for the quantiser's column order; the i-th
+  channel in that order belongs to group i // group_size, so every group has
+  group_size channels scattered over k.
 
 Tensor ids: A=1, codes=2, scale=3, zero=4, bias=5, logits=6, fc1 codes=7,
-fc1 scales=8, fc2 codes=9, fc2 scales=10.
+fc1 scales=8, fc2 codes=9, fc2 scales=10, g_idx=11.
 """
 from __future__ import annotations
 
@@ -32,6 +36,7 @@ BF16 = 1
 
 T_A, T_CODES, T_SCALE, T_ZERO, T_BIAS, T_LOGITS = 1, 2, 3, 4, 5, 6
 T_FC1, T_FC1_S, T_FC2, T_FC2_S = 7, 8, 9, 10
+T_GIDX = 11
 
 
 def seed_for(config: int, case: int, tensor: int) -> int:
@@ -68,6 +73,14 @@ def uniform_bits(rng, shape, dtype, lo, hi) -> np.ndarray:
 
 def code_bytes(rng, shape) -> np.ndarray:
     return rng.integers(0, 256, size=shape, dtype=np.uint8)
+
+
+def act_order_g_idx(rng, k: int, group_size: int) -> np.ndarray:
+    """int32 [k] group index of an act-order checkpoint (see the recipe)."""
+    order = rng.permutation(k)
+    g = np.empty(k, dtype=np.int32)
+    g[order] = np.arange(k, dtype=np.int32) // group_size
+    return g
 
 
 @dataclass

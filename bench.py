@@ -56,6 +56,12 @@ WORKLOADS = {
     "w8_large": dict(config=3, unit="TFLOP/s", dtype="f16",
                      desc="A16W8 per-channel large m: m in {256,1024,4096,8192}; (N,K) in "
                           "{(2048,2048),(4096,4096),(4608,3584)}, fp16"),
+    "w4_act_order": dict(config=6, unit="GB/s", dtype="bf16",
+                         desc="W4A16 GPTQ act-order (g_idx), group 128, asymmetric, bf16: the "
+                              "w4_g64 shapes (m in {1,512}; (N,K) in {(2048,2048),(3072,2048),"
+                              "(13312,2048),(131072,2048),(2048,13312)}); g_idx = a random "
+                              "channel order cut into groups of 128; bytes = codes, scales, "
+                              "zeros"),
     "w4_tiny": dict(config=1, unit="GB/s", dtype="bf16",
                     desc="W4A16 tiny: m=1, N=256, K=512, group 64, bf16"),
     "moe": dict(config=5, unit="GB/s", dtype="bf16",
@@ -123,6 +129,14 @@ def workload_cases(name: str):
 
 def case_flops(c) -> float:
     return 2.0 * c.m * c.n * c.k
+
+
+def case_launches(c) -> int:
+    """This library's kernels per GEMM call: the act-order column gather, the
+    fp16 copy of bf16 activations (4-bit weights on the tensor cores), the
+    GEMM kernel."""
+    tc = c.m >= 65
+    return ((c.g_idx is not None) + (tc and c.bits == 4 and c.act_dtype == inputs.BF16) + 1)
 
 
 def measured_peaks():
@@ -236,8 +250,12 @@ def oracle_pass(cases, frac: float, threads: int):
         n_sub = max(64, int(c.n * frac) // 64 * 64)
         s = slice_case(c, n_sub)
         m_sub = c.m if c.m <= 64 else max(1, int(c.m * frac))
-        oracle.gemm(s.A[:m_sub], s.act_dtype, s.B, s.scales, s.zeros, s.bias, m_sub, s.n, s.k,
-                    s.group_size, s.bits, nthreads=threads)
+        if s.g_idx is not None:
+            oracle.gemm_gidx(s.A[:m_sub], s.act_dtype, s.B, s.scales, s.zeros, s.g_idx, s.bias,
+                             m_sub, s.n, s.k, s.group_size, s.bits, nthreads=threads)
+        else:
+            oracle.gemm(s.A[:m_sub], s.act_dtype, s.B, s.scales, s.zeros, s.bias, m_sub, s.n,
+                        s.k, s.group_size, s.bits, nthreads=threads)
         wbytes += s.weight_bytes
         flops += 2.0 * m_sub * s.n * s.k
     return time.perf_counter() - t0, wbytes, flops
@@ -714,13 +732,20 @@ def run_ours(args, ws, rank, local):
     max_ws = 0
     for c in cases:
         Brm = torch.from_numpy(c.B).to(dev)
-        Bp = wo.pack(Brm, c.n, c.k, c.bits)
+        perm = None
+        if c.g_idx is not None:  # act-order: codes packed in group-sorted channel order
+            perm = wo.act_order_perm(c.g_idx, c.k, c.group_size).to(dev)
+            Bp = wo.pack_act_order(Brm, perm, c.n, c.k, c.bits)
+            need = wo.wo_act_order_workspace_size(c.m, c.n, c.k, c.group_size, c.bits)
+        else:
+            Bp = wo.pack(Brm, c.n, c.k, c.bits)
+            need = wo.wo_workspace_size(c.m, c.n, c.k, c.group_size, c.bits)
         del Brm
-        d = dict(c=c, A=up16(c.A, c), B=Bp, s=up16(c.scales, c),
+        d = dict(c=c, A=up16(c.A, c), B=Bp, s=up16(c.scales, c), perm=perm,
                  z=None if c.zeros is None else up16(c.zeros, c),
                  b=None if c.bias is None else up16(c.bias, c),
                  C=torch.empty((c.m, c.n), dtype=dt_of(c), device=dev))
-        max_ws = max(max_ws, wo.wo_workspace_size(c.m, c.n, c.k, c.group_size, c.bits))
+        max_ws = max(max_ws, need)
         dev_cases.append(d)
     workspace = torch.zeros(max(max_ws, 256), dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel()
@@ -728,6 +753,11 @@ def run_ours(args, ws, rank, local):
 
     def call(d, A=None, C=None):
         c = d["c"]
+        if d["perm"] is not None:
+            wo.wo_gemm_act_order(d["A"] if A is None else A, d["B"], d["perm"], d["s"], d["z"],
+                                 d["b"], d["C"] if C is None else C, c.m, c.n, c.k,
+                                 c.group_size, c.bits, c.act_dtype, workspace, ws_bytes, stream)
+            return
         wo.wo_gemm(d["A"] if A is None else A, d["B"], d["s"], d["z"], d["b"],
                    d["C"] if C is None else C, c.m, c.n, c.k, c.group_size, c.bits,
                    c.act_dtype, workspace, ws_bytes, stream)
@@ -750,7 +780,7 @@ def run_ours(args, ws, rank, local):
             graphs.append(g)
     torch.cuda.synchronize()
 
-    launches_per_step = len(cases)  # one kernel per wo_gemm at these sizes
+    launches_per_step = sum(case_launches(c) for c in cases)
     bytes_per_step = sum(c.weight_bytes for c in cases)
     flops_per_step = sum(case_flops(c) for c in cases)
     ncase = len(cases)
@@ -841,6 +871,11 @@ def run_ours(args, ws, rank, local):
         with torch.cuda.stream(stream):
             for d, Av, Cv in zip(dev_cases, a_views[b], c_views[b]):
                 c = d["c"]
+                if d["perm"] is not None:
+                    wo.gemm_act_order(Av, d["B"], d["perm"], d["s"], c.n, c.k, c.bits,
+                                      c.group_size, zeros=d["z"], bias=d["b"], out=Cv,
+                                      workspace=workspace, stream=stream)
+                    continue
                 wo.gemm(Av, d["B"], d["s"], c.n, c.k, c.bits, group_size=c.group_size,
                         zeros=d["z"], bias=d["b"], out=Cv, workspace=workspace,
                         stream=stream)
@@ -867,8 +902,9 @@ def run_ours(args, ws, rank, local):
         return 0
 
     hbm_gbs, bf16_tf, peak_src = measured_peaks()
-    # the step graph holds only this library's kernels, one per case, back to
-    # back: their average duration is the step time over the launches
+    # the step graph holds only this library's kernels, the GEMM kernel of
+    # each case (plus its prepasses: act-order gather, fp16 copy of bf16 A),
+    # back to back: the algorithmic bytes (or flops) over the step time
     kern_ms = total_ms / args.steps
     if w["unit"] == "GB/s":
         achieved = bytes_per_step / (kern_ms / 1e3) / 1e9
@@ -893,7 +929,8 @@ def run_ours(args, ws, rank, local):
     else:
         roof["algorithmic_flops_per_launch"] = flops_per_step / ncase
     roof["kernel"] = kname
-    roof["timing"] = (f"{ncase} launches per step back to back in one CUDA graph; achieved = "
+    roof["timing"] = (f"{ncase} GEMM calls ({launches_per_step} launches) per step back to "
+                      "back in one CUDA graph; achieved = "
                       "algorithmic bytes (or flops) per step / step time")
 
     line = {

@@ -124,6 +124,75 @@ WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* sca
                   size_t workspace_bytes, void* stream);
 
 /*
+ * GPTQ act-order checkpoints ("[Misc][Kernel]: Add GPTQAllSpark
+ * Quantization": the desc_act / has_g_idx case its kernel leaves out).  The
+ * quantiser visited the input channels in its own order, so input channel c
+ * belongs to group g_idx[c] rather than c / group_size:
+ *     C[m, n] = sum_c A[m, c] * ((q[n][c] - 8) * scale[n][g_idx[c]]
+ *                                + zero[n][g_idx[c]]) + bias[n].
+ * A sum over k does not depend on the order of its terms, so sorting the
+ * channels by group turns this into the ordinary group-wise GEMM: the codes
+ * are packed in sorted order once (wo_pack_act_order), and each call gathers
+ * A's columns into the same order before the group-wise kernels run
+ * (wo_gemm_act_order).  scales and zeros stay [n, k/group_size], indexed by
+ * group number; A, B_rowmajor and C keep the checkpoint's channel order.
+ */
+
+/*
+ * The channel order that sorts a group index, on the HOST.
+ *   g_idx: HOST int32 [k], the group of each input channel, 0 <= g_idx[c] <
+ *          k / group_size (group_size -1 or k: one group, all entries 0).
+ *   perm:  HOST int32 [k] output: perm[j] = the j-th channel in order of
+ *          (g_idx[c], c), so positions [b*group_size, (b+1)*group_size) hold
+ *          the channels of group b.
+ * WO_ERR_INVALID_ARG for a null pointer, k <= 0, a group_size that does not
+ * divide k or an entry outside [0, k/group_size); WO_ERR_UNSUPPORTED when the
+ * groups are not all exactly group_size channels (GPTQ's are).  Pure host
+ * code: no CUDA call.
+ */
+WO_API wo_status wo_act_order_perm(const int32_t* g_idx, int k, int group_size, int32_t* perm);
+
+/*
+ * wo_pack with the input channels reordered: packed column j holds
+ * row-major column perm[j].  perm is a DEVICE int32 [k] (4-byte aligned),
+ * the output of wo_act_order_perm copied to the device; an entry outside
+ * [0, k) packs code 0 (no out-of-bounds read).  Other arguments and
+ * requirements as wo_pack.  wo_unpack of the result gives the row-major
+ * codes with columns in the order perm.
+ */
+WO_API wo_status wo_pack_act_order(const uint8_t* B_rowmajor, uint8_t* B_packed,
+                                   const int32_t* perm, int n, int k, int bits, void* stream);
+
+/*
+ * Workspace bytes of wo_gemm_act_order: the wo_gemm workspace of the same
+ * problem, at least its shared header and split-K counter area
+ * (256 + 65536 bytes), rounded up to 256, followed by an act_dtype [m, k]
+ * copy of A in sorted channel order.  0 for invalid arguments or m == 0 or
+ * n == 0.  The zero-fill rule of wo_gemm's workspace applies to the whole
+ * buffer, and one buffer may serve wo_gemm and wo_gemm_act_order calls in
+ * turn (on one stream).
+ */
+WO_API size_t wo_act_order_workspace_size(int m, int n, int k, int group_size, int bits);
+
+/*
+ * The act-order GEMM above.
+ *   A:        act_dtype [m, k] in the checkpoint's channel order.
+ *   B_packed: output of wo_pack_act_order with the same perm.
+ *   perm:     DEVICE int32 [k], 16-byte aligned, from wo_act_order_perm; an
+ *             entry outside [0, k) reads A as 0.
+ *   other arguments, requirements and the ordering rule: as wo_gemm, with
+ *   the workspace sized by wo_act_order_workspace_size.
+ * Runs a column gather of A into the workspace (a programmatic dependent
+ * launch: it reads perm before the previous operation on the stream
+ * completes, A after), then the wo_gemm kernels on the gathered copy.
+ */
+WO_API wo_status wo_gemm_act_order(const void* A, const uint8_t* B_packed, const int32_t* perm,
+                                   const void* scales, const void* zeros, const void* bias,
+                                   void* C, int m, int n, int k, int group_size, int bits,
+                                   wo_dtype act_dtype, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
  * Rows of a quantised embedding (vocab) table, dequantised (vLLM-Omni
  * "cpu_int4.py", CPUInt4EmbeddingMethod.embedding: the rows of the token ids,
  * w = (q - offset) * scale (+ zero) in fp32, rounded once to the activation

@@ -28,7 +28,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["wo_pack", "wo_unpack", "wo_packed_bytes", "wo_workspace_size", "wo_gemm",
               "wo_moe_workspace_size", "wo_moe_ffn", "wo_status_string", "wo_check_workspace",
-              "wo_selftest_wait_timeout", "wo_embed"]:
+              "wo_selftest_wait_timeout", "wo_embed", "wo_act_order_perm",
+              "wo_pack_act_order", "wo_act_order_workspace_size", "wo_gemm_act_order"]:
         assert n in names
 
 
@@ -163,3 +164,88 @@ def test_embed_rejects_bad_arguments_before_launch(lib, kw, expect):
     st = lib.wo_embed(a["ids"], a["T"], a["B"], a["s"], a["zeros"], a["out"], a["vocab"],
                       a["hidden"], a["group"], a["bits"], a["act"], None)
     assert st == expect
+
+
+# ---------------------------------------------------------- act-order -------
+# wo_act_order_perm is host code, so it is tested here in full.
+
+def _perm(g_idx, k, group):
+    import numpy as np
+    out = np.full(k, -7, dtype=np.int32)
+    gi = np.ascontiguousarray(g_idx, dtype=np.int32)   # kept alive across the call
+    st = wo.load_library().wo_act_order_perm(gi.ctypes.data, k, group, out.ctypes.data)
+    return st, out
+
+
+@pytest.mark.parametrize("k,group,seed", [(128, 64, 0), (4096, 128, 1), (3584, 64, 2),
+                                          (512, 512, 3), (512, -1, 4)])
+def test_act_order_perm_is_the_stable_group_sort(lib, k, group, seed):
+    import numpy as np
+    from weight_only_quantized_fpa_gb300 import inputs
+    g = group if group != -1 else k
+    gi = inputs.act_order_g_idx(inputs.rng_for(11, seed, inputs.T_GIDX), k, g)
+    st, perm = _perm(gi, k, group)
+    assert st == 0
+    assert np.array_equal(perm, np.argsort(gi, kind="stable"))
+    # every run of g positions holds one group, channels ascending
+    assert np.array_equal(gi[perm], np.arange(k) // g)
+    assert np.array_equal(np.sort(perm), np.arange(k))
+
+
+def test_act_order_perm_in_order_index_is_identity(lib):
+    import numpy as np
+    k = 1024
+    st, perm = _perm(np.arange(k) // 128, k, 128)
+    assert st == 0 and np.array_equal(perm, np.arange(k))
+
+
+def test_act_order_perm_rejects_bad_indices(lib):
+    import numpy as np
+    k = 256
+    gi = (np.arange(k) // 64).astype(np.int32)
+    bad = gi.copy(); bad[3] = 4          # group 4 does not exist (k / 64 = 4 groups)
+    assert _perm(bad, k, 64)[0] == 1
+    bad = gi.copy(); bad[3] = -1
+    assert _perm(bad, k, 64)[0] == 1
+    bad = gi.copy(); bad[0] = 1          # group 0 short, group 1 long
+    assert _perm(bad, k, 64)[0] == 2
+    assert _perm(gi, k, 100)[0] == 1     # group does not divide k
+    assert _perm(gi, 0, 64)[0] == 1
+    assert lib.wo_act_order_perm(None, k, 64, 4096) == 1
+
+
+def test_act_order_perm_binding_checks_host_arrays(lib):
+    import numpy as np
+    with pytest.raises(ValueError):
+        wo.wo_act_order_perm(np.zeros(10, np.int32), 64, 64, np.empty(64, np.int32))
+    with pytest.raises(ValueError):
+        wo.wo_act_order_perm(np.zeros(64, np.int32), 64, 64, np.empty(64, np.int64))
+
+
+def _ao_status(lib, m=4, n=256, k=512, group=64, bits=4, act=1, A=4096, B=8192, perm=1 << 16,
+               s=64, z=None, bias=None, C=16384, ws=None, ws_bytes=0):
+    return lib.wo_gemm_act_order(A, B, perm, s, z, bias, C, m, n, k, group, bits, act, ws,
+                                 ws_bytes, None)
+
+
+def test_act_order_gemm_rejects_bad_arguments_before_launch(lib):
+    need = wo.wo_act_order_workspace_size(4, 256, 512, 64, 4)
+    plain = wo.wo_workspace_size(4, 256, 512, 64, 4)
+    assert need >= max(plain, 256 + 65536) + 4 * 512 * 2   # never inside the counter area
+    assert _ao_status(lib, n=100) == 1
+    assert _ao_status(lib, group=32) == 2
+    assert _ao_status(lib, perm=None, ws=1 << 20, ws_bytes=need) == 1
+    assert _ao_status(lib, perm=(1 << 16) + 4, ws=1 << 20, ws_bytes=need) == 1   # 16-byte rule
+    # the plain GEMM's workspace is not enough: the gathered A lives after it
+    assert _ao_status(lib, ws=1 << 20, ws_bytes=plain) == 3
+    assert _ao_status(lib, ws=(1 << 20) + 16, ws_bytes=need) == 3
+    assert _ao_status(lib, m=0, A=None, B=None, s=None, C=None, perm=None) == 0
+    assert wo.wo_act_order_workspace_size(0, 256, 512, 64, 4) == 0
+    assert wo.wo_act_order_workspace_size(4, 100, 512, 64, 4) == 0
+
+
+def test_pack_act_order_rejects_bad_arguments(lib):
+    assert lib.wo_pack_act_order(4096, 1 << 20, None, 256, 512, 4, None) == 1
+    assert lib.wo_pack_act_order(4096, 1 << 20, (1 << 16) + 2, 256, 512, 4, None) == 1
+    assert lib.wo_pack_act_order(4096, 1 << 20, 1 << 16, 100, 512, 4, None) == 1
+    assert lib.wo_pack_act_order(1 << 20, (1 << 20) + 4096, 1 << 16, 256, 512, 8, None) == 1

@@ -20,8 +20,11 @@ __all__ = [
     "WO_F16", "WO_BF16", "WoError", "load_library", "library_path",
     "wo_status_string", "wo_packed_bytes", "wo_pack", "wo_unpack", "wo_workspace_size",
     "wo_gemm", "wo_moe_workspace_size", "wo_moe_ffn", "wo_check_workspace",
-    "wo_gemm_tc_noalloc", "wo_selftest_wait_timeout",
-    "pack", "unpack", "pack_experts", "gemm", "moe_ffn", "Workspace",
+    "wo_gemm_tc_noalloc", "wo_selftest_wait_timeout", "wo_embed",
+    "wo_act_order_perm", "wo_pack_act_order", "wo_act_order_workspace_size",
+    "wo_gemm_act_order",
+    "pack", "unpack", "pack_experts", "gemm", "embed", "moe_ffn", "Workspace",
+    "act_order_perm", "pack_act_order", "gemm_act_order",
 ]
 
 WO_F16 = 0
@@ -80,6 +83,14 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.wo_moe_ffn.restype = I
         lib.wo_embed.argtypes = [P, I, P, P, P, P, I, I, I, I, I, P]
         lib.wo_embed.restype = I
+        lib.wo_act_order_perm.argtypes = [P, I, I, P]
+        lib.wo_act_order_perm.restype = I
+        lib.wo_pack_act_order.argtypes = [P, P, P, I, I, I, P]
+        lib.wo_pack_act_order.restype = I
+        lib.wo_act_order_workspace_size.argtypes = [I, I, I, I, I]
+        lib.wo_act_order_workspace_size.restype = S
+        lib.wo_gemm_act_order.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+        lib.wo_gemm_act_order.restype = I
         lib.wo_check_workspace.argtypes = [P, S, P]
         lib.wo_check_workspace.restype = I
         lib.wo_gemm_tc_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
@@ -167,6 +178,50 @@ def wo_embed(ids, T: int, B_packed, scales, zeros, out, vocab: int, hidden: int,
     _raise(load_library().wo_embed(_ptr(ids), T, _ptr(B_packed), _ptr(scales), _ptr(zeros),
                                    _ptr(out), vocab, hidden, group_size, bits, act_dtype,
                                    _stream_ptr(stream)), "wo_embed")
+
+
+def _host_i32(a, k: int, what: str):
+    """A host int32 array of k entries (CPU tensor or numpy) and its address."""
+    import numpy as np
+    if hasattr(a, "device") and hasattr(a, "data_ptr"):
+        if a.device.type != "cpu":
+            raise ValueError(f"{what} must be in host memory")
+        a = a.numpy()
+    arr = np.ascontiguousarray(a, dtype=np.int32).reshape(-1)
+    if arr.size != k:
+        raise ValueError(f"{what} must have k = {k} entries, got {arr.size}")
+    return arr, arr.ctypes.data
+
+
+def wo_act_order_perm(g_idx, k: int, group_size: int, perm) -> None:
+    """HOST arrays: g_idx int32 [k] in, perm int32 [k] out (numpy, filled in place)."""
+    import numpy as np
+    gi, gp = _host_i32(g_idx, k, "g_idx")  # gi keeps the array alive across the call
+    if not (isinstance(perm, np.ndarray) and perm.dtype == np.int32 and perm.size == k
+            and perm.flags.c_contiguous):
+        raise ValueError("perm must be a contiguous numpy int32 array of k entries")
+    _raise(load_library().wo_act_order_perm(gp, k, group_size, perm.ctypes.data),
+           "wo_act_order_perm")
+
+
+def wo_pack_act_order(B_rowmajor, B_packed, perm, n: int, k: int, bits: int,
+                      stream=None) -> None:
+    _raise(load_library().wo_pack_act_order(_ptr(B_rowmajor), _ptr(B_packed), _ptr(perm), n, k,
+                                            bits, _stream_ptr(stream)), "wo_pack_act_order")
+
+
+def wo_act_order_workspace_size(m: int, n: int, k: int, group_size: int, bits: int) -> int:
+    return int(load_library().wo_act_order_workspace_size(m, n, k, group_size, bits))
+
+
+def wo_gemm_act_order(A, B_packed, perm, scales, zeros, bias, C, m: int, n: int, k: int,
+                      group_size: int, bits: int, act_dtype: int, workspace, workspace_bytes: int,
+                      stream=None) -> None:
+    _raise(load_library().wo_gemm_act_order(_ptr(A), _ptr(B_packed), _ptr(perm), _ptr(scales),
+                                            _ptr(zeros), _ptr(bias), _ptr(C), m, n, k,
+                                            group_size, bits, act_dtype, _ptr(workspace),
+                                            workspace_bytes, _stream_ptr(stream)),
+           "wo_gemm_act_order")
 
 
 def wo_moe_workspace_size(T: int, hidden: int, inter: int, experts: int, topk: int) -> int:
@@ -288,6 +343,48 @@ def gemm(A, B_packed, scales, n: int, k: int, bits: int, group_size: int = -1, z
         ws, ws_bytes = workspace, workspace.numel()
     wo_gemm(A, B_packed, scales, zeros, bias, out, m, n, k, group_size, bits, act, ws, ws_bytes,
             stream)
+    return out
+
+
+def act_order_perm(g_idx, k: int, group_size: int):
+    """The channel order that sorts a GPTQ act-order group index (host work):
+    returns an int32 CPU tensor perm [k], perm[j] = the j-th channel in order
+    of (g_idx[c], c).  Copy it to the device for pack_act_order and
+    gemm_act_order."""
+    import numpy as np
+    import torch
+    perm = np.empty(k, dtype=np.int32)
+    wo_act_order_perm(g_idx, k, group_size, perm)
+    return torch.from_numpy(perm)
+
+
+def pack_act_order(B_rowmajor, perm, n: int, k: int, bits: int, stream=None):
+    """wo_pack of the codes with input channels in the order perm (a device
+    int32 [k] tensor); waits for the packing, as pack() does."""
+    import torch
+    out = torch.empty(wo_packed_bytes(n, k, bits), dtype=torch.uint8, device=B_rowmajor.device)
+    wo_pack_act_order(B_rowmajor, out, perm, n, k, bits, stream)
+    _sync(stream)
+    return out
+
+
+def gemm_act_order(A, B_packed, perm, scales, n: int, k: int, bits: int, group_size: int,
+                   zeros=None, bias=None, out=None, workspace=None, stream=None):
+    """The GPTQ act-order GEMM through wo_gemm_act_order: A [m, k] in the
+    checkpoint's channel order, B_packed from pack_act_order with the same
+    device perm; returns C [m, n]."""
+    import torch
+    m = A.shape[0]
+    act = _dtype_code(A)
+    if out is None:
+        out = torch.empty((m, n), dtype=A.dtype, device=A.device)
+    need = wo_act_order_workspace_size(m, n, k, group_size, bits)
+    if workspace is None:
+        ws, ws_bytes = _workspace_for(A.device, need)
+    else:
+        ws, ws_bytes = workspace, workspace.numel()
+    wo_gemm_act_order(A, B_packed, perm, scales, zeros, bias, out, m, n, k, group_size, bits, act,
+                      ws, ws_bytes, stream)
     return out
 
 

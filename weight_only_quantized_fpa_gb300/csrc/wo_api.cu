@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <vector>
 
 #include "wo_internal.h"
 
@@ -103,7 +104,8 @@ static wo_status pack_common(const uint8_t* src, uint8_t* dst, int n, int k, int
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
     if (s0 < d0 + bytes && d0 < s0 + bytes)
         return WO_ERR_INVALID_ARG;  // overlapping buffers
-    return cuda_status(launch_pack(src, dst, n, k, bits, unpack, static_cast<cudaStream_t>(stream)));
+    return cuda_status(
+        launch_pack(src, dst, n, k, bits, unpack, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 wo_status wo_pack(const uint8_t* B_rowmajor, uint8_t* B_packed, int n, int k, int bits,
@@ -130,10 +132,15 @@ size_t wo_workspace_size(int m, int n, int k, int group_size, int bits)
     return stream_workspace_bytes();
 }
 
-wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, const void* zeros,
-                  const void* bias, void* C, int m, int n, int k, int group_size, int bits,
-                  wo_dtype act_dtype, void* workspace, size_t workspace_bytes, void* stream)
+// Argument checks of wo_gemm, with `ws_need` the workspace the GEMM itself
+// needs; fills `a` on success.  m == 0 or n == 0 returns WO_OK with a.m or
+// a.n zero (nothing to launch).
+static wo_status gemm_prepare(const void* A, const uint8_t* B_packed, const void* scales,
+                              const void* zeros, const void* bias, void* C, int m, int n, int k,
+                              int group_size, int bits, wo_dtype act_dtype, void* workspace,
+                              size_t workspace_bytes, GemmArgs& a)
 {
+    a = GemmArgs{};
     wo_status st = check_gemm_shape(m, n, k, group_size, bits);
     if (st != WO_OK)
         return st;
@@ -151,8 +158,6 @@ wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, co
     const size_t need = wo_workspace_size(m, n, k, group_size, bits);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return WO_ERR_WORKSPACE;
-
-    GemmArgs a{};
     a.A = A;
     a.B = B_packed;
     a.scales = scales;
@@ -167,10 +172,111 @@ wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, co
     a.act = act_dtype;
     a.ws = workspace;
     a.ws_bytes = workspace_bytes;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_tc(m, n, k, group_size, bits))
-        return cuda_status(launch_tc(a, plan_tc(m, n, k, bits, act_dtype), s));
+    return WO_OK;
+}
+
+static wo_status gemm_launch(const GemmArgs& a, cudaStream_t s)
+{
+    if (use_tc(a.m, a.n, a.k, a.group, a.bits))
+        return cuda_status(launch_tc(a, plan_tc(a.m, a.n, a.k, a.bits, a.act), s));
     return cuda_status(launch_stream_gemm(a, s));
+}
+
+wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, const void* zeros,
+                  const void* bias, void* C, int m, int n, int k, int group_size, int bits,
+                  wo_dtype act_dtype, void* workspace, size_t workspace_bytes, void* stream)
+{
+    GemmArgs a;
+    const wo_status st = gemm_prepare(A, B_packed, scales, zeros, bias, C, m, n, k, group_size,
+                                      bits, act_dtype, workspace, workspace_bytes, a);
+    if (st != WO_OK || a.m == 0 || a.n == 0)
+        return st;
+    return gemm_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+// ---- GPTQ act-order ---------------------------------------------------------
+
+wo_status wo_act_order_perm(const int32_t* g_idx, int k, int group_size, int32_t* perm)
+{
+    if (!g_idx || !perm || k <= 0)
+        return WO_ERR_INVALID_ARG;
+    const int g = norm_group(group_size, k);
+    if (g <= 0 || k % g != 0)
+        return WO_ERR_INVALID_ARG;
+    const int G = k / g;
+    std::vector<int> count(G, 0);
+    for (int c = 0; c < k; ++c) {
+        if (g_idx[c] < 0 || g_idx[c] >= G)
+            return WO_ERR_INVALID_ARG;
+        ++count[g_idx[c]];
+    }
+    for (int b = 0; b < G; ++b)
+        if (count[b] != g)
+            return WO_ERR_UNSUPPORTED;  // groups of unequal size
+    // stable counting sort: group b's channels fill positions [b*g, (b+1)*g)
+    std::vector<int> next(G);
+    for (int b = 0; b < G; ++b)
+        next[b] = b * g;
+    for (int c = 0; c < k; ++c)
+        perm[next[g_idx[c]]++] = c;
+    return WO_OK;
+}
+
+wo_status wo_pack_act_order(const uint8_t* B_rowmajor, uint8_t* B_packed, const int32_t* perm,
+                            int n, int k, int bits, void* stream)
+{
+    const size_t bytes = wo_packed_bytes(n, k, bits);
+    if (bytes == 0 || !B_rowmajor || !B_packed || !perm || !aligned(B_rowmajor, 16) ||
+        !aligned(B_packed, 16) || !aligned(perm, 4))
+        return WO_ERR_INVALID_ARG;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(B_rowmajor);
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(B_packed);
+    if (s0 < d0 + bytes && d0 < s0 + bytes)
+        return WO_ERR_INVALID_ARG;  // overlapping buffers
+    return cuda_status(launch_pack(B_rowmajor, B_packed, n, k, bits, false, perm,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+// Offset of the gathered activations in an act-order workspace: after the
+// GEMM's own workspace, and never inside the header and counter area that
+// every call shares (the small-m GEMM itself needs only the header).
+static size_t act_order_a_offset(int m, int n, int k, int group_size, int bits)
+{
+    const size_t g = wo_workspace_size(m, n, k, group_size, bits);
+    return align_up(g > kWsScratch ? g : kWsScratch, 256);
+}
+
+size_t wo_act_order_workspace_size(int m, int n, int k, int group_size, int bits)
+{
+    if (check_gemm_shape(m, n, k, group_size, bits) != WO_OK || m == 0 || n == 0)
+        return 0;
+    return act_order_a_offset(m, n, k, group_size, bits) + align_up((size_t)m * k * 2, 256);
+}
+
+wo_status wo_gemm_act_order(const void* A, const uint8_t* B_packed, const int32_t* perm,
+                            const void* scales, const void* zeros, const void* bias, void* C,
+                            int m, int n, int k, int group_size, int bits, wo_dtype act_dtype,
+                            void* workspace, size_t workspace_bytes, void* stream)
+{
+    GemmArgs a;
+    wo_status st = gemm_prepare(A, B_packed, scales, zeros, bias, C, m, n, k, group_size, bits,
+                                act_dtype, workspace, workspace_bytes, a);
+    if (st != WO_OK || a.m == 0 || a.n == 0)
+        return st;
+    if (!perm || !aligned(perm, 16))
+        return WO_ERR_INVALID_ARG;
+    const size_t need = wo_act_order_workspace_size(m, n, k, group_size, bits);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return WO_ERR_WORKSPACE;
+    const size_t off = act_order_a_offset(m, n, k, group_size, bits);
+    void* Ap = static_cast<char*>(workspace) + off;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = cuda_status(launch_gather_cols(A, perm, Ap, m, k, s));
+    if (st != WO_OK)
+        return st;
+    a.A = Ap;
+    a.ws_bytes = off;
+    return gemm_launch(a, s);
 }
 
 wo_status wo_embed(const int32_t* ids, int T, const uint8_t* B_packed, const void* scales,

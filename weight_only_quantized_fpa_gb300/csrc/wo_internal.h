@@ -27,8 +27,12 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int num_sms();  // SM count of the current device (152 when none is visible)
 
 // ---- pack -----------------------------------------------------------------
+// perm (pack only, optional): packed column j takes row-major column perm[j]
 cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,
-                        cudaStream_t s);
+                        const int32_t* perm, cudaStream_t s);
+// A' = A[:, perm] (act-order GEMM): rows of k 16-bit values, perm [k]
+cudaError_t launch_gather_cols(const void* A, const int32_t* perm, void* Ap, int m, int k,
+                               cudaStream_t s);
 // rows ids[0..T) of a packed [vocab, hidden] table, dequantised (wo_embed)
 cudaError_t launch_embed(const int32_t* ids, int T, const uint8_t* B, const void* scales,
                          const void* zeros, void* out, int vocab, int hidden, int group, int bits,

@@ -36,9 +36,12 @@ __device__ __forceinline__ void u4_coord(int s, int p, int g, int t, int& row, i
     kk = 16 * s + 2 * t + 8 * (R >> 1) + h;
 }
 
+// perm (optional, [k]): packed column j takes row-major column perm[j] (a GPTQ
+// act-order checkpoint's channels, sorted by group).  An entry outside
+// [0, k) reads code 0, so a bad permutation cannot read out of bounds.
 template <int BITS>
 __global__ void pack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int n,
-                            int k, long long chunks)
+                            int k, long long chunks, const int32_t* __restrict__ perm)
 {
     constexpr int KT = Geom<BITS>::KT;
     const int ktiles = k / KT;
@@ -56,7 +59,11 @@ __global__ void pack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict
                 for (int j = 0; j < 4; ++j) {
                     int row, kk;
                     u8_coord(4 * wi + j, g, t, row, kk);
-                    const uint32_t v = src[(size_t)(nb * 16 + row) * k + kt * KT + kk];
+                    int kg = kt * KT + kk;
+                    if (perm)
+                        kg = perm[kg];
+                    const uint32_t v =
+                        (unsigned)kg < (unsigned)k ? src[(size_t)(nb * 16 + row) * k + kg] : 0u;
                     w |= v << (8 * j);
                 }
                 words[wi] = w;
@@ -68,8 +75,11 @@ __global__ void pack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict
                 for (int p = 0; p < 8; ++p) {
                     int row, kk;
                     u4_coord(s, p, g, t, row, kk);
-                    const int kg = kt * KT + kk;
-                    const uint8_t byte = src[(size_t)(nb * 16 + row) * kb + kg / 2];
+                    int kg = kt * KT + kk;
+                    if (perm)
+                        kg = perm[kg];
+                    const uint8_t byte =
+                        (unsigned)kg < (unsigned)k ? src[(size_t)(nb * 16 + row) * kb + kg / 2] : 0;
                     const uint32_t q = (kg & 1) ? (byte >> 4) : (byte & 0x0F);
                     w |= q << (4 * p);
                 }
@@ -254,7 +264,7 @@ cudaError_t launch_embed(const int32_t* ids, int T, const uint8_t* B, const void
 }
 
 cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,
-                        cudaStream_t s)
+                        const int32_t* perm, cudaStream_t s)
 {
     const long long bytes = bits == 8 ? (long long)n * k : (long long)n * k / 2;
     const long long chunks = bytes / 16;
@@ -269,12 +279,12 @@ cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits
         if (unpack)
             unpack_kernel<8><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
         else
-            pack_kernel<8><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
+            pack_kernel<8><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks, perm);
     } else {
         if (unpack)
             unpack_kernel<4><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
         else
-            pack_kernel<4><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks);
+            pack_kernel<4><<<(unsigned)blocks, threads, 0, s>>>(src, dst, n, k, chunks, perm);
     }
     return cudaGetLastError();
 }

@@ -98,6 +98,7 @@ class GemmCase:
     scales: np.ndarray       # uint16 [n] or [n, k/group]
     zeros: np.ndarray | None
     bias: np.ndarray | None
+    g_idx: np.ndarray | None = None  # int32 [k]: act-order group of each input channel
 
     @property
     def weight_bytes(self) -> int:
@@ -109,7 +110,8 @@ class GemmCase:
 
 def make_gemm_case(config: int, case: int, m: int, n: int, k: int, *, bits: int,
                    group_size: int, act_dtype: int, scale_lo: float, scale_hi: float,
-                   with_zeros: bool, with_bias: bool, name: str = "") -> GemmCase:
+                   with_zeros: bool, with_bias: bool, name: str = "",
+                   act_order: bool = False) -> GemmCase:
     A = normal_bits(rng_for(config, case, T_A), (m, k), act_dtype)
     if bits == 8:
         B = code_bytes(rng_for(config, case, T_CODES), (n, k))
@@ -123,8 +125,10 @@ def make_gemm_case(config: int, case: int, m: int, n: int, k: int, *, bits: int,
              if with_zeros else None)
     bias = (normal_bits(rng_for(config, case, T_BIAS), (n,), act_dtype, 0.1)
             if with_bias else None)
+    g_idx = (act_order_g_idx(rng_for(config, case, T_GIDX), k, k if per_channel else group_size)
+             if act_order else None)
     return GemmCase(name or f"cfg{config}.case{case}", m, n, k, bits, group_size,
-                    act_dtype, A, B, scales, zeros, bias)
+                    act_dtype, A, B, scales, zeros, bias, g_idx)
 
 
 # -- the five workloads ------------------------------------------------------
@@ -148,7 +152,12 @@ W4_G64 = dict(config=4, shapes=[(m, n, k) for m in (1, 512) for (n, k) in W4_G64
               bits=4, group_size=64, act_dtype=BF16, scale_lo=0.005, scale_hi=0.02,
               with_zeros=True, with_bias=False)
 
-GEMM_WORKLOADS = {1: W4_TINY, 2: W8_DECODE, 3: W8_LARGE, 4: W4_G64}
+# GPTQ act-order (g_idx), group 128, on the shapes of the group-64 workload
+W4_ACT_ORDER = dict(config=6, shapes=[(m, n, k) for m in (1, 512) for (n, k) in W4_G64_NK],
+                    bits=4, group_size=128, act_dtype=BF16, scale_lo=0.005, scale_hi=0.02,
+                    with_zeros=True, with_bias=False, act_order=True)
+
+GEMM_WORKLOADS = {1: W4_TINY, 2: W8_DECODE, 3: W8_LARGE, 4: W4_G64, 6: W4_ACT_ORDER}
 
 
 def workload_case(config: int, case: int) -> GemmCase:
@@ -158,7 +167,8 @@ def workload_case(config: int, case: int) -> GemmCase:
     return make_gemm_case(config, case, m, n, k, bits=w["bits"], group_size=w["group_size"],
                           act_dtype=w["act_dtype"], scale_lo=w["scale_lo"],
                           scale_hi=w["scale_hi"], with_zeros=w["with_zeros"],
-                          with_bias=w["with_bias"], name=f"cfg{config}:m{m}n{n}k{k}")
+                          with_bias=w["with_bias"], name=f"cfg{config}:m{m}n{n}k{k}",
+                          act_order=w.get("act_order", False))
 
 
 @dataclass

@@ -62,6 +62,9 @@ WORKLOADS = {
                               "(13312,2048),(131072,2048),(2048,13312)}); g_idx = a random "
                               "channel order cut into groups of 128; bytes = codes, scales, "
                               "zeros"),
+    "w4_g128": dict(config=7, unit="GB/s", dtype="bf16",
+                    desc="W4A16 group 128, asymmetric, bf16, channels in order: the w4_act_order "
+                         "shapes and value distributions without the act-order group index"),
     "w4_tiny": dict(config=1, unit="GB/s", dtype="bf16",
                     desc="W4A16 tiny: m=1, N=256, K=512, group 64, bf16"),
     "moe": dict(config=5, unit="GB/s", dtype="bf16",
@@ -157,15 +160,16 @@ def kernel_source_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_from_profile(kernel: str, src_hash: str):
+def traffic_from_profile(kernel: str, src_hash: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel source; else None."""
+    was taken on the current kernel source and on this bench workload; else
+    None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(kernel)
-        if e and e.get("source_hash") == src_hash:
+        if e and e.get("source_hash") == src_hash and e.get("bench_workload") == workload:
             return e
     except (OSError, ValueError):
         pass
@@ -394,7 +398,7 @@ def embed_traffic():
         sh = kernel_source_hash(["wo_pack.cu", "wo_common.cuh"])
     except OSError:
         return None
-    tr = traffic_from_profile("embed_kernel", sh)
+    tr = traffic_from_profile("embed_kernel", sh, "embed")
     return tr["dram_bytes_per_launch"] if tr else None
 
 
@@ -670,7 +674,7 @@ def run_moe(args, ws, rank, local):
         sh = kernel_source_hash(["wo_moe.cu", "wo_gemm_tc.cu", "wo_common.cuh", "wo_sm100.cuh"])
     except OSError:
         sh = None
-    tr = traffic_from_profile("moe_ffn", sh) if sh else None
+    tr = traffic_from_profile("moe_ffn", sh, "moe") if sh else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -922,7 +926,7 @@ def run_ours(args, ws, rank, local):
         sh = kernel_source_hash(src)
     except OSError:
         sh = None
-    tr = traffic_from_profile(kname, sh) if sh else None
+    tr = traffic_from_profile(kname, sh, args.workload) if sh else None
     roof["traffic"] = tr["dram_bytes_per_launch"] if tr else None
     if w["unit"] == "GB/s":
         roof["algorithmic_bytes_per_launch"] = bytes_per_step / ncase

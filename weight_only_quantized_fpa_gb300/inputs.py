@@ -157,7 +157,10 @@ W4_ACT_ORDER = dict(config=6, shapes=[(m, n, k) for m in (1, 512) for (n, k) in 
                     bits=4, group_size=128, act_dtype=BF16, scale_lo=0.005, scale_hi=0.02,
                     with_zeros=True, with_bias=False, act_order=True)
 
-GEMM_WORKLOADS = {1: W4_TINY, 2: W8_DECODE, 3: W8_LARGE, 4: W4_G64, 6: W4_ACT_ORDER}
+# the same without act-order (channels in order, group 128)
+W4_G128 = dict(W4_ACT_ORDER, config=7, act_order=False)
+
+GEMM_WORKLOADS = {1: W4_TINY, 2: W8_DECODE, 3: W8_LARGE, 4: W4_G64, 6: W4_ACT_ORDER, 7: W4_G128}
 
 
 def workload_case(config: int, case: int) -> GemmCase:

@@ -282,13 +282,18 @@ def cpu_baseline(cases, unit, budget_s=8.0):
 
 # ------------------------------------------------------------ distributed --
 
-def dist_setup():
+def dist_setup(backend: str | None = None):
+    """Rank, world size and local rank from the torchrun environment; one
+    process group for the barriers and the max over ranks (NCCL on GPUs,
+    gloo where there are none, e.g. the CPU tests of this path)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl"
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
     return ws, rank, local
 
@@ -304,7 +309,8 @@ def max_over_ranks(ws, x: float) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

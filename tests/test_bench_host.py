@@ -1,0 +1,51 @@
+"""CPU tests of bench.py's host logic: launch counting, the DRAM-traffic
+lookup, and the workloads' case lists."""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from weight_only_quantized_fpa_gb300 import inputs  # noqa: E402
+
+
+def test_launch_count_per_call():
+    c = inputs.make_gemm_case(9, 0, 1, 64, 128, bits=4, group_size=64, act_dtype=inputs.BF16,
+                              scale_lo=0.01, scale_hi=0.02, with_zeros=True, with_bias=False)
+    assert bench.case_launches(c) == 1                       # streaming kernel
+    c.m = 512
+    assert bench.case_launches(c) == 2                       # fp16 copy of A + tensor cores
+    c.act_dtype = inputs.F16
+    assert bench.case_launches(c) == 1
+    c.g_idx = np.zeros(c.k, dtype=np.int32)
+    assert bench.case_launches(c) == 2                       # + the act-order gather
+    c.m = 1
+    assert bench.case_launches(c) == 2
+
+
+def test_traffic_is_reported_only_for_its_workload_and_source():
+    src = ["wo_stream.cu", "wo_common.cuh", "wo_sm100.cuh"]
+    h = bench.kernel_source_hash(src)
+    e = bench.traffic_from_profile("stream_kernel", h, "w8_decode")
+    if e is None:
+        pytest.skip("stream_kernel changed since its DRAM traffic was captured")
+    assert e["bench_workload"] == "w8_decode"
+    assert bench.traffic_from_profile("stream_kernel", h, "w4_g64") is None
+    assert bench.traffic_from_profile("stream_kernel", "0" * 16, "w8_decode") is None
+
+
+@pytest.mark.parametrize("name", ["w4_act_order", "w4_g128"])
+def test_group128_workloads_share_shapes(name):
+    cases = bench.workload_cases(name)
+    assert [(c.m, c.n, c.k) for c in cases] == inputs.W4_G64["shapes"]
+    for c in cases[:3]:
+        assert c.group_size == 128 and c.bits == 4
+        if name == "w4_act_order":
+            # every group holds exactly 128 channels
+            assert np.array_equal(np.bincount(c.g_idx), np.full(c.k // 128, 128))
+        else:
+            assert c.g_idx is None

@@ -26,7 +26,7 @@ constexpr int kGatherThreads = 256;
 // Launched with programmatic stream serialisation: the indices are read
 // before the wait on the previous grid (they are load-time data), A after it.
 __global__ void __launch_bounds__(kGatherThreads)
-    gather_cols_kernel(const uint16_t* __restrict__ A, const int32_t* __restrict__ perm,
+    act_order_gather_kernel(const uint16_t* __restrict__ A, const int32_t* __restrict__ perm,
                        uint16_t* __restrict__ Ap, int m, int k)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -68,7 +68,7 @@ constexpr int kGatherSmemMaxK = 49152;
 __host__ __device__ constexpr size_t gather_smem_bytes(int k) { return (size_t)(2 * k + 8) * 2; }
 
 __global__ void __launch_bounds__(kGatherSmemThreads)
-    gather_rows_kernel(const uint16_t* __restrict__ A, const int32_t* __restrict__ perm,
+    act_order_gather_smem_kernel(const uint16_t* __restrict__ A, const int32_t* __restrict__ perm,
                        uint16_t* __restrict__ Ap, int m, int k)
 {
     extern __shared__ __align__(16) uint16_t gsm[];
@@ -129,7 +129,7 @@ cudaError_t launch_gather_cols(const void* A, const int32_t* perm, void* Ap, int
         if (e != cudaSuccess)
             return e;
         if (dev < 0 || dev >= 64 || smem_set[dev].load() < (int)smem) {
-            if ((e = cudaFuncSetAttribute(gather_rows_kernel,
+            if ((e = cudaFuncSetAttribute(act_order_gather_smem_kernel,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem)) != cudaSuccess)
                 return e;
@@ -146,7 +146,7 @@ cudaError_t launch_gather_cols(const void* A, const int32_t* perm, void* Ap, int
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, gather_rows_kernel, static_cast<const uint16_t*>(A), perm,
+        return cudaLaunchKernelEx(&cfg, act_order_gather_smem_kernel, static_cast<const uint16_t*>(A), perm,
                                   static_cast<uint16_t*>(Ap), m, k);
     }
     const int nch = k / 8;
@@ -166,7 +166,7 @@ cudaError_t launch_gather_cols(const void* A, const int32_t* perm, void* Ap, int
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gather_cols_kernel, static_cast<const uint16_t*>(A), perm,
+    return cudaLaunchKernelEx(&cfg, act_order_gather_kernel, static_cast<const uint16_t*>(A), perm,
                               static_cast<uint16_t*>(Ap), m, k);
 }
 

@@ -204,17 +204,23 @@ wo_status wo_act_order_perm(const int32_t* g_idx, int k, int group_size, int32_t
     if (g <= 0 || k % g != 0)
         return WO_ERR_INVALID_ARG;
     const int G = k / g;
-    std::vector<int> count(G, 0);
+    // the group counters are the only host memory used; no exception may
+    // leave a C entry point, so an allocation failure becomes a status
+    std::vector<int> next;
+    try {
+        next.assign(G, 0);
+    } catch (...) {
+        return WO_ERR_INVALID_ARG;
+    }
     for (int c = 0; c < k; ++c) {
         if (g_idx[c] < 0 || g_idx[c] >= G)
             return WO_ERR_INVALID_ARG;
-        ++count[g_idx[c]];
+        ++next[g_idx[c]];
     }
     for (int b = 0; b < G; ++b)
-        if (count[b] != g)
+        if (next[b] != g)
             return WO_ERR_UNSUPPORTED;  // groups of unequal size
     // stable counting sort: group b's channels fill positions [b*g, (b+1)*g)
-    std::vector<int> next(G);
     for (int b = 0; b < G; ++b)
         next[b] = b * g;
     for (int c = 0; c < k; ++c)

@@ -138,10 +138,10 @@ def test_w8_per_channel_any_order_matches_plain_oracle(wo):
     assert_within_tolerance(from_device_bits(C), c.act_dtype, ref, "w8 act-order")
 
 
-@pytest.mark.parametrize("case", [2, 7])
+@pytest.mark.parametrize("case", [2, 3, 7, 8])
 def test_act_order_workload_sampled(wo, case):
-    # the bench workload's full sizes (13312 x 2048, group 128) in its launch
-    # configuration, on sampled rows
+    # the bench workload's full sizes (13312 and 131072 x 2048, group 128) in
+    # its launch configuration, on sampled rows
     c = inputs.workload_case(6, case)
     ac = ActOrderCase(wo, c)
     C = ac.run(wo)
@@ -197,3 +197,16 @@ def test_act_order_workspace_shared_with_plain_gemm(wo, m):
                          -1, 8)
     assert_within_tolerance(from_device_bits(C2), sp.act_dtype, ref_sp, "k split after")
     assert wo.wo_check_workspace(ws, need) == 0
+
+
+@pytest.mark.parametrize("case", [3, 4, 8, 9])
+def test_group128_in_order_workload_sampled(wo, case):
+    # the in-order group-128 workload the act-order one is compared with, at
+    # full size, through wo_gemm
+    from helpers import DeviceCase
+    c = inputs.workload_case(7, case)
+    dc = DeviceCase(c)
+    C = dc.run()
+    torch.cuda.synchronize()
+    rows = sample_rows(c.m, 8)
+    assert_within_tolerance(from_device_bits(C)[rows], c.act_dtype, dc.oracle_rows(rows), c.name)

@@ -18,6 +18,26 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 
+// Activation loads after griddepcontrol.wait go through L2 only (.cg): A may
+// have been written by the previous grid while this one was already
+// resident, so no read of it may be served by a non-coherent or L1 copy.
+__device__ __forceinline__ uint16_t ld_cg_u16(const uint16_t* p)
+{
+    uint16_t v;
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
 // A'[r, j] = A[r, perm[j]].
 //
 // Few rows (the weight-streaming sizes): a thread owns 8 consecutive output columns
@@ -26,8 +46,8 @@ constexpr int kGatherThreads = 256;
 // Launched with programmatic stream serialisation: the indices are read
 // before the wait on the previous grid (they are load-time data), A after it.
 __global__ void __launch_bounds__(kGatherThreads)
-    act_order_gather_kernel(const uint16_t* __restrict__ A, const int32_t* __restrict__ perm,
-                       uint16_t* __restrict__ Ap, int m, int k)
+    act_order_gather_kernel(const uint16_t* A, const int32_t* __restrict__ perm,
+                            uint16_t* __restrict__ Ap, int m, int k)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int nch = k >> 3;
@@ -47,9 +67,9 @@ __global__ void __launch_bounds__(kGatherThreads)
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = (unsigned)idx[2 * i] < (unsigned)k ? __ldg(a + idx[2 * i]) : 0u;
+            const uint32_t lo = (unsigned)idx[2 * i] < (unsigned)k ? ld_cg_u16(a + idx[2 * i]) : 0u;
             const uint32_t hi =
-                (unsigned)idx[2 * i + 1] < (unsigned)k ? __ldg(a + idx[2 * i + 1]) : 0u;
+                (unsigned)idx[2 * i + 1] < (unsigned)k ? ld_cg_u16(a + idx[2 * i + 1]) : 0u;
             w[i] = lo | (hi << 16);
         }
         *reinterpret_cast<uint4*>(Ap + (size_t)r * k + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -68,8 +88,8 @@ constexpr int kGatherSmemMaxK = 49152;
 __host__ __device__ constexpr size_t gather_smem_bytes(int k) { return (size_t)(2 * k + 8) * 2; }
 
 __global__ void __launch_bounds__(kGatherSmemThreads)
-    act_order_gather_smem_kernel(const uint16_t* __restrict__ A, const int32_t* __restrict__ perm,
-                       uint16_t* __restrict__ Ap, int m, int k)
+    act_order_gather_smem_kernel(const uint16_t* A, const int32_t* __restrict__ perm,
+                                 uint16_t* __restrict__ Ap, int m, int k)
 {
     extern __shared__ __align__(16) uint16_t gsm[];
     uint16_t* pos = gsm;     // [k]: source column of each output column
@@ -94,7 +114,7 @@ __global__ void __launch_bounds__(kGatherSmemThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (c0 + u * kGatherSmemThreads < nch)
-                    v[u] = __ldg(src + c0 + u * kGatherSmemThreads);
+                    v[u] = ld_cg_v4(src + c0 + u * kGatherSmemThreads);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (c0 + u * kGatherSmemThreads < nch)

@@ -114,6 +114,14 @@ def run_profile_case(args):
     A, s = up16(c.A), up16(c.scales)
     z = None if c.zeros is None else up16(c.zeros)
     b = None if c.bias is None else up16(c.bias)
+    if c.g_idx is not None:  # act-order: group-sorted pack, gather per call
+        perm = wo.act_order_perm(c.g_idx, c.k, c.group_size).cuda()
+        B = wo.pack_act_order(torch.from_numpy(c.B).cuda(), perm, c.n, c.k, c.bits)
+        for _ in range(args.steps):
+            wo.gemm_act_order(A, B, perm, s, c.n, c.k, c.bits, c.group_size, zeros=z, bias=b)
+        torch.cuda.synchronize()
+        print(f"profiled {c.name}: {args.steps} calls", file=sys.stderr)
+        return 0
     B = wo.pack(torch.from_numpy(c.B).cuda(), c.n, c.k, c.bits)
     for _ in range(args.steps):
         wo.gemm(A, B, s, c.n, c.k, c.bits, group_size=c.group_size, zeros=z, bias=b)

@@ -249,3 +249,23 @@ def test_pack_act_order_rejects_bad_arguments(lib):
     assert lib.wo_pack_act_order(4096, 1 << 20, (1 << 16) + 2, 256, 512, 4, None) == 1
     assert lib.wo_pack_act_order(4096, 1 << 20, 1 << 16, 100, 512, 4, None) == 1
     assert lib.wo_pack_act_order(1 << 20, (1 << 20) + 4096, 1 << 16, 256, 512, 8, None) == 1
+
+
+def test_act_order_binding_checks_perm_tensor():
+    # the torch-level helpers refuse a permutation the C layer would read
+    # from the wrong place or with the wrong width, before any CUDA call
+    import numpy as np
+    import torch
+    k = 256
+    good = torch.arange(k, dtype=torch.int32)
+    wo._check_perm(good, k, torch.device("cpu"))
+    with pytest.raises(TypeError):
+        wo._check_perm(np.arange(k, dtype=np.int32), k, "cpu")
+    with pytest.raises(ValueError):
+        wo._check_perm(good.to(torch.int64), k, "cpu")
+    with pytest.raises(ValueError):
+        wo._check_perm(good[:128], k, "cpu")
+    with pytest.raises(ValueError):
+        wo._check_perm(torch.arange(2 * k, dtype=torch.int32)[::2], k, "cpu")
+    with pytest.raises(ValueError):   # a perm on another device than the operands
+        wo._check_perm(good, k, torch.device("meta"))

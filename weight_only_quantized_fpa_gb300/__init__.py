@@ -358,10 +358,24 @@ def act_order_perm(g_idx, k: int, group_size: int):
     return torch.from_numpy(perm)
 
 
+def _check_perm(perm, k: int, device) -> None:
+    """perm must be a contiguous int32 tensor of k entries on `device` (the
+    C layer reads it as a device array and cannot check where it lives)."""
+    import torch
+    if not isinstance(perm, torch.Tensor):
+        raise TypeError("perm must be a torch tensor (the output of act_order_perm, "
+                        "moved to the device)")
+    if perm.dtype != torch.int32 or perm.numel() != k or not perm.is_contiguous():
+        raise ValueError(f"perm must be a contiguous int32 tensor of k = {k} entries")
+    if perm.device != torch.device(device):
+        raise ValueError(f"perm is on {perm.device}, the operands on {device}")
+
+
 def pack_act_order(B_rowmajor, perm, n: int, k: int, bits: int, stream=None):
     """wo_pack of the codes with input channels in the order perm (a device
     int32 [k] tensor); waits for the packing, as pack() does."""
     import torch
+    _check_perm(perm, k, B_rowmajor.device)
     out = torch.empty(wo_packed_bytes(n, k, bits), dtype=torch.uint8, device=B_rowmajor.device)
     wo_pack_act_order(B_rowmajor, out, perm, n, k, bits, stream)
     _sync(stream)
@@ -374,6 +388,7 @@ def gemm_act_order(A, B_packed, perm, scales, n: int, k: int, bits: int, group_s
     checkpoint's channel order, B_packed from pack_act_order with the same
     device perm; returns C [m, n]."""
     import torch
+    _check_perm(perm, k, A.device)
     m = A.shape[0]
     act = _dtype_code(A)
     if out is None:

@@ -269,3 +269,18 @@ def test_act_order_binding_checks_perm_tensor():
         wo._check_perm(torch.arange(2 * k, dtype=torch.int32)[::2], k, "cpu")
     with pytest.raises(ValueError):   # a perm on another device than the operands
         wo._check_perm(good, k, torch.device("meta"))
+
+
+@pytest.mark.parametrize("m,n,k,group", [(1, 256, 1024, 64), (16, 4096, 4096, 128),
+                                         (64, 192, 512, 64), (65, 256, 512, 128),
+                                         (200, 320, 6144, -1), (512, 131072, 2048, 128),
+                                         (130, 320, 4096, 128)])
+def test_act_order_workspace_keeps_gathered_A_clear_of_shared_area(lib, m, n, k, group):
+    # layout: the GEMM's own workspace (at least the header and the split-K
+    # counters, 256 + 65536 bytes, shared by every call), then m*k*2 bytes
+    # of gathered activations
+    def up(x):
+        return (x + 255) // 256 * 256
+    need = wo.wo_act_order_workspace_size(m, n, k, group, 4)
+    plain = wo.wo_workspace_size(m, n, k, group, 4)
+    assert need == up(max(plain, 256 + 65536)) + up(m * k * 2)

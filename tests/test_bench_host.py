@@ -70,3 +70,22 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+@pytest.mark.parametrize("n,k", [(2048, 2048), (131072, 2048), (2048, 13312)])
+def test_w4_g64_bytes_are_four_and_a_half_bits_per_weight(n, k):
+    # vLLM-Omni "cpu_int4.py", module docstring: 4-bit codes with a bf16 scale
+    # and offset per group of 64 are 4.5 bits per weight.  The bench's
+    # algorithmic bytes (the roofline's numerator) must count exactly that.
+    c = inputs.make_gemm_case(4, 0, 1, n, k, bits=4, group_size=64, act_dtype=inputs.BF16,
+                              scale_lo=0.005, scale_hi=0.02, with_zeros=True, with_bias=False)
+    assert c.weight_bytes * 8 == 4.5 * n * k
+
+
+def test_w8_per_channel_bytes_are_codes_plus_one_scale_per_channel():
+    # "acext User Guide (v1.7)" 1.3.1: one int8 per weight and a single scale
+    # per output channel
+    n, k = 4608, 3584
+    c = inputs.make_gemm_case(2, 0, 1, n, k, bits=8, group_size=-1, act_dtype=inputs.F16,
+                              scale_lo=0.001, scale_hi=0.01, with_zeros=False, with_bias=True)
+    assert c.weight_bytes == n * k + 2 * n

@@ -65,6 +65,18 @@ WORKLOADS = {
     "w4_g128": dict(config=7, unit="GB/s", dtype="bf16",
                     desc="W4A16 group 128, asymmetric, bf16, channels in order: the w4_act_order "
                          "shapes and value distributions without the act-order group index"),
+    "w8_decode_bf16": dict(config=8, unit="GB/s", dtype="bf16",
+                           desc="A16W8 per-channel decode with bf16 activations, scales and "
+                                "bias: the w8_decode shapes (m in {1,4,16})"),
+    "w4_g64_f16": dict(config=9, unit="GB/s", dtype="f16",
+                       desc="W4A16 group 64 with fp16 activations, scales and zeros: the w4_g64 "
+                            "shapes (m in {1,512})"),
+    "w4_per_channel": dict(config=10, unit="GB/s", dtype="bf16",
+                           desc="4-bit codes with one bf16 scale and zero per output channel: "
+                                "the w4_g64 shapes (m in {1,512})"),
+    "w8_mid": dict(config=11, unit="GB/s", dtype="f16",
+                   desc="A16W8 per-channel, fp16, m in {24,32,48,64} (between decode and the "
+                        "tensor-core sizes) on the w8_decode (N,K)"),
     "w4_tiny": dict(config=1, unit="GB/s", dtype="bf16",
                     desc="W4A16 tiny: m=1, N=256, K=512, group 64, bf16"),
     "moe": dict(config=5, unit="GB/s", dtype="bf16",

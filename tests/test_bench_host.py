@@ -89,3 +89,18 @@ def test_w8_per_channel_bytes_are_codes_plus_one_scale_per_channel():
     c = inputs.make_gemm_case(2, 0, 1, n, k, bits=8, group_size=-1, act_dtype=inputs.F16,
                               scale_lo=0.001, scale_hi=0.01, with_zeros=False, with_bias=True)
     assert c.weight_bytes == n * k + 2 * n
+
+
+@pytest.mark.parametrize("name,act,group,ms", [
+    ("w8_decode_bf16", inputs.BF16, -1, {1, 4, 16}),
+    ("w4_g64_f16", inputs.F16, 64, {1, 512}),
+    ("w4_per_channel", inputs.BF16, -1, {1, 512}),
+    ("w8_mid", inputs.F16, -1, {24, 32, 48, 64})])
+def test_widened_workloads(name, act, group, ms):
+    w = bench.WORKLOADS[name]
+    cfg = inputs.GEMM_WORKLOADS[w["config"]]
+    assert cfg["act_dtype"] == act and cfg["group_size"] == group
+    assert {m for (m, _, _) in cfg["shapes"]} == ms
+    assert w["dtype"] == ("bf16" if act == inputs.BF16 else "f16")
+    c = inputs.workload_case(w["config"], 0)
+    assert c.act_dtype == act and c.scales.shape == ((c.n,) if group == -1 else (c.n, c.k // group))

@@ -160,7 +160,16 @@ W4_ACT_ORDER = dict(config=6, shapes=[(m, n, k) for m in (1, 512) for (n, k) in 
 # the same without act-order (channels in order, group 128)
 W4_G128 = dict(W4_ACT_ORDER, config=7, act_order=False)
 
-GEMM_WORKLOADS = {1: W4_TINY, 2: W8_DECODE, 3: W8_LARGE, 4: W4_G64, 6: W4_ACT_ORDER, 7: W4_G128}
+# the other activation dtype with each code width (bf16 with 8-bit decode,
+# fp16 with 4-bit), per-channel 4-bit, and 8-bit decode at 17..64 rows
+W8_DECODE_BF16 = dict(W8_DECODE, config=8, act_dtype=BF16)
+W4_G64_F16 = dict(W4_G64, config=9, act_dtype=F16)
+W4_PER_CHANNEL = dict(W4_G64, config=10, group_size=-1)
+W8_MID = dict(W8_DECODE, config=11, shapes=[(m, n, k) for m in (24, 32, 48, 64)
+                                            for (n, k) in W8_DECODE_NK])
+
+GEMM_WORKLOADS = {1: W4_TINY, 2: W8_DECODE, 3: W8_LARGE, 4: W4_G64, 6: W4_ACT_ORDER, 7: W4_G128,
+                  8: W8_DECODE_BF16, 9: W4_G64_F16, 10: W4_PER_CHANNEL, 11: W8_MID}
 
 
 def workload_case(config: int, case: int) -> GemmCase:

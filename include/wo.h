@@ -124,6 +124,33 @@ WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* sca
                   size_t workspace_bytes, void* stream);
 
 /*
+ * The configuration wo_gemm runs for a problem (the counterpart of acext
+ * 1.2.1's getChosenConfig, which returns the kernel configuration a runner
+ * will use; here the choice is a static plan, reported, not passed in).
+ * Pure host code: no CUDA call beyond reading the device's SM count (152
+ * when no device is visible).
+ */
+typedef enum { WO_KERNEL_STREAM = 0, WO_KERNEL_TENSOR_CORE = 1 } wo_kernel;
+
+typedef struct {
+    wo_kernel kernel;      /* weight streaming (small m) or tensor cores */
+    int tile_m;            /* rows of C per CTA tile (streaming: m) */
+    int tile_n;            /* output channels per CTA tile */
+    int k_splits;          /* CTAs (streaming: one cluster) or units per tile along k */
+    int ctas;              /* CTAs launched */
+    int stages;            /* streaming: shared-memory ring stages per CTA; else 0 */
+    size_t workspace_bytes; /* == wo_workspace_size */
+} wo_gemm_plan_t;
+
+/*
+ * Fills *plan for wo_gemm(m, n, k, group_size, bits, act_dtype).  Same
+ * argument rules as wo_gemm; WO_ERR_INVALID_ARG for a NULL plan; m == 0 or
+ * n == 0 gives a plan with ctas == 0.
+ */
+WO_API wo_status wo_gemm_plan(int m, int n, int k, int group_size, int bits, wo_dtype act_dtype,
+                              wo_gemm_plan_t* plan);
+
+/*
  * GPTQ act-order checkpoints ("[Misc][Kernel]: Add GPTQAllSpark
  * Quantization": the desc_act / has_g_idx case its kernel leaves out).  The
  * quantiser visited the input channels in its own order, so input channel c

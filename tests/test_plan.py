@@ -1,0 +1,73 @@
+"""CPU tests of the kernel choice and launch plan (wo_gemm_plan, the static
+counterpart of acext 1.2.1's getChosenConfig).  Pure host code: with no GPU
+visible the library plans for 152 SMs, GB300's count.  The GPU parity tests
+pick their small shapes to cover every tile configuration; these tests keep
+that true."""
+import pytest
+
+import weight_only_quantized_fpa_gb300 as wo
+from weight_only_quantized_fpa_gb300 import build as wo_build
+
+SMS = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    wo_build.build()
+    return wo.load_library()
+
+
+@pytest.mark.parametrize("m,n,k,bits,group,tile,splits", [
+    (250, 12736, 512, 4, 64, (256, 128), 1),
+    (300, 19520, 512, 8, -1, (128, 256), 1),
+    (300, 15296, 512, 8, -1, (256, 256), 1),
+    (260, 19584, 512, 4, 64, (128, 256), 1),
+    (300, 15296, 512, 4, 64, (256, 256), 1),
+    (200, 320, 6144, 8, -1, (128, 256), 2),
+    (130, 448, 12288, 4, 64, (128, 256), 4),
+    (200, 384, 3584, 8, -1, (128, 128), 2),
+    (130, 320, 4096, 4, 64, (128, 128), 2),
+    (4096, 4096, 4096, 8, -1, (256, 256), 1),
+    (512, 13312, 2048, 4, 64, (256, 256), 1),
+])
+def test_tensor_core_tile_configurations(m, n, k, bits, group, tile, splits):
+    p = wo.gemm_plan(m, n, k, bits, group, wo.WO_F16 if bits == 8 else wo.WO_BF16)
+    assert p["kernel"] == "tensor_core"
+    assert (p["tile_m"], p["tile_n"]) == tile
+    assert p["k_splits"] == splits
+    units = -(-m // tile[0]) * -(-n // tile[1]) * splits
+    assert p["ctas"] == min(units, SMS)
+    if splits > 1:  # a split plan gives every CTA exactly one unit
+        assert units <= SMS
+    assert p["workspace_bytes"] == wo.wo_workspace_size(m, n, k, group, bits)
+
+
+@pytest.mark.parametrize("bits,group", [(8, -1), (4, 64), (4, 128), (4, -1)])
+def test_kernel_choice_by_m(bits, group):
+    n, k = 512, 2048
+    for m, kern in [(1, "stream"), (16, "stream"), (17, "stream"), (64, "stream"),
+                    (65, "tensor_core"), (256, "tensor_core")]:
+        assert wo.gemm_plan(m, n, k, bits, group)["kernel"] == kern, (m, bits, group)
+
+
+@pytest.mark.parametrize("m,n,k,bits,group", [(1, 4608, 3584, 8, -1), (4, 3584, 18944, 8, -1),
+                                              (16, 37888, 3584, 8, -1), (1, 2048, 13312, 4, 64),
+                                              (1, 131072, 2048, 4, 64), (48, 3584, 3584, 8, -1)])
+def test_stream_plans_fill_one_resident_wave(m, n, k, bits, group):
+    p = wo.gemm_plan(m, n, k, bits, group, wo.WO_F16)
+    assert p["kernel"] == "stream" and p["tile_m"] == m
+    assert p["tile_n"] in (128, 256) and n % 16 == 0
+    assert 1 <= p["k_splits"] <= 8                    # portable cluster size
+    assert p["ctas"] == -(-n // p["tile_n"]) * p["k_splits"]
+    if p["k_splits"] > 1:                             # splits only up to two CTAs per SM
+        assert p["ctas"] <= 2 * SMS
+    assert p["stages"] >= 1 and p["workspace_bytes"] == 256
+
+
+def test_plan_argument_rules():
+    assert wo.gemm_plan(0, 256, 512, 8)["ctas"] == 0
+    with pytest.raises(wo.WoError):
+        wo.gemm_plan(4, 100, 512, 8)
+    with pytest.raises(wo.WoError):
+        wo.gemm_plan(4, 256, 512, 8, 64)        # 8-bit is per channel
+    assert wo.load_library().wo_gemm_plan(4, 256, 512, -1, 8, 0, None) == 1

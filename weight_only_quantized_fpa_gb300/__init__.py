@@ -24,7 +24,7 @@ __all__ = [
     "wo_act_order_perm", "wo_pack_act_order", "wo_act_order_workspace_size",
     "wo_gemm_act_order",
     "pack", "unpack", "pack_experts", "gemm", "embed", "moe_ffn", "Workspace",
-    "act_order_perm", "pack_act_order", "gemm_act_order",
+    "act_order_perm", "pack_act_order", "gemm_act_order", "wo_gemm_plan", "gemm_plan",
 ]
 
 WO_F16 = 0
@@ -83,6 +83,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.wo_moe_ffn.restype = I
         lib.wo_embed.argtypes = [P, I, P, P, P, P, I, I, I, I, I, P]
         lib.wo_embed.restype = I
+        lib.wo_gemm_plan.argtypes = [I, I, I, I, I, I, ctypes.POINTER(GemmPlan)]
+        lib.wo_gemm_plan.restype = I
         lib.wo_act_order_perm.argtypes = [P, I, I, P]
         lib.wo_act_order_perm.restype = I
         lib.wo_pack_act_order.argtypes = [P, P, P, I, I, I, P]
@@ -102,6 +104,13 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
 
 
 # ---------------------------------------------------------------- helpers --
+
+class GemmPlan(ctypes.Structure):
+    """wo_gemm_plan_t (include/wo.h)."""
+    _fields_ = [("kernel", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("k_splits", ctypes.c_int), ("ctas", ctypes.c_int), ("stages", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
+
 
 def _ptr(t) -> int | None:
     if t is None:
@@ -178,6 +187,22 @@ def wo_embed(ids, T: int, B_packed, scales, zeros, out, vocab: int, hidden: int,
     _raise(load_library().wo_embed(_ptr(ids), T, _ptr(B_packed), _ptr(scales), _ptr(zeros),
                                    _ptr(out), vocab, hidden, group_size, bits, act_dtype,
                                    _stream_ptr(stream)), "wo_embed")
+
+
+def wo_gemm_plan(m: int, n: int, k: int, group_size: int, bits: int, act_dtype: int) -> GemmPlan:
+    plan = GemmPlan()
+    _raise(load_library().wo_gemm_plan(m, n, k, group_size, bits, act_dtype, ctypes.byref(plan)),
+           "wo_gemm_plan")
+    return plan
+
+
+def gemm_plan(m: int, n: int, k: int, bits: int, group_size: int = -1,
+              act_dtype: int = WO_BF16) -> dict:
+    """The configuration wo_gemm runs for this problem, as a dict."""
+    p = wo_gemm_plan(m, n, k, group_size, bits, act_dtype)
+    return {"kernel": "tensor_core" if p.kernel == 1 else "stream", "tile_m": p.tile_m,
+            "tile_n": p.tile_n, "k_splits": p.k_splits, "ctas": p.ctas, "stages": p.stages,
+            "workspace_bytes": int(p.workspace_bytes)}
 
 
 def _host_i32(a, k: int, what: str):

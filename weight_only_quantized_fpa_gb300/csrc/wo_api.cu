@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "wo_internal.h"
+#include "wo_stream.h"
 
 namespace wo {
 
@@ -192,6 +193,43 @@ wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* scales, co
     if (st != WO_OK || a.m == 0 || a.n == 0)
         return st;
     return gemm_launch(a, static_cast<cudaStream_t>(stream));
+}
+
+wo_status wo_gemm_plan(int m, int n, int k, int group_size, int bits, wo_dtype act_dtype,
+                       wo_gemm_plan_t* plan)
+{
+    if (!plan)
+        return WO_ERR_INVALID_ARG;
+    *plan = wo_gemm_plan_t{};
+    const wo_status st = check_gemm_shape(m, n, k, group_size, bits);
+    if (st != WO_OK)
+        return st;
+    if (act_dtype != WO_F16 && act_dtype != WO_BF16)
+        return WO_ERR_INVALID_ARG;
+    if (m == 0 || n == 0)
+        return WO_OK;
+    plan->workspace_bytes = wo_workspace_size(m, n, k, group_size, bits);
+    const int g = norm_group(group_size, k);
+    if (use_tc(m, n, k, g, bits)) {
+        const TcPlan p = plan_tc(m, n, k, bits, act_dtype);
+        const int tm = 128 * p.ms;
+        const long long units =
+            (long long)((m + tm - 1) / tm) * ((n + p.bn - 1) / p.bn) * p.splits;
+        plan->kernel = WO_KERNEL_TENSOR_CORE;
+        plan->tile_m = tm;
+        plan->tile_n = p.bn;
+        plan->k_splits = p.splits;
+        plan->ctas = (int)(units < num_sms() ? units : num_sms());
+        return WO_OK;
+    }
+    const StreamPlan p = plan_stream(m, n, k, g, bits, OUT_PLAIN, 0);
+    plan->kernel = WO_KERNEL_STREAM;
+    plan->tile_m = m;
+    plan->tile_n = p.nw * 32;  // each consumer warp owns two 16-channel blocks
+    plan->k_splits = p.splits;
+    plan->ctas = p.grid_x * p.splits;
+    plan->stages = p.stages;
+    return WO_OK;
 }
 
 // ---- GPTQ act-order ---------------------------------------------------------

@@ -284,3 +284,37 @@ def test_act_order_workspace_keeps_gathered_A_clear_of_shared_area(lib, m, n, k,
     need = wo.wo_act_order_workspace_size(m, n, k, group, 4)
     plain = wo.wo_workspace_size(m, n, k, group, 4)
     assert need == up(max(plain, 256 + 65536)) + up(m * k * 2)
+
+
+def _moe_status(lib, T=16, H=4096, I=1408, E=64, topk=2, act=1, A=1 << 20, logits=1 << 21,
+                fc1=1 << 22, s1=1 << 23, fc2=1 << 24, s2=1 << 25, out=1 << 26, ws=None,
+                ws_bytes=0):
+    return lib.wo_moe_ffn(A, logits, fc1, s1, fc2, s2, out, T, H, I, E, topk, 0, act, ws,
+                          ws_bytes, None)
+
+
+def test_moe_rejects_bad_arguments_before_launch(lib):
+    # every call fails validation, so the placeholder addresses are never used
+    need = wo.wo_moe_workspace_size(16, 4096, 1408, 64, 2)
+    assert need > 0
+    assert _moe_status(lib, T=-1) == 1
+    assert _moe_status(lib, H=4000) == 1          # hidden % 64
+    assert _moe_status(lib, I=1400) == 1          # inter % 64
+    assert _moe_status(lib, E=0) == 1
+    assert _moe_status(lib, topk=3, E=2) == 1     # topk > experts
+    assert _moe_status(lib, topk=9, E=64) == 1    # topk > 8
+    assert _moe_status(lib, act=2) == 1
+    assert _moe_status(lib, A=None, ws=1 << 27, ws_bytes=need) == 1
+    assert _moe_status(lib, logits=(1 << 21) + 2, ws=1 << 27, ws_bytes=need) == 1
+    assert _moe_status(lib, out=(1 << 26) + 8, ws=1 << 27, ws_bytes=need) == 1
+    assert _moe_status(lib) == 3                  # no workspace
+    assert _moe_status(lib, ws=1 << 27, ws_bytes=need - 1) == 3
+    assert _moe_status(lib, ws=(1 << 27) + 128, ws_bytes=need) == 3
+    assert _moe_status(lib, T=0, A=None) == 0     # no tokens: a no-op
+
+
+def test_moe_workspace_size_invalid_is_zero(lib):
+    assert wo.wo_moe_workspace_size(0, 4096, 1408, 64, 2) == 0
+    assert wo.wo_moe_workspace_size(16, 4096, 1408, 2, 3) == 0
+    assert wo.wo_moe_workspace_size(1024, 4096, 1408, 64, 2) > \
+        wo.wo_moe_workspace_size(16, 4096, 1408, 64, 2)

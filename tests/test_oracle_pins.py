@@ -523,6 +523,31 @@ def test_gidx_channel_reads_only_its_own_group():
             assert np.array_equal(C2, base) == (gg != g[col])
 
 
+def _read_act_order_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "act_order_gemm.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            group, gi, q, sc, zc, a, c = [p.strip() for p in line.split("|")]
+            cases.append((int(group), [int(x) for x in gi.split()], [int(x) for x in q.split()],
+                          [float(x) for x in sc.split()], [float(x) for x in zc.split()],
+                          [float(x) for x in a.split()], float(c)))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(len(_read_act_order_golden())))
+def test_gidx_golden(case):
+    group, gi, q, sc, zc, a, expect = _read_act_order_golden()[case]
+    k = len(q)
+    B = np.array([[q[2 * j] | (q[2 * j + 1] << 4) for j in range(k // 2)]], dtype=np.uint8)
+    bits = lambda v: inputs.to_bits(np.array(v, dtype=np.float64), BF16)  # noqa: E731
+    C = oracle.gemm_gidx(bits([a]), BF16, B, bits([sc]), bits([zc]), np.array(gi, np.int32),
+                         None, 1, 1, k, group, 4)
+    assert C[0, 0] == expect
+
+
 def test_gidx_rejects_out_of_range_group():
     m, n, k, group = 1, 16, 128, 64
     c, g = _gidx_case(6, m, n, k, group)

@@ -523,6 +523,36 @@ def test_gidx_channel_reads_only_its_own_group():
             assert np.array_equal(C2, base) == (gg != g[col])
 
 
+def _read_gemm_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "gemm_worked.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, group, q, sc, zc, a, b, c = [p.strip() for p in line.split("|")]
+            cases.append((int(bits), int(group), [int(x) for x in q.split()],
+                          [float(x) for x in sc.split()],
+                          None if zc == "-" else [float(x) for x in zc.split()],
+                          [float(x) for x in a.split()], None if b == "-" else float(b),
+                          float(c)))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(len(_read_gemm_golden())))
+def test_gemm_golden(case):
+    bits, group, q, sc, zc, a, bias, expect = _read_gemm_golden()[case]
+    k = len(q)
+    if bits == 8:
+        B = np.array([q], dtype=np.uint8)
+    else:
+        B = np.array([[q[2 * j] | (q[2 * j + 1] << 4) for j in range(k // 2)]], dtype=np.uint8)
+    bf = lambda v: inputs.to_bits(np.array(v, dtype=np.float64), BF16)  # noqa: E731
+    C = oracle.gemm(bf([a]), BF16, B, bf([sc]), None if zc is None else bf([zc]),
+                    None if bias is None else bf([bias]), 1, 1, k, group, bits)
+    assert C[0, 0] == expect
+
+
 def _read_act_order_golden():
     cases = []
     with open(os.path.join(GOLDEN, "act_order_gemm.txt")) as f:

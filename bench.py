@@ -285,7 +285,7 @@ def oracle_pass(cases, frac: float, threads: int):
     return time.perf_counter() - t0, wbytes, flops
 
 
-def cpu_baseline(cases, unit, budget_s=8.0):
+def cpu_baseline(cases, unit, budget_s=10.0):
     threads = os.cpu_count() or 1
     frac = 1.0 / 64
     dt, wb, fl = oracle_pass(cases, frac, threads)
@@ -293,11 +293,20 @@ def cpu_baseline(cases, unit, budget_s=8.0):
     if dt < budget_s / 4:
         frac = min(1.0, frac * max(1.0, budget_s / max(dt, 1e-3) / 2))
         dt, wb, fl = oracle_pass(cases, frac, threads)
+    # a whole workload that takes well under the budget is repeated, so the
+    # figure rests on about the budget's worth of CPU work
+    reps = 1
+    if frac >= 1.0 and dt < budget_s / 2:
+        reps = max(1, min(100, int(budget_s / max(dt, 1e-3))))
+        dt = wb = fl = 0.0
+        for _ in range(reps):
+            d, b, f = oracle_pass(cases, frac, threads)
+            dt, wb, fl = dt + d, wb + b, fl + f
     value = wb / dt / 1e9 if unit == "GB/s" else fl / dt / 1e12
     return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
             "sample": f"every case of the workload on the first {frac:.4f} of its output "
-                      f"channels (rows capped likewise above m=64); {dt:.2f} s wall, "
-                      f"{wb / 1e6:.1f} MB of weights"}
+                      f"channels (rows capped likewise above m=64), {reps} pass(es); "
+                      f"{dt:.2f} s wall, {wb / 1e6:.1f} MB of weights"}
 
 
 # ------------------------------------------------------------ distributed --

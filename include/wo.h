@@ -284,17 +284,27 @@ WO_API wo_status wo_moe_ffn(const void* A, const float* gating_logits, const uin
  *   m*4 bytes of row scales, each rounded up to 256 bytes, within 16 MiB and
  *   256 KiB (e.g. m*k <= 8,388,608 and m <= 65,536); larger problems return
  *   WO_ERR_WORKSPACE with nothing enqueued.  Other cases need no scratch.
- *   The first call on a device looks up the array's device address and
- *   zeroes its error word (a blocking cudaMemset), so make that first call
- *   before any stream capture.  The call allocates and frees nothing.
- *   Every call shares the array: calls whose kernels overlap on the GPU
- *   (unordered streams) race on it.  A kernel that gives up a bounded wait
- *   is not reported by this entry point.
+ *   Every call looks up the array's address in the caller's current CUDA
+ *   context (a host-side lookup), so another context, or a primary context
+ *   recreated by cudaDeviceReset, uses its own copy.  The first call in a
+ *   context zeroes that copy's error word (a blocking cudaMemset), so make
+ *   that first call before any stream capture.  The call allocates and frees
+ *   nothing.  Every call shares the array: calls whose kernels overlap on the
+ *   GPU (unordered streams) race on it.  A kernel that gives up a bounded
+ *   wait records it in the array's error word: wo_noalloc_check reads it.
  */
 WO_API wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed, const void* scales,
                                     const void* zeros, const void* bias, void* C, int m, int n,
                                     int k, int group_size, int bits, wo_dtype act_dtype,
                                     void* stream);
+
+/*
+ * The failure report of wo_gemm_tc_noalloc (no counterpart on the pages):
+ * synchronises `stream`, then reads and clears the error word of the
+ * built-in scratch of the current context.  Returns WO_OK, WO_ERR_TIMEOUT
+ * (a kernel gave up a bounded wait since the last check), or WO_ERR_CUDA.
+ */
+WO_API wo_status wo_noalloc_check(void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the error word a kernel may
@@ -318,6 +328,14 @@ WO_API wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, voi
  */
 WO_API wo_status wo_selftest_wait_timeout(void* workspace, size_t workspace_bytes, unsigned limit_us,
                                           void* stream);
+
+/*
+ * wo_selftest_wait_timeout on the built-in scratch of wo_gemm_tc_noalloc
+ * (no counterpart on the pages): the bounded wait runs out after `limit_us`
+ * microseconds (1..1000000) and records its code in that scratch's error
+ * word, which wo_noalloc_check then reports as WO_ERR_TIMEOUT.
+ */
+WO_API wo_status wo_noalloc_selftest_wait_timeout(unsigned limit_us, void* stream);
 
 #ifdef __cplusplus
 }

@@ -83,11 +83,21 @@ class DeviceCase:
                            c.group_size, c.bits)
 
 
-def sample_rows(m: int, count: int = 12, seed: int = 0) -> np.ndarray:
-    """First, last and a few random rows (sorted, unique)."""
+def sample_rows(m: int, count: int = 64, seed: int = 0) -> np.ndarray:
+    """At least `count` rows (all rows when m <= count), sorted and unique: the
+    first and last row, one row in every 128-row block (so both 128-row halves
+    of a 256-row tile, every tile a persistent CTA runs as its second or later
+    unit, and the ragged last tile are all checked; the row within the block
+    moves through the four 32-row TMEM lane quadrants from block to block),
+    then random rows up to `count`."""
     if m <= count:
         return np.arange(m)
     rng = np.random.default_rng(seed)
-    rows = set([0, m - 1, m // 2])
-    rows.update(rng.choice(m, size=count - 3, replace=False).tolist())
+    rows = {0, m - 1}
+    for b, b0 in enumerate(range(0, m, 128)):
+        rows.add(min(b0 + 32 * (b % 4) + int(rng.integers(0, 32)), m - 1))
+    free = np.setdiff1d(np.arange(m), np.fromiter(rows, dtype=np.int64))
+    need = count - len(rows)
+    if need > 0:
+        rows.update(rng.choice(free, size=need, replace=False).tolist())
     return np.array(sorted(rows))

@@ -146,7 +146,7 @@ def test_act_order_workload_sampled(wo, case):
     ac = ActOrderCase(wo, c)
     C = ac.run(wo)
     torch.cuda.synchronize()
-    rows = sample_rows(c.m, 8)
+    rows = sample_rows(c.m)
     assert_within_tolerance(from_device_bits(C)[rows], c.act_dtype, ac.oracle_rows(rows),
                             c.name)
 
@@ -208,5 +208,5 @@ def test_group128_in_order_workload_sampled(wo, case):
     dc = DeviceCase(c)
     C = dc.run()
     torch.cuda.synchronize()
-    rows = sample_rows(c.m, 8)
+    rows = sample_rows(c.m)
     assert_within_tolerance(from_device_bits(C)[rows], c.act_dtype, dc.oracle_rows(rows), c.name)

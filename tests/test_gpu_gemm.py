@@ -32,7 +32,7 @@ def _check_full(dc: DeviceCase, what: str):
     return assert_within_tolerance(from_device_bits(C), dc.c.act_dtype, ref, what)
 
 
-def _check_sampled(dc: DeviceCase, what: str, count=12):
+def _check_sampled(dc: DeviceCase, what: str, count=64):
     C = dc.run()
     torch.cuda.synchronize()
     rows = sample_rows(dc.c.m, count)
@@ -138,7 +138,7 @@ def test_w4_g64(wo, case):
     if dc.c.m == 1:
         _check_full(dc, dc.c.name)
     else:
-        _check_sampled(dc, dc.c.name, count=8)
+        _check_sampled(dc, dc.c.name)
 
 
 # ---------------------------------------------------------- properties -----

@@ -358,6 +358,37 @@ def test_gemm_one_hot_rows_pick_weight_columns(bits):
         assert np.array_equal(C[i], w.astype(np.float64))
 
 
+def _read_embed_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "embed_rows.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, group, dt, hidden, codes, sc, zc, idx, row = [x.strip() for x in line.split("|")]
+            cases.append((int(bits), int(group), F16 if dt == "f16" else BF16, int(hidden),
+                          [int(x) for x in codes.split()], [float(x) for x in sc.split()],
+                          None if zc == "-" else [float(x) for x in zc.split()], int(idx),
+                          [float(x) for x in row.split()]))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(len(_read_embed_golden())))
+def test_embed_golden(case):
+    # hand-worked rows (tests/golden/embed_rows.txt): dequantisation, the
+    # single rounding (two ties to even) and the zero row of an id out of range
+    bits, group, dt, hidden, codes, sc, zc, idx, expect = _read_embed_golden()[case]
+    q = np.array(codes, dtype=np.uint8)
+    vocab = q.size // hidden
+    q = q.reshape(vocab, hidden)
+    B = q if bits == 8 else (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    s = inputs.to_bits(np.array(sc), dt)
+    z = None if zc is None else inputs.to_bits(np.array(zc), dt)
+    assert np.array_equal(_value(s, dt), np.array(sc))  # the inputs are exact in dt
+    got = oracle.embed(np.array([idx], dtype=np.int32), B, s, z, vocab, hidden, group, bits, dt)
+    assert np.array_equal(_value(got[0], dt), np.array(expect))
+
+
 @pytest.mark.parametrize("bits,group,dtype", [(4, 64, BF16), (8, -1, F16), (4, -1, F16)])
 def test_embed_rows_are_identity_gemm_columns(bits, group, dtype):
     # A = I_k gives C[i, j] = w[j][i]: column id of that product, rounded

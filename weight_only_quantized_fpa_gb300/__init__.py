@@ -20,7 +20,8 @@ __all__ = [
     "WO_F16", "WO_BF16", "WoError", "load_library", "library_path",
     "wo_status_string", "wo_packed_bytes", "wo_pack", "wo_unpack", "wo_workspace_size",
     "wo_gemm", "wo_moe_workspace_size", "wo_moe_ffn", "wo_check_workspace",
-    "wo_gemm_tc_noalloc", "wo_selftest_wait_timeout", "wo_embed",
+    "wo_gemm_tc_noalloc", "wo_noalloc_check", "wo_noalloc_selftest_wait_timeout",
+    "wo_selftest_wait_timeout", "wo_embed",
     "wo_act_order_perm", "wo_pack_act_order", "wo_act_order_workspace_size",
     "wo_gemm_act_order",
     "pack", "unpack", "pack_experts", "gemm", "embed", "moe_ffn", "Workspace",
@@ -99,6 +100,10 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.wo_gemm_tc_noalloc.restype = I
         lib.wo_selftest_wait_timeout.argtypes = [P, S, ctypes.c_uint, P]
         lib.wo_selftest_wait_timeout.restype = I
+        lib.wo_noalloc_check.argtypes = [P]
+        lib.wo_noalloc_check.restype = I
+        lib.wo_noalloc_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+        lib.wo_noalloc_selftest_wait_timeout.restype = I
         _lib = lib
         return lib
 
@@ -272,6 +277,18 @@ def wo_gemm_tc_noalloc(A, B_packed, scales, zeros, bias, C, m: int, n: int, k: i
                                              _ptr(bias), _ptr(C), m, n, k, group_size, bits,
                                              act_dtype, _stream_ptr(stream)),
            "wo_gemm_tc_noalloc")
+
+
+def wo_noalloc_check(stream=None) -> int:
+    """Synchronise and return the status the kernels left in the built-in
+    scratch of wo_gemm_tc_noalloc (the word is cleared)."""
+    return int(load_library().wo_noalloc_check(_stream_ptr(stream)))
+
+
+def wo_noalloc_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """A wait that runs out after limit_us, reporting into the built-in scratch."""
+    _raise(load_library().wo_noalloc_selftest_wait_timeout(limit_us, _stream_ptr(stream)),
+           "wo_noalloc_selftest_wait_timeout")
 
 
 def wo_selftest_wait_timeout(workspace, workspace_bytes: int, limit_us: int, stream=None) -> None:

@@ -26,6 +26,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int num_sms();  // SM count of the current device (152 when none is visible)
 
+// bounded-wait self-test: one CTA waits on an mbarrier nothing completes,
+// gives up after limit_us and records its code in *err (wo_selftest.cu)
+cudaError_t launch_wait_timeout(unsigned* err, unsigned limit_us, cudaStream_t s);
+
 // ---- pack -----------------------------------------------------------------
 // perm (pack only, optional): packed column j takes row-major column perm[j]
 cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,

@@ -9,17 +9,23 @@
 //
 // The scratch (error word, fp16 copy of bf16 activations and their row
 // scales) lives in g_scratch below; every GPU that loads this library keeps
-// it (16.31 MiB) until the process exits.  Host code cannot use
-// g_scratch's name as a device address, so the first call on each device
-// looks the address up with cudaGetSymbolAddress (with that device current)
-// and caches it.  That first call also zeroes the error word with a blocking
-// cudaMemset, so it should come before any stream capture.
+// it (16.31 MiB) until the process exits.  Host code cannot use g_scratch's
+// name as a device address: each call looks the address up with
+// cudaGetSymbolAddress in the caller's current context (a host-side table
+// lookup), so a context other than the device's primary one, or a primary
+// context recreated after cudaDeviceReset, gets its own copy's address.  The
+// first call that meets a new (context, address) pair zeroes that copy's
+// error word with a blocking cudaMemset, so it should come before any stream
+// capture.
 //
 // All calls share the one array: two calls whose kernels overlap on the GPU
 // (different streams, no ordering between them) race on it.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <vector>
 
 #include "wo_internal.h"
 
@@ -34,30 +40,58 @@ constexpr size_t kNoAllocBytes = kWsScratch + ((size_t)16 << 20) + ((size_t)256 
 
 static __device__ __align__(256) unsigned char g_scratch[kNoAllocBytes];
 
-std::mutex g_mu;
-void* g_addr[64] = {nullptr};
+// The current context (driver entry point fetched through the runtime, so
+// the library needs no link-time libcuda); null when it cannot be read.
+CUcontext current_context()
+{
+    static const PFN_cuCtxGetCurrent_v4000 fn = []() -> PFN_cuCtxGetCurrent_v4000 {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        cudaGetLastError();
+        return nullptr;
+    }();
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS)
+        return nullptr;
+    return c;
+}
 
-// Device address of g_scratch on the current device, set up on first use.
+struct Cleared {
+    CUcontext ctx;
+    void* addr;
+};
+
+std::mutex g_mu;
+std::vector<Cleared> g_cleared;  // (context, address) pairs whose error word was zeroed
+
+// Device address of g_scratch in the current context; zeroes its error word
+// the first time a (context, address) pair is seen.
 cudaError_t scratch_address(void** out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
+    const CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess)
-            return e;
+    bool seen = false;
+    for (const Cleared& c : g_cleared)
+        seen = seen || (c.ctx == ctx && c.addr == p);
+    if (!seen) {
         e = cudaMemset(p, 0, kWsHeader);  // error word starts at zero
         if (e != cudaSuccess)
             return e;
-        g_addr[dev] = p;
+        try {
+            g_cleared.push_back(Cleared{ctx, p});
+        } catch (...) {
+            // no record: the next call zeroes the word again, harmless
+        }
     }
-    *out = g_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -114,4 +148,34 @@ extern "C" wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed,
     a.ws_bytes = kNoAllocBytes;
     return launch_tc(a, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess ? WO_OK
                                                                                 : WO_ERR_CUDA;
+}
+
+extern "C" wo_status wo_noalloc_check(void* stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return WO_ERR_CUDA;
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess)
+        return WO_ERR_CUDA;
+    unsigned flag = 0;
+    if (cudaMemcpy(&flag, scratch, sizeof flag, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return WO_ERR_CUDA;
+    if (flag == 0)
+        return WO_OK;
+    if (cudaMemset(scratch, 0, sizeof flag) != cudaSuccess)
+        return WO_ERR_CUDA;
+    return WO_ERR_TIMEOUT;
+}
+
+extern "C" wo_status wo_noalloc_selftest_wait_timeout(unsigned limit_us, void* stream)
+{
+    if (limit_us < 1 || limit_us > 1000000)
+        return WO_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess)
+        return WO_ERR_CUDA;
+    return launch_wait_timeout(static_cast<unsigned*>(scratch), limit_us,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? WO_OK
+               : WO_ERR_CUDA;
 }

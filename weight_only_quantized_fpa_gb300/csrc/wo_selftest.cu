@@ -27,6 +27,13 @@ __global__ void wait_timeout_kernel(unsigned* err, unsigned long long limit_ns)
 }
 
 }  // namespace
+
+cudaError_t launch_wait_timeout(unsigned* err, unsigned limit_us, cudaStream_t s)
+{
+    wait_timeout_kernel<<<1, 32, 0, s>>>(err, (unsigned long long)limit_us * 1000ull);
+    return cudaGetLastError();
+}
+
 }  // namespace wo
 
 extern "C" wo_status wo_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
@@ -35,7 +42,8 @@ extern "C" wo_status wo_selftest_wait_timeout(void* workspace, size_t workspace_
     if (!workspace || workspace_bytes < wo::kWsHeader ||
         (reinterpret_cast<uintptr_t>(workspace) % 256) != 0 || limit_us < 1 || limit_us > 1000000)
         return WO_ERR_INVALID_ARG;
-    wo::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<unsigned*>(workspace), (unsigned long long)limit_us * 1000ull);
-    return cudaGetLastError() == cudaSuccess ? WO_OK : WO_ERR_CUDA;
+    return wo::launch_wait_timeout(static_cast<unsigned*>(workspace), limit_us,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? WO_OK
+               : WO_ERR_CUDA;
 }

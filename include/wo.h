@@ -278,12 +278,14 @@ WO_API wo_status wo_moe_ffn(const void* A, const float* gating_logits, const uin
  * counterpart: their runners always take a caller-allocated workspace.
  *   Arguments as for wo_gemm, minus the workspace.  Always runs the
  *   tensor-core kernel, whatever m is.
- *   Scratch: a 16.31 MiB array in the library's device memory, held on every
- *   GPU that loads the library until the process exits.  It must hold the
- *   fp16 copy of bf16 activations that 4-bit weights need: m*k*2 bytes plus
- *   m*4 bytes of row scales, each rounded up to 256 bytes, within 16 MiB and
- *   256 KiB (e.g. m*k <= 8,388,608 and m <= 65,536); larger problems return
- *   WO_ERR_WORKSPACE with nothing enqueued.  Other cases need no scratch.
+ *   Scratch: a 24.06 MiB array in the library's device memory, held on every
+ *   GPU that loads the library until the process exits.  8-bit weights need
+ *   none of it.  4-bit weights need, each rounded up to 256 bytes, within
+ *   24 MiB in all: n*(k/group_size)*4 bytes of pre-scaled scale and zero
+ *   pairs, n*2 bytes of column scales and, with bf16 activations, the fp16
+ *   copy of A (m*k*2 bytes) and its row scales (m*4 bytes) -- e.g. m*k up
+ *   to about 12 million; larger problems return WO_ERR_WORKSPACE with
+ *   nothing enqueued.
  *   Every call looks up the array's address in the caller's current CUDA
  *   context (a host-side lookup), so another context, or a primary context
  *   recreated by cudaDeviceReset, uses its own copy.  The first call in a

@@ -18,11 +18,14 @@ def test_launch_count_per_call():
                               scale_lo=0.01, scale_hi=0.02, with_zeros=True, with_bias=False)
     assert bench.case_launches(c) == 1                       # streaming kernel
     c.m = 512
-    assert bench.case_launches(c) == 2                       # fp16 copy of A + tensor cores
+    assert bench.case_launches(c) == 2                       # 4-bit prepass + tensor cores
     c.act_dtype = inputs.F16
-    assert bench.case_launches(c) == 1
+    assert bench.case_launches(c) == 2                       # the prepass runs for fp16 A too
+    c.bits = 8
+    assert bench.case_launches(c) == 1                       # 8-bit: the GEMM kernel alone
+    c.bits = 4
     c.g_idx = np.zeros(c.k, dtype=np.int32)
-    assert bench.case_launches(c) == 2                       # + the act-order gather
+    assert bench.case_launches(c) == 3                       # + the act-order gather
     c.m = 1
     assert bench.case_launches(c) == 2
 

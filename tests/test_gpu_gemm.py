@@ -100,6 +100,62 @@ def test_w4_nonnegative_activations_long_groups(wo, m, n, k, group):
     _check_full(DeviceCase(c), f"w4 |a| m{m} k{k} g{group}")
 
 
+# --------------------------------- 4-bit inputs outside fp16's own range --
+#
+# The tensor-core kernel multiplies 4-bit weights in fp16; its prepass brings
+# every output channel's scales and zeros (and bf16 activation rows) into
+# fp16's range by powers of two that the epilogue undoes.  These cases would
+# overflow fp16 (scales >= 2^13 make (q - 8) * s reach 2^16) or fall into its
+# subnormals (scales near 1e-6) without that; activation rows here span more
+# than 2^30.  m = 4 runs the weight-streaming kernel, the others the
+# tensor-core kernel (k split included).
+
+def _domain_case(m, n, k, act, seed, *, s_lo, s_hi, z_sigma, s_span=0, a_span=0, row_span=0,
+                 a_shift=0, group=64, bias=False):
+    c = inputs.make_gemm_case(13, seed, m, n, k, bits=4, group_size=group, act_dtype=act,
+                              scale_lo=s_lo, scale_hi=s_hi, with_zeros=True, with_bias=bias)
+    G = 1 if group in (-1, k) else k // group
+    c.zeros = inputs.normal_bits(inputs.rng_for(13, seed, inputs.T_ZERO), c.scales.shape, act,
+                                 z_sigma)
+    if s_span:  # per group, scales times 2^-u, u uniform in 0..s_span
+        u = inputs.rng_for(13, seed, 20).integers(0, s_span + 1, size=(n, G))
+        val = oracle.decode(c.scales, act) * np.exp2(-u.astype(np.float64))
+        c.scales = inputs.to_bits(val.reshape(c.scales.shape), act)
+    if a_span or row_span or a_shift:  # A times 2^u per element, 2^v per row, 2^a_shift
+        rng = inputs.rng_for(13, seed, 21)
+        u = rng.integers(-a_span, a_span + 1, size=(m, k)) if a_span else 0
+        v = rng.integers(-row_span, row_span + 1, size=(m, 1)) if row_span else 0
+        val = oracle.decode(c.A, act) * np.exp2(u + v + a_shift)
+        c.A = inputs.to_bits(val, act)
+    return c
+
+
+DOMAIN = [
+    # m, n, k, act, s_lo, s_hi, z_sigma, extra
+    (200, 384, 1024, inputs.BF16, 8192.0, 16384.0, 4096.0, {}),          # (q-8)s beyond 65504
+    # fp16 output: A scaled by 2^-10 so that C (about 2^23 otherwise) fits in fp16
+    (200, 384, 1024, inputs.F16, 8192.0, 16384.0, 2048.0, dict(a_shift=-10)),
+    (4, 384, 1024, inputs.BF16, 8192.0, 16384.0, 4096.0, {}),
+    (300, 448, 1024, inputs.BF16, 5e-7, 2e-6, 1e-6, {}),                 # fp16 subnormal scales
+    (130, 320, 1024, inputs.F16, 5e-7, 2e-6, 1e-6, {}),
+    (4, 320, 1024, inputs.F16, 5e-7, 2e-6, 1e-6, {}),
+    (200, 384, 1024, inputs.BF16, 0.005, 0.02, 0.01, dict(a_span=16)),   # rows span 2^32+
+    (200, 384, 1024, inputs.BF16, 0.005, 0.02, 0.01, dict(a_span=16, row_span=60, bias=True)),
+    (4, 384, 1024, inputs.BF16, 0.005, 0.02, 0.01, dict(a_span=16, row_span=60)),
+    (200, 384, 1024, inputs.BF16, 0.005, 0.02, 1e-4, dict(s_span=30)),   # a channel's scales span 2^30
+    (130, 448, 12288, inputs.BF16, 8192.0, 16384.0, 4096.0, {}),         # k split in 4
+    (96, 128, 512, inputs.BF16, 5e-7, 2e-6, 1e-6, dict(group=-1)),       # per channel
+]
+
+
+@pytest.mark.parametrize("m,n,k,act,s_lo,s_hi,z_sigma,extra", DOMAIN)
+def test_w4_inputs_beyond_fp16_range(wo, m, n, k, act, s_lo, s_hi, z_sigma, extra):
+    c = _domain_case(m, n, k, act, 500 + m + n + int(np.log2(s_hi) + 64), s_lo=s_lo, s_hi=s_hi,
+                     z_sigma=z_sigma, **extra)
+    st = _check_full(DeviceCase(c), f"w4 domain m{m} s~{s_hi:g} {extra}")
+    assert st["ref_max"] > 0
+
+
 def test_split_k_long_reduction(wo):
     # few channels and a long k: the k range is split across a cluster of CTAs
     c = inputs.make_gemm_case(8, 77, 4, 64, 18944, bits=8, group_size=-1, act_dtype=inputs.F16,

@@ -128,7 +128,7 @@ size_t wo_workspace_size(int m, int n, int k, int group_size, int bits)
     if (use_tc(m, n, k, group_size, bits)) {
         // bf16 activations with 4-bit weights need an fp16 copy of A; size for
         // the larger of the two activation dtypes' needs
-        return plan_tc(m, n, k, bits, WO_BF16).ws_bytes;
+        return plan_tc(m, n, k, norm_group(group_size, k), bits, WO_BF16).ws_bytes;
     }
     return stream_workspace_bytes();
 }
@@ -179,7 +179,7 @@ static wo_status gemm_prepare(const void* A, const uint8_t* B_packed, const void
 static wo_status gemm_launch(const GemmArgs& a, cudaStream_t s)
 {
     if (use_tc(a.m, a.n, a.k, a.group, a.bits))
-        return cuda_status(launch_tc(a, plan_tc(a.m, a.n, a.k, a.bits, a.act), s));
+        return cuda_status(launch_tc(a, plan_tc(a.m, a.n, a.k, a.group, a.bits, a.act), s));
     return cuda_status(launch_stream_gemm(a, s));
 }
 
@@ -211,7 +211,7 @@ wo_status wo_gemm_plan(int m, int n, int k, int group_size, int bits, wo_dtype a
     plan->workspace_bytes = wo_workspace_size(m, n, k, group_size, bits);
     const int g = norm_group(group_size, k);
     if (use_tc(m, n, k, g, bits)) {
-        const TcPlan p = plan_tc(m, n, k, bits, act_dtype);
+        const TcPlan p = plan_tc(m, n, k, g, bits, act_dtype);
         const int tm = 128 * p.ms;
         const long long units =
             (long long)((m + tm - 1) / tm) * ((n + p.bn - 1) / p.bn) * p.splits;

@@ -28,19 +28,29 @@
 //                accumulator (256 x 256, 8-bit) the dequantisation warps,
 //                idle until it is handed back, drain two thirds of it;
 //   warps 8-15   dequantisation: code ring -> registers -> exact (q - 128)
-//                for 8-bit codes or fp16 round((q - 8) * s + z) for 4-bit
+//                for 8-bit codes or fp16 round((q - 8) * s' + z') for 4-bit
 //                group codes, written with stmatrix into the operand ring in
 //                the K-major 128-byte-swizzled layout the MMA reads (4-bit
-//                scales and zeros are loaded into registers a few k blocks
-//                ahead).
+//                scale and zero pairs are loaded into registers a few k
+//                blocks ahead).
 // Every mbarrier wait is bounded: a wait that runs out records an error word
 // in the workspace header and the CTA winds down (see the abort path).
 //
 // Operand types: 8-bit codes run the MMA in the activation dtype, in which
-// q - 128 is exact.  4-bit codes run it in fp16: A is first converted to
-// fp16 by a prepass with a per-row power-of-two scale (exact for bf16 values
-// of normal range), and the weight is fp16 round((q - 8) * s + z) computed
-// by one fused multiply-add per pair from the exact fp16 (q - 8).
+// q - 128 is exact.  4-bit codes run it in fp16, with both operands brought
+// into fp16's range by powers of two that the epilogue undoes: a prepass
+// (tc_prep_kernel) picks for every output channel n a power of two 2^E_n
+// that puts the channel's largest |scale| or |zero| in [2^10, 2^11) and
+// writes the channel's scales and zeros times 2^-E_n as fp16 pairs
+// (s', z'); for bf16 activations it also converts A to fp16 with a
+// per-row power of two 2^E_r (row maximum in [2^14, 2^15); exact for bf16
+// values within 2^24 of the row maximum).  The weight is then
+// fp16 round((q - 8) * s' + z'), one fused multiply-add per pair from the
+// exact fp16 (q - 8), at most 9 * 2^11 in magnitude, and the epilogue
+// scales the fp32 sum by 2^(E_r + E_n).  So any finite bf16 scale, zero and
+// activation is in range; only values more than 2^24 below their channel's
+// (or row's) largest fall into fp16's subnormals, where their share of the
+// sum is below the output's rounding.
 #include "wo_common.cuh"
 #include "wo_internal.h"
 #include "wo_sm100.cuh"
@@ -93,8 +103,9 @@ struct TcParams {
     int m, n, k;
     int num_kb;              // k / BK
     int m_tiles, n_tiles;    // output tiles along m and n
-    const uint16_t* scales;  // 8-bit: [n]; 4-bit: [n, G]
-    const uint16_t* zeros;   // 4-bit only, [n, G] or null
+    const uint16_t* scales;  // 8-bit: [n]
+    const uint32_t* sz;      // 4-bit: [n, G] fp16 pairs (s' low, z' high), pre-scaled by 2^-E_n
+    const uint16_t* colscale;  // 4-bit: [n] 2^E_n as bf16 bits
     const uint16_t* bias;    // [n] or null
     const float* rowscale;   // 4-bit with a converted A: [m] powers of two; else null
     uint16_t* C;
@@ -135,13 +146,13 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int bm, in
     }
 }
 
-// 4-bit: the scale and zero bits of one dequant warp's tiles for one k block
-// (rows g and g + 8 of each tile, low and high halves), loaded a few k
-// blocks ahead of their use.
+// 4-bit: the pre-scaled (s', z') fp16 pairs of one dequant warp's tiles for
+// one k block (channels g and g + 8 of each tile), loaded a few k blocks
+// ahead of their use.
 template <int BITS, int BN>
 struct DqScales {
     static constexpr int R = BITS == 4 ? TcCfg<BITS, BN>::R : 1;
-    uint32_t s2[R], z2[R];
+    uint32_t lo[R], hi[R];
 };
 
 template <int BITS, int BN>
@@ -156,24 +167,15 @@ __device__ __forceinline__ void load_scales(const TcParams& p, int n0, int kb, i
         for (int r = 0; r < Cfg::R; ++r) {
             const int nb = (dw + kDequantWarps * r) / Cfg::TPN;
             const int ch = n0 + nb * 16 + g;
-            c.s2[r] = 0u;
-            c.z2[r] = 0u;
+            c.lo[r] = 0u;
+            c.hi[r] = 0u;
             if (ch < p.n) {  // n is a multiple of 16: row ch + 8 is in range too
-                const size_t lo = (size_t)ch * p.G + gi, hi = lo + (size_t)8 * p.G;
-                c.s2[r] = (uint32_t)ld_nc_u16(p.scales + lo) | ((uint32_t)ld_nc_u16(p.scales + hi) << 16);
-                if (p.zeros)
-                    c.z2[r] = (uint32_t)ld_nc_u16(p.zeros + lo) | ((uint32_t)ld_nc_u16(p.zeros + hi) << 16);
+                const size_t lo = (size_t)ch * p.G + gi;
+                c.lo[r] = ld_nc_u32(p.sz + lo);
+                c.hi[r] = ld_nc_u32(p.sz + lo + (size_t)8 * p.G);
             }
         }
     }
-}
-
-// Broadcast one 16-bit value (given in the activation dtype) as an fp16 pair.
-template <int ACT>
-__device__ __forceinline__ uint32_t f16_pair(uint32_t bits16)
-{
-    const uint32_t h = from_f32<ACT_F16>(to_f32<ACT>((uint16_t)bits16));
-    return h | (h << 16);
 }
 
 // Dequantise one warp's share of a k block: code stage at c_s -> operand
@@ -195,11 +197,11 @@ __device__ __forceinline__ void dequant_stage(uint32_t c_s, const DqScales<BITS,
         const int tile = dw + kDequantWarps * r;
         const int nb = tile / Cfg::TPN, tl = tile % Cfg::TPN;
         uint32_t slo = 0, shi = 0, zlo = 0, zhi = 0;
-        if constexpr (BITS == 4) {
-            slo = f16_pair<ACT>(sc.s2[r] & 0xFFFFu);
-            shi = f16_pair<ACT>(sc.s2[r] >> 16);
-            zlo = f16_pair<ACT>(sc.z2[r] & 0xFFFFu);
-            zhi = f16_pair<ACT>(sc.z2[r] >> 16);
+        if constexpr (BITS == 4) {  // s' and z' of channels g and g + 8, each doubled
+            slo = prmt(sc.lo[r], 0u, 0x1010u);
+            zlo = prmt(sc.lo[r], 0u, 0x3232u);
+            shi = prmt(sc.hi[r], 0u, 0x1010u);
+            zhi = prmt(sc.hi[r], 0u, 0x3232u);
         }
         // lane -> row address of stmatrix matrix mi: rows r8 (+8 for mi >= 2),
         // 16-byte chunk of 8 codes (+1 for mi odd); matrices 0 and 1 (and 2
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
             const int col = n0 + 2 * (lane * CW + i);
-            csc[i] = BITS == 8 ? col_pair(p.scales, col) : 0u;
+            csc[i] = col_pair(BITS == 8 ? p.scales : p.colscale, col);
             cbi[i] = p.bias ? col_pair(p.bias, col) : 0u;
         }
     };
@@ -345,13 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int src = (cc * 16 + j) / CW;
-            if constexpr (BITS == 8)  // 4-bit: the scales were applied to the codes
-                sc[j] = __shfl_sync(0xffffffffu, csc[j % CW], src);
+            sc[j] = __shfl_sync(0xffffffffu, csc[j % CW], src);
             bi[j] = __shfl_sync(0xffffffffu, cbi[j % CW], src);
         }
     };
-    // scale (8-bit) or row scale (4-bit), bias, one rounding: 32 values of
-    // row `row`, columns nc..nc+31
+    // scale (8-bit) or row and column powers of two (4-bit), bias, one
+    // rounding: 32 values of row `row`, columns nc..nc+31
     auto finish = [&](int row, int nc, float rs, const float (&v)[32], const uint32_t (&sc)[16],
                       const uint32_t (&bi)[16]) {
         uint32_t packed[16];
@@ -362,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v0 *= to_f32<ACT>((uint16_t)(sc[j] & 0xFFFFu));
                 v1 *= to_f32<ACT>((uint16_t)(sc[j] >> 16));
             } else {
-                v0 *= rs;
-                v1 *= rs;
+                v0 *= rs * to_f32<ACT_BF16>((uint16_t)(sc[j] & 0xFFFFu));
+                v1 *= rs * to_f32<ACT_BF16>((uint16_t)(sc[j] >> 16));
             }
             if (p.bias) {
                 v0 += to_f32<ACT>((uint16_t)(bi[j] & 0xFFFFu));
@@ -697,15 +698,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// A bf16 -> fp16 with a per-row power-of-two scale: row r is multiplied by
-// 2^-E (E chosen so max |a| * 2^-E lies in [2^14, 2^15)), which is exact,
-// then rounded to fp16, which is exact for bf16 values whose scaled
-// magnitude is at least 2^-14; rowscale[r] = 2^E undoes it in the epilogue.
-// One CTA per row, 16-byte loads and stores (k % 64 == 0 and A 16-byte
-// aligned on this path); up to kA16Cache chunks of 8 values per thread stay
-// in registers between the max and the conversion, so rows up to 16384
-// values are read once.
-constexpr int kA16Threads = 256, kA16Cache = 8;
+// The 4-bit prepass (one launch before the GEMM), in two kinds of CTA:
+//   - CTAs [0, a_ctas), bf16 activations only: row r of A times 2^-E_r
+//     (E_r chosen so max |a| * 2^-E_r lies in [2^14, 2^15)), which is exact,
+//     rounded to fp16, which is exact for bf16 values whose scaled magnitude
+//     is at least 2^-14; rowscale[r] = 2^E_r.  One CTA per row, 16-byte
+//     loads and stores (k % 64 == 0 and A 16-byte aligned on this path); up
+//     to kA16Cache chunks of 8 values per thread stay in registers between
+//     the maximum and the conversion, so rows of up to 16384 values are read
+//     once.
+//   - the other CTAs, one warp per output channel n: M = the largest |scale|
+//     or |zero| of the channel's groups, E_n with M * 2^-E_n in [2^10, 2^11)
+//     (clamped to [-120, 120], so that 2^E_n and 2^-E_n are normal floats),
+//     then every group's (fp16(s * 2^-E_n), fp16(z * 2^-E_n)) pair into sz
+//     and 2^E_n into colscale (bf16 bits).  (q - 8) s' + z' is then at most
+//     8 * 2^11 + 2^11 in magnitude.
+constexpr int kPrepThreads = 256, kA16Cache = 8;
 
 __device__ __forceinline__ float absmax_bf16x8(const uint4& v)
 {
@@ -730,13 +738,9 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v, float inv)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(kA16Threads) a_to_f16_kernel(const uint16_t* __restrict__ A,
-                                                               uint16_t* __restrict__ A16,
-                                                               float* __restrict__ rowscale, int m, int k)
+__device__ __forceinline__ void prep_a_row(const uint16_t* __restrict__ A, uint16_t* __restrict__ A16,
+                                           float* __restrict__ rowscale, int row, int k)
 {
-    const int row = blockIdx.x;
-    if (row >= m)
-        return;
     const uint4* a = reinterpret_cast<const uint4*>(A + (size_t)row * k);
     uint4* o = reinterpret_cast<uint4*>(A16 + (size_t)row * k);
     const int nch = k >> 3;  // chunks of 8 values
@@ -744,13 +748,13 @@ __global__ void __launch_bounds__(kA16Threads) a_to_f16_kernel(const uint16_t* _
     float mx = 0.f;
 #pragma unroll
     for (int i = 0; i < kA16Cache; ++i) {
-        const int j = (int)threadIdx.x + i * kA16Threads;
+        const int j = (int)threadIdx.x + i * kPrepThreads;
         if (j < nch) {
             c[i] = __ldg(a + j);
             mx = fmaxf(mx, absmax_bf16x8(c[i]));
         }
     }
-    for (int j = (int)threadIdx.x + kA16Cache * kA16Threads; j < nch; j += kA16Threads)
+    for (int j = (int)threadIdx.x + kA16Cache * kPrepThreads; j < nch; j += kPrepThreads)
         mx = fmaxf(mx, absmax_bf16x8(__ldg(a + j)));
     __shared__ float red[32];
     for (int s = 16; s > 0; s >>= 1)
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(kA16Threads) a_to_f16_kernel(const uint16_t* _
         red[threadIdx.x >> 5] = mx;
     __syncthreads();
     if (threadIdx.x < 32) {
-        float v = threadIdx.x < (kA16Threads >> 5) ? red[threadIdx.x] : 0.f;
+        float v = threadIdx.x < (kPrepThreads >> 5) ? red[threadIdx.x] : 0.f;
         for (int s = 16; s > 0; s >>= 1)
             v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, s));
         if (threadIdx.x == 0)
@@ -776,14 +780,61 @@ __global__ void __launch_bounds__(kA16Threads) a_to_f16_kernel(const uint16_t* _
     const float inv = ldexpf(1.f, -E);
 #pragma unroll
     for (int i = 0; i < kA16Cache; ++i) {
-        const int j = (int)threadIdx.x + i * kA16Threads;
+        const int j = (int)threadIdx.x + i * kPrepThreads;
         if (j < nch)
             o[j] = bf16x8_to_f16x8(c[i], inv);
     }
-    for (int j = (int)threadIdx.x + kA16Cache * kA16Threads; j < nch; j += kA16Threads)
+    for (int j = (int)threadIdx.x + kA16Cache * kPrepThreads; j < nch; j += kPrepThreads)
         o[j] = bf16x8_to_f16x8(__ldg(a + j), inv);
     if (threadIdx.x == 0)
         rowscale[row] = ldexpf(1.f, E);
+}
+
+template <int ACT>
+__device__ __forceinline__ void prep_channel(const uint16_t* __restrict__ scales,
+                                             const uint16_t* __restrict__ zeros, int ch, int G,
+                                             uint32_t* __restrict__ sz, uint16_t* __restrict__ colscale,
+                                             int lane)
+{
+    const uint16_t* s = scales + (size_t)ch * G;
+    const uint16_t* z = zeros ? zeros + (size_t)ch * G : nullptr;
+    float mx = 0.f;
+    for (int g = lane; g < G; g += 32) {
+        mx = fmaxf(mx, fabsf(to_f32<ACT>(ld_nc_u16(s + g))));
+        if (z)
+            mx = fmaxf(mx, fabsf(to_f32<ACT>(ld_nc_u16(z + g))));
+    }
+    for (int o = 16; o > 0; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int E = 0;
+    if (mx > 0.f && mx <= 3.0e38f) {
+        int e2;
+        frexpf(mx, &e2);  // mx in [2^(e2 - 1), 2^e2)
+        E = min(max(e2 - 11, -120), 120);
+    }
+    const float inv = __int_as_float((127 - E) << 23);  // 2^-E, a normal float
+    for (int g = lane; g < G; g += 32) {
+        const uint32_t sv = from_f32<ACT_F16>(to_f32<ACT>(ld_nc_u16(s + g)) * inv);
+        const uint32_t zv = z ? from_f32<ACT_F16>(to_f32<ACT>(ld_nc_u16(z + g)) * inv) : 0u;
+        sz[(size_t)ch * G + g] = sv | (zv << 16);
+    }
+    if (lane == 0)
+        colscale[ch] = (uint16_t)((127 + E) << 7);  // 2^E as bf16
+}
+
+template <int ACT>
+__global__ void __launch_bounds__(kPrepThreads)
+    tc_prep_kernel(const uint16_t* __restrict__ A, uint16_t* __restrict__ A16, float* __restrict__ rowscale,
+                   int a_ctas, int k, const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
+                   int n, int G, uint32_t* __restrict__ sz, uint16_t* __restrict__ colscale)
+{
+    if ((int)blockIdx.x < a_ctas) {
+        prep_a_row(A, A16, rowscale, (int)blockIdx.x, k);
+        return;
+    }
+    const int ch = ((int)blockIdx.x - a_ctas) * (kPrepThreads / 32) + (int)(threadIdx.x >> 5);
+    if (ch < n)
+        prep_channel<ACT>(scales, zeros, ch, G, sz, colscale, (int)(threadIdx.x & 31));
 }
 
 // Output tile shape: MS sub-tiles of 128 rows by BN columns, the one whose
@@ -1185,7 +1236,7 @@ cudaError_t launch_moe_tc_t(const CUtensorMap& ma, const CUtensorMap& mc, const 
 
 }  // namespace
 
-TcPlan plan_tc(int m, int n, int k, int bits, int act, bool allow_split)
+TcPlan plan_tc(int m, int n, int k, int group, int bits, int act, bool allow_split)
 {
     TcPlan p{};
     const TcShape sh = tc_shape(m, n, bits);
@@ -1217,9 +1268,12 @@ TcPlan plan_tc(int m, int n, int k, int bits, int act, bool allow_split)
     const long long tiles = (long long)((m + BM * p.ms - 1) / (BM * p.ms)) * ((n + p.bn - 1) / p.bn);
     p.a16_bytes = (bits == 4 && act == WO_BF16) ? align_up((size_t)m * k * 2, 256) : 0;
     p.rowscale_bytes = p.a16_bytes ? align_up((size_t)m * 4, 256) : 0;
+    p.sz_bytes = bits == 4 ? align_up((size_t)n * (size_t)(k / group) * 4, 256) : 0;
+    p.colscale_bytes = bits == 4 ? align_up((size_t)n * 2, 256) : 0;
     p.partial_bytes =
         p.splits > 1 ? align_up((size_t)tiles * p.splits * BM * p.ms * p.bn * 4, 256) : 0;
-    p.ws_bytes = kWsScratch + p.a16_bytes + p.rowscale_bytes + p.partial_bytes;
+    p.ws_bytes = kWsScratch + p.a16_bytes + p.rowscale_bytes + p.sz_bytes + p.colscale_bytes +
+                 p.partial_bytes;
     return p;
 }
 
@@ -1232,7 +1286,6 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     tp.k = a.k;
     tp.num_kb = a.k / BK;
     tp.scales = static_cast<const uint16_t*>(a.scales);
-    tp.zeros = static_cast<const uint16_t*>(a.zeros);
     tp.bias = static_cast<const uint16_t*>(a.bias);
     tp.C = static_cast<uint16_t*>(a.C);
     tp.G = a.k / a.group;
@@ -1241,22 +1294,38 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     tp.err = reinterpret_cast<unsigned*>(ws);
     tp.splits = plan.splits;
     tp.counters = reinterpret_cast<unsigned*>(ws + kWsHeader);
-    tp.partial = plan.splits > 1
-                     ? reinterpret_cast<float*>(ws + kWsScratch + plan.a16_bytes + plan.rowscale_bytes)
-                     : nullptr;
+    // scratch after the header and counters: [A16][rowscale][sz][colscale][partials]
+    char* const a16_at = ws + kWsScratch;
+    char* const rs_at = a16_at + plan.a16_bytes;
+    char* const sz_at = rs_at + plan.rowscale_bytes;
+    char* const cs_at = sz_at + plan.sz_bytes;
+    char* const part_at = cs_at + plan.colscale_bytes;
+    tp.partial = plan.splits > 1 ? reinterpret_cast<float*>(part_at) : nullptr;
     // stream the larger operand once (A: m*k*2 bytes, codes: n*k*bits/8)
     tp.m_fast = (double)a.m * 2.0 <= (double)a.n * a.bits / 8.0;
 
     const void* Aop = a.A;
-    if (plan.a16_bytes) {
-        uint16_t* A16 = reinterpret_cast<uint16_t*>(ws + kWsScratch);
-        float* rsc = reinterpret_cast<float*>(ws + kWsScratch + plan.a16_bytes);
-        a_to_f16_kernel<<<a.m, kA16Threads, 0, s>>>(static_cast<const uint16_t*>(a.A), A16, rsc, a.m, a.k);
+    if (a.bits == 4) {
+        // the prepass: channel scales into fp16 range (and bf16 A into fp16)
+        const int a_ctas = plan.a16_bytes ? a.m : 0;
+        uint16_t* A16 = reinterpret_cast<uint16_t*>(a16_at);
+        float* rsc = reinterpret_cast<float*>(rs_at);
+        tp.sz = reinterpret_cast<const uint32_t*>(sz_at);
+        tp.colscale = reinterpret_cast<const uint16_t*>(cs_at);
+        const int ctas = a_ctas + (a.n + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+        auto prep = a.act == WO_F16 ? tc_prep_kernel<ACT_F16> : tc_prep_kernel<ACT_BF16>;
+        prep<<<ctas, kPrepThreads, 0, s>>>(static_cast<const uint16_t*>(a.A), A16, rsc, a_ctas, a.k,
+                                            static_cast<const uint16_t*>(a.scales),
+                                            static_cast<const uint16_t*>(a.zeros), a.n, tp.G,
+                                            reinterpret_cast<uint32_t*>(sz_at),
+                                            reinterpret_cast<uint16_t*>(cs_at));
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;
-        Aop = A16;
-        tp.rowscale = rsc;
+        if (a_ctas) {
+            Aop = A16;
+            tp.rowscale = rsc;
+        }
     }
     const int OT = a.bits == 4 ? WO_F16 : a.act;
     CUtensorMap ma;

@@ -70,12 +70,15 @@ struct TcPlan {
     int splits;             // k split (units per tile); 1: none
     size_t a16_bytes;       // fp16 copy of a bf16 A (4-bit weights only)
     size_t rowscale_bytes;  // its per-row power-of-two scales
+    size_t sz_bytes;        // 4-bit: pre-scaled fp16 (scale, zero) pairs [n, G]
+    size_t colscale_bytes;  // 4-bit: per-channel powers of two [n] (bf16 bits)
     size_t partial_bytes;   // k split: fp32 partial tiles
     size_t ws_bytes;        // total, header and counter area included
 };
 
 // allow_split = false plans without the k split (no partial-tile scratch).
-TcPlan plan_tc(int m, int n, int k, int bits, int act, bool allow_split = true);
+// group: codes per scale group along k (k for per-channel).
+TcPlan plan_tc(int m, int n, int k, int group, int bits, int act, bool allow_split = true);
 cudaError_t launch_tc(const GemmArgs& a, const TcPlan& p, cudaStream_t s);
 
 // MoE expert GEMMs on the tensor cores (8-bit codes; hidden and inter

@@ -7,9 +7,10 @@
 // cudaMalloc (which can synchronise the whole device).  They pass inputs and
 // outputs only.
 //
-// The scratch (error word, fp16 copy of bf16 activations and their row
-// scales) lives in g_scratch below; every GPU that loads this library keeps
-// it (16.31 MiB) until the process exits.  Host code cannot use g_scratch's
+// The scratch (error word; for 4-bit weights the per-channel pre-scaled
+// scale and zero pairs and column scales, and with bf16 activations the
+// fp16 copy of A and its row scales) lives in g_scratch below; every GPU
+// that loads this library keeps it (24.06 MiB) until the process exits.  Host code cannot use g_scratch's
 // name as a device address: each call looks the address up with
 // cudaGetSymbolAddress in the caller's current context (a host-side table
 // lookup), so a context other than the device's primary one, or a primary
@@ -33,10 +34,13 @@ namespace wo {
 namespace {
 
 // Size of the built-in scratch: the 64.25 KiB header area every tensor-core
-// call uses, plus 16 MiB for the fp16 copy of bf16 activations (m * k * 2
-// bytes, 4-bit weights only) and 256 KiB for its row scales (m * 4 bytes),
-// e.g. m * k <= 8,388,608 with m <= 65,536.
-constexpr size_t kNoAllocBytes = kWsScratch + ((size_t)16 << 20) + ((size_t)256 << 10);
+// call uses, plus 24 MiB for the per-call scratch of 4-bit weights: the
+// pre-scaled scale and zero pairs (n * (k / group) * 4 bytes), the column
+// scales (n * 2 bytes) and, with bf16 activations, the fp16 copy of A
+// (m * k * 2 bytes) and its row scales (m * 4 bytes), each rounded up to
+// 256 bytes.  8-bit weights need none of it.
+constexpr size_t kNoAllocExtra = (size_t)24 << 20;
+constexpr size_t kNoAllocBytes = kWsScratch + kNoAllocExtra;
 
 static __device__ __align__(256) unsigned char g_scratch[kNoAllocBytes];
 
@@ -123,9 +127,8 @@ extern "C" wo_status wo_gemm_tc_noalloc(const void* A, const uint8_t* B_packed,
         !aligned16(C) || !aligned2(scales) || (zeros && !aligned2(zeros)) ||
         (bias && !aligned2(bias)))
         return WO_ERR_INVALID_ARG;
-    const TcPlan plan = plan_tc(m, n, k, bits, act_dtype, false);  // no k split: no partial tiles
-    if (plan.a16_bytes > ((size_t)16 << 20) || plan.rowscale_bytes > ((size_t)256 << 10) ||
-        plan.ws_bytes > kNoAllocBytes)
+    const TcPlan plan = plan_tc(m, n, k, g, bits, act_dtype, false);  // no k split: no partial tiles
+    if (plan.ws_bytes > kNoAllocBytes)
         return WO_ERR_WORKSPACE;  // the problem needs more scratch than is built in
     void* scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess)

@@ -108,9 +108,12 @@ WO_API size_t wo_workspace_size(int m, int n, int k, int group_size, int bits);
  *   bits 8: group_size -1 or k (per channel), zeros NULL.
  *   bits 4: group_size 64 or 128 (a multiple of 64 dividing k), or -1/k.
  * Requires n % 64 == 0, k % 64 == 0 and k > 0; m == 0 or n == 0 is a no-op.
- * The kernel is chosen by m: a split-K weight-streaming kernel for small m,
- * a tcgen05 tensor-core kernel for large m.  Results are deterministic:
- * identical inputs give bit-identical C.
+ * The kernel is chosen by m: for 4-bit weights at decode-sized m (1..16)
+ * a persistent weight-streaming kernel (group-wise weights also need
+ * 16-byte aligned scales and zeros and k / group_size a multiple of 8), else
+ * up to m = 64 a cluster-split weight-streaming kernel, and a tcgen05
+ * tensor-core kernel for larger m (wo_gemm_plan reports the choice).  Results are deterministic: identical inputs give
+ * bit-identical C.
  * Ordering: the small-m kernel uses programmatic dependent launch.  It may
  * start reading B_packed, scales, zeros and bias while the previous
  * operation on the stream is still running, so those must not be written by
@@ -130,13 +133,19 @@ WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* sca
  * Pure host code: no CUDA call beyond reading the device's SM count (152
  * when no device is visible).
  */
-typedef enum { WO_KERNEL_STREAM = 0, WO_KERNEL_TENSOR_CORE = 1 } wo_kernel;
+typedef enum {
+    WO_KERNEL_STREAM = 0,            /* cluster-split weight streaming (m <= 64) */
+    WO_KERNEL_TENSOR_CORE = 1,       /* tcgen05 tensor cores (m >= 65) */
+    WO_KERNEL_STREAM_PERSISTENT = 2  /* persistent weight streaming (4-bit, m <= 16) */
+} wo_kernel;
 
 typedef struct {
-    wo_kernel kernel;      /* weight streaming (small m) or tensor cores */
+    wo_kernel kernel;      /* which kernel family runs */
     int tile_m;            /* rows of C per CTA tile (streaming: m) */
-    int tile_n;            /* output channels per CTA tile */
-    int k_splits;          /* CTAs (streaming: one cluster) or units per tile along k */
+    int tile_n;            /* output channels per CTA tile (persistent: per strip) */
+    int k_splits;          /* CTAs of one cluster (streaming), units per tile along k
+                              (tensor cores), or the most pieces one strip's k range is
+                              cut into across CTAs (persistent) */
     int ctas;              /* CTAs launched */
     int stages;            /* streaming: shared-memory ring stages per CTA; else 0 */
     size_t workspace_bytes; /* == wo_workspace_size */

@@ -26,11 +26,14 @@ int main(void)
     CHECK(wo_packed_bytes(100, 512, 8) == 0);
     CHECK(strcmp(wo_status_string(WO_ERR_WORKSPACE), "WO_ERR_WORKSPACE") == 0);
 
-    /* the plan: decode on the weight-streaming kernel, large m on tensor cores */
+    /* the plan: decode on the weight-streaming kernels (4-bit: the persistent
+       one), large m on tensor cores */
     wo_gemm_plan_t p;
     CHECK(wo_gemm_plan(1, 4608, 3584, -1, 8, WO_F16, &p) == WO_OK);
     CHECK(p.kernel == WO_KERNEL_STREAM && p.tile_m == 1 && p.ctas > 0);
     CHECK(p.workspace_bytes == wo_workspace_size(1, 4608, 3584, -1, 8));
+    CHECK(wo_gemm_plan(1, 131072, 2048, 64, 4, WO_BF16, &p) == WO_OK);
+    CHECK(p.kernel == WO_KERNEL_STREAM_PERSISTENT && p.tile_n == 256 && p.ctas > 0);
     CHECK(wo_gemm_plan(4096, 4096, 4096, -1, 8, WO_F16, &p) == WO_OK);
     CHECK(p.kernel == WO_KERNEL_TENSOR_CORE && p.tile_m == 256 && p.tile_n == 256);
     CHECK(wo_gemm_plan(4, 256, 512, 64, 8, WO_F16, &p) == WO_ERR_UNSUPPORTED);

@@ -88,6 +88,41 @@ def test_small_shapes(wo, m, n, k, bits, group, act, zeros, bias):
     _check_full(DeviceCase(c), f"m{m} n{n} k{k} w{bits} g{group}")
 
 
+# 4-bit decode sizes (m <= 16) run the persistent kernel: strips of 256 channels
+# (the last one partly past n), stages of 128 codes (a half stage at the end
+# when k % 128 == 64), strips cut into pieces across CTAs when there are few
+# of them (summed through the workspace by the last piece to arrive)
+PERSISTENT = [
+    # m, n, k, bits, group, act, zeros, bias
+    (8, 320, 2048, 4, 64, inputs.F16, True, True),       # 8 rows: one activation row block
+    (9, 320, 2048, 4, 64, inputs.BF16, True, True),      # 9 rows: two
+    (1, 320, 2048, 4, 64, inputs.BF16, True, False),     # one row: tiles spread over columns
+    (1, 2112, 4096, 4, 128, inputs.F16, True, True),     # one row, group 128
+    (1, 192, 704, 4, -1, inputs.F16, True, True),        # one row, per channel, k % 128 == 64
+    (12, 448, 4096, 4, 64, inputs.BF16, True, True),
+    (16, 192, 8192, 4, 128, inputs.F16, True, False),    # group 128, few strips, long k
+    (1, 704, 1536, 4, 64, inputs.F16, False, True),      # no zeros
+    (3, 128, 576, 4, -1, inputs.BF16, True, True),       # per channel, k % 128 == 64
+    (1, 64, 11776, 4, 64, inputs.BF16, True, False),     # one strip over many CTAs
+    (2, 4160, 192, 4, -1, inputs.F16, True, True),       # many strips, 2 stages each
+    (7, 2368, 3136, 4, 64, inputs.BF16, True, True),     # k % 512 == 64: the cluster kernel
+]
+
+
+@pytest.mark.parametrize("m,n,k,bits,group,act,zeros,bias", PERSISTENT)
+def test_persistent_decode_shapes(wo, m, n, k, bits, group, act, zeros, bias):
+    c = inputs.make_gemm_case(14, m + n + k, m, n, k, bits=bits, group_size=group, act_dtype=act,
+                              scale_lo=0.005 if bits == 4 else 0.001,
+                              scale_hi=0.02 if bits == 4 else 0.01, with_zeros=zeros,
+                              with_bias=bias)
+    dc = DeviceCase(c)
+    _check_full(dc, f"decode m{m} n{n} k{k} w{bits} g{group}")
+    C1 = dc.run().clone()
+    C2 = dc.run()
+    torch.cuda.synchronize()
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))  # pieces summed in k order
+
+
 @pytest.mark.parametrize("m,n,k,group", [(1, 128, 16384, -1), (4, 256, 16384, 64), (2, 128, 8192, -1)])
 def test_w4_nonnegative_activations_long_groups(wo, m, n, k, group):
     # 4-bit codes with bf16 activations that are all >= 0 (as after a gated

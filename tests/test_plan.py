@@ -44,15 +44,18 @@ def test_tensor_core_tile_configurations(m, n, k, bits, group, tile, splits):
 
 @pytest.mark.parametrize("bits,group", [(8, -1), (4, 64), (4, 128), (4, -1)])
 def test_kernel_choice_by_m(bits, group):
+    # 4-bit decode runs the persistent kernel; 8-bit decode stays on the
+    # cluster-split one, which measured faster for every 8-bit decode shape
     n, k = 512, 2048
-    for m, kern in [(1, "stream"), (16, "stream"), (17, "stream"), (64, "stream"),
-                    (65, "tensor_core"), (256, "tensor_core")]:
+    small = "stream_persistent" if bits == 4 else "stream"
+    for m, kern in [(1, small), (16, small), (17, "stream"),
+                    (64, "stream"), (65, "tensor_core"), (256, "tensor_core")]:
         assert wo.gemm_plan(m, n, k, bits, group)["kernel"] == kern, (m, bits, group)
 
 
-@pytest.mark.parametrize("m,n,k,bits,group", [(1, 4608, 3584, 8, -1), (4, 3584, 18944, 8, -1),
-                                              (16, 37888, 3584, 8, -1), (1, 2048, 13312, 4, 64),
-                                              (1, 131072, 2048, 4, 64), (48, 3584, 3584, 8, -1)])
+@pytest.mark.parametrize("m,n,k,bits,group", [(24, 4608, 3584, 8, -1), (32, 3584, 18944, 8, -1),
+                                              (24, 37888, 3584, 8, -1), (20, 2048, 13312, 4, 64),
+                                              (64, 131072, 2048, 4, 64), (48, 3584, 3584, 8, -1)])
 def test_stream_plans_fill_one_resident_wave(m, n, k, bits, group):
     p = wo.gemm_plan(m, n, k, bits, group, wo.WO_F16)
     assert p["kernel"] == "stream" and p["tile_m"] == m
@@ -62,6 +65,40 @@ def test_stream_plans_fill_one_resident_wave(m, n, k, bits, group):
     if p["k_splits"] > 1:                             # splits only up to two CTAs per SM
         assert p["ctas"] <= 2 * SMS
     assert p["stages"] >= 1 and p["workspace_bytes"] == 256
+
+
+@pytest.mark.parametrize("m,n,k,bits,group", [(1, 4608, 3584, 4, -1), (4, 3584, 18944, 4, 64),
+                                              (16, 37888, 3584, 4, 64), (1, 2048, 13312, 4, 64),
+                                              (1, 131072, 2048, 4, 64), (9, 256, 1024, 4, 128),
+                                              (3, 192, 320, 4, -1), (2, 128, 512, 4, -1)])
+def test_persistent_plans_split_the_weights_evenly(m, n, k, bits, group):
+    # decode sizes: strips of 256 channels by stages of 128 codes, the
+    # strip-major units divided evenly over two CTAs per SM (fewer when there
+    # are fewer units); pieces of a strip that several CTAs share sum through
+    # the workspace after the header and counter area
+    p = wo.gemm_plan(m, n, k, bits, group, wo.WO_BF16)
+    assert p["kernel"] == "stream_persistent" and p["tile_m"] == m and p["tile_n"] == 256
+    units = -(-n // 256) * -(-k // 128)
+    assert p["ctas"] == min(units, 2 * SMS)
+    q = units // p["ctas"]
+    nst = -(-k // 128)
+    assert 1 <= p["k_splits"] <= nst
+    assert p["k_splits"] >= min(nst, -(-nst // max(q, 1)))  # room for every piece
+    assert p["stages"] >= 2
+    mt = 1 if m <= 8 else 2
+    partial = -(-n // 256) * p["k_splits"] * 256 * (8 * mt) * 4
+    assert p["workspace_bytes"] == 256 + 65536 + -(-partial // 256) * 256
+
+
+def test_grouped_4bit_decode_with_unaligned_row_of_groups_uses_the_cluster_kernel():
+    # scale boxes of 8 groups need k / group to be a multiple of 8
+    p = wo.gemm_plan(1, 256, 320, 4, 64)
+    assert p["kernel"] == "stream"
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 4608, 3584), (4, 3584, 18944), (16, 37888, 3584)])
+def test_8bit_decode_uses_the_cluster_kernel(m, n, k):
+    assert wo.gemm_plan(m, n, k, 8, -1, wo.WO_F16)["kernel"] == "stream"
 
 
 def test_plan_argument_rules():

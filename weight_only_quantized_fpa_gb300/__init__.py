@@ -205,7 +205,8 @@ def gemm_plan(m: int, n: int, k: int, bits: int, group_size: int = -1,
               act_dtype: int = WO_BF16) -> dict:
     """The configuration wo_gemm runs for this problem, as a dict."""
     p = wo_gemm_plan(m, n, k, group_size, bits, act_dtype)
-    return {"kernel": "tensor_core" if p.kernel == 1 else "stream", "tile_m": p.tile_m,
+    kernel = {0: "stream", 1: "tensor_core", 2: "stream_persistent"}[int(p.kernel)]
+    return {"kernel": kernel, "tile_m": p.tile_m,
             "tile_n": p.tile_n, "k_splits": p.k_splits, "ctas": p.ctas, "stages": p.stages,
             "workspace_bytes": int(p.workspace_bytes)}
 

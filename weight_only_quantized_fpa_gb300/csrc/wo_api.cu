@@ -3,6 +3,8 @@
 // arguments return a status with nothing enqueued.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -69,6 +71,36 @@ bool use_tc(int m, int n, int k, int group_size, int bits)
     return m >= kTcMinM || !stream_supported(m, n, k, norm_group(group_size, k), bits);
 }
 
+// Below the tensor-core sizes, decode-sized m (1..16) runs the persistent
+// kernel (wo_gemv.cu) when its plan exists and, for group-wise 4-bit weights,
+// the scales and zeros are 16-byte aligned (they are fetched by TMA); the
+// other cases run the cluster-split streaming kernel (wo_stream.cu).  The
+// environment variable WO_DECODE_KERNEL=stream forces the latter (an A/B
+// switch for measurements; both kernels give results within tolerance, but
+// not bit-identical ones).
+bool decode_forced_stream()
+{
+    static const bool forced = [] {
+        const char* v = std::getenv("WO_DECODE_KERNEL");
+        return v && std::strcmp(v, "stream") == 0;
+    }();
+    return forced;
+}
+
+bool use_gemv_shape(int m, int n, int k, int group, int bits)
+{
+    return m >= 1 && m <= 16 && !decode_forced_stream() && gemv_supported(m, n, k, group, bits);
+}
+
+bool use_gemv(const GemmArgs& a)
+{
+    if (!use_gemv_shape(a.m, a.n, a.k, a.group, a.bits))
+        return false;
+    if (a.bits == 4 && a.group != a.k)
+        return aligned(a.scales, 16) && (!a.zeros || aligned(a.zeros, 16));
+    return true;
+}
+
 }  // namespace
 }  // namespace wo
 
@@ -130,7 +162,11 @@ size_t wo_workspace_size(int m, int n, int k, int group_size, int bits)
         // the larger of the two activation dtypes' needs
         return plan_tc(m, n, k, norm_group(group_size, k), bits, WO_BF16).ws_bytes;
     }
-    return stream_workspace_bytes();
+    // either small-m kernel may run (the persistent one needs its partial sums)
+    const size_t gv = use_gemv_shape(m, n, k, norm_group(group_size, k), bits)
+                          ? gemv_workspace_bytes(m, n, k, norm_group(group_size, k), bits)
+                          : 0;
+    return gv > stream_workspace_bytes() ? gv : stream_workspace_bytes();
 }
 
 // Argument checks of wo_gemm, with `ws_need` the workspace the GEMM itself
@@ -180,6 +216,8 @@ static wo_status gemm_launch(const GemmArgs& a, cudaStream_t s)
 {
     if (use_tc(a.m, a.n, a.k, a.group, a.bits))
         return cuda_status(launch_tc(a, plan_tc(a.m, a.n, a.k, a.group, a.bits, a.act), s));
+    if (use_gemv(a))
+        return cuda_status(launch_gemv(a, s));
     return cuda_status(launch_stream_gemm(a, s));
 }
 
@@ -220,6 +258,17 @@ wo_status wo_gemm_plan(int m, int n, int k, int group_size, int bits, wo_dtype a
         plan->tile_n = p.bn;
         plan->k_splits = p.splits;
         plan->ctas = (int)(units < num_sms() ? units : num_sms());
+        return WO_OK;
+    }
+    if (use_gemv_shape(m, n, k, g, bits)) {
+        // (group-wise 4-bit with scales not 16-byte aligned runs WO_KERNEL_STREAM)
+        const GemvInfo gi = gemv_info(m, n, k, g, bits);
+        plan->kernel = WO_KERNEL_STREAM_PERSISTENT;
+        plan->tile_m = m;
+        plan->tile_n = gi.strip_channels;
+        plan->k_splits = gi.max_pieces;
+        plan->ctas = gi.ctas;
+        plan->stages = gi.stages;
         return WO_OK;
     }
     const StreamPlan p = plan_stream(m, n, k, g, bits, OUT_PLAIN, 0);

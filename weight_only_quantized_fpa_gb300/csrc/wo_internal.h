@@ -62,6 +62,15 @@ size_t stream_workspace_bytes();
 bool stream_supported(int m, int n, int k, int group, int bits);
 cudaError_t launch_stream_gemm(const GemmArgs& a, cudaStream_t s);
 
+// decode-sized m (1..16): the persistent weight-streaming kernel (wo_gemv.cu)
+struct GemvInfo {
+    int ctas, stages, strip_channels, max_pieces;
+};
+bool gemv_supported(int m, int n, int k, int group, int bits);
+size_t gemv_workspace_bytes(int m, int n, int k, int group, int bits);  // 0 when unsupported
+GemvInfo gemv_info(int m, int n, int k, int group, int bits);
+cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t s);
+
 // ---- tensor-core kernel (large m) -----------------------------------------
 constexpr int kTcMinM = 65;  // m at and above which wo_gemm uses the tensor-core kernel
 

@@ -3,6 +3,10 @@ inputs: element by element at sizes the oracle finishes in seconds, and on
 sampled rows at the workloads' full sizes, in the launch configuration the
 bench times.  Tolerance (fp outputs): rel-L2 <= 2e-3 and
 max |C - C_ref| <= 1e-2 * max |C_ref| against the fp64 oracle."""
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 
@@ -88,10 +92,13 @@ def test_small_shapes(wo, m, n, k, bits, group, act, zeros, bias):
     _check_full(DeviceCase(c), f"m{m} n{n} k{k} w{bits} g{group}")
 
 
-# 4-bit decode sizes (m <= 16) run the persistent kernel: strips of 256 channels
-# (the last one partly past n), stages of 128 codes (a half stage at the end
-# when k % 128 == 64), strips cut into pieces across CTAs when there are few
-# of them (summed through the workspace by the last piece to arrive)
+# 4-bit decode sizes (m <= 16): the persistent kernel's edge cases.  Strips of
+# 256 channels (the last one partly past n), stages of 128 codes (a half
+# stage at the end when k % 128 == 64), strips cut into pieces across CTAs
+# when there are few of them (summed through the workspace by the last
+# piece to arrive).  The automatic choice sends many of these shapes to the
+# cluster kernel; test_decode_shapes_on_the_persistent_kernel runs them all
+# again with the persistent kernel forced.
 PERSISTENT = [
     # m, n, k, bits, group, act, zeros, bias
     (8, 320, 2048, 4, 64, inputs.F16, True, True),       # 8 rows: one activation row block
@@ -105,12 +112,15 @@ PERSISTENT = [
     (3, 128, 576, 4, -1, inputs.BF16, True, True),       # per channel, k % 128 == 64
     (1, 64, 11776, 4, 64, inputs.BF16, True, False),     # one strip over many CTAs
     (2, 4160, 192, 4, -1, inputs.F16, True, True),       # many strips, 2 stages each
-    (7, 2368, 3136, 4, 64, inputs.BF16, True, True),     # k % 512 == 64: the cluster kernel
+    (4, 320, 16384, 4, 64, inputs.BF16, True, True),     # persistent by the automatic choice
+    (7, 2368, 3136, 4, 64, inputs.BF16, True, True),     # k / 64 not a multiple of 8: cluster kernel
 ]
 
 
 @pytest.mark.parametrize("m,n,k,bits,group,act,zeros,bias", PERSISTENT)
-def test_persistent_decode_shapes(wo, m, n, k, bits, group, act, zeros, bias):
+def test_decode_shapes(wo, m, n, k, bits, group, act, zeros, bias):
+    if os.environ.get("WO_DECODE_KERNEL") == "persistent" and (group == -1 or (k // group) % 8 == 0):
+        assert wo.gemm_plan(m, n, k, bits, group, act)["kernel"] == "stream_persistent"
     c = inputs.make_gemm_case(14, m + n + k, m, n, k, bits=bits, group_size=group, act_dtype=act,
                               scale_lo=0.005 if bits == 4 else 0.001,
                               scale_hi=0.02 if bits == 4 else 0.01, with_zeros=zeros,
@@ -121,6 +131,20 @@ def test_persistent_decode_shapes(wo, m, n, k, bits, group, act, zeros, bias):
     C2 = dc.run()
     torch.cuda.synchronize()
     assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))  # pieces summed in k order
+
+
+def test_decode_shapes_on_the_persistent_kernel(wo):
+    # the decode cases again, in a process whose wo_gemm always takes the
+    # persistent kernel where it applies (the choice is read once per process)
+    if os.environ.get("WO_DECODE_KERNEL"):
+        pytest.skip("already forced")
+    env = dict(os.environ, WO_DECODE_KERNEL="persistent")
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.abspath(__file__), "-q", "-m", "gpu",
+                        "-p", "no:cacheprovider", "-k", "test_decode_shapes and not persistent_kernel"],
+                       env=env, capture_output=True, text=True, timeout=600,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    assert "passed" in r.stdout
 
 
 @pytest.mark.parametrize("m,n,k,group", [(1, 128, 16384, -1), (4, 256, 16384, 64), (2, 128, 8192, -1)])

@@ -44,13 +44,29 @@ def test_tensor_core_tile_configurations(m, n, k, bits, group, tile, splits):
 
 @pytest.mark.parametrize("bits,group", [(8, -1), (4, 64), (4, 128), (4, -1)])
 def test_kernel_choice_by_m(bits, group):
-    # 4-bit decode runs the persistent kernel; 8-bit decode stays on the
-    # cluster-split one, which measured faster for every 8-bit decode shape
     n, k = 512, 2048
-    small = "stream_persistent" if bits == 4 else "stream"
-    for m, kern in [(1, small), (16, small), (17, "stream"),
+    for m, kern in [(1, "stream"), (16, "stream"), (17, "stream"),
                     (64, "stream"), (65, "tensor_core"), (256, "tensor_core")]:
         assert wo.gemm_plan(m, n, k, bits, group)["kernel"] == kern, (m, bits, group)
+
+
+@pytest.mark.parametrize("n,k,group,persistent", [
+    (131072, 2048, 64, True),   # the cluster kernel would need 512 CTAs: more than one wave
+    (2048, 13312, 64, True),    # 128 cluster CTAs of 106 KB each: SMs left idle
+    (2048, 13312, 128, True),
+    (131072, 2048, -1, True),
+    (13312, 2048, 64, False),   # 208 CTAs in one wave
+    (2048, 2048, 64, False),    # 2 MB of weights: the cluster kernel's shorter critical path
+    (3072, 2048, -1, False)])
+def test_4bit_decode_kernel_choice(n, k, group, persistent):
+    # 4-bit decode sizes take the persistent kernel where the cluster-split
+    # one cannot keep the GPU busy; 8-bit decode always stays on the latter,
+    # and so does m = 17
+    for m in (1, 16):
+        want = "stream_persistent" if persistent else "stream"
+        assert wo.gemm_plan(m, n, k, 4, group)["kernel"] == want, (m, n, k)
+        assert wo.gemm_plan(m, n, k, 8, -1)["kernel"] == "stream"
+    assert wo.gemm_plan(17, n, k, 4, group)["kernel"] == "stream"
 
 
 @pytest.mark.parametrize("m,n,k,bits,group", [(24, 4608, 3584, 8, -1), (32, 3584, 18944, 8, -1),
@@ -67,10 +83,10 @@ def test_stream_plans_fill_one_resident_wave(m, n, k, bits, group):
     assert p["stages"] >= 1 and p["workspace_bytes"] == 256
 
 
-@pytest.mark.parametrize("m,n,k,bits,group", [(1, 4608, 3584, 4, -1), (4, 3584, 18944, 4, 64),
-                                              (16, 37888, 3584, 4, 64), (1, 2048, 13312, 4, 64),
-                                              (1, 131072, 2048, 4, 64), (9, 256, 1024, 4, 128),
-                                              (3, 192, 320, 4, -1), (2, 128, 512, 4, -1)])
+@pytest.mark.parametrize("m,n,k,bits,group", [(1, 2048, 13312, 4, 64), (4, 1024, 18944, 4, 64),
+                                              (16, 131072, 2048, 4, 128), (1, 131072, 2048, 4, 64),
+                                              (9, 256, 16384, 4, 128), (3, 320, 16384, 4, -1),
+                                              (2, 64, 65536, 4, 64)])
 def test_persistent_plans_split_the_weights_evenly(m, n, k, bits, group):
     # decode sizes: strips of 256 channels by stages of 128 codes, the
     # strip-major units divided evenly over two CTAs per SM (fewer when there
@@ -84,7 +100,7 @@ def test_persistent_plans_split_the_weights_evenly(m, n, k, bits, group):
     nst = -(-k // 128)
     assert 1 <= p["k_splits"] <= nst
     assert p["k_splits"] >= min(nst, -(-nst // max(q, 1)))  # room for every piece
-    assert p["stages"] >= 2
+    assert p["stages"] >= 3
     mt = 1 if m <= 8 else 2
     partial = -(-n // 256) * p["k_splits"] * 256 * (8 * mt) * 4
     assert p["workspace_bytes"] == 256 + 65536 + -(-partial // 256) * 256

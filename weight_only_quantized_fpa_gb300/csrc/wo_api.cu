@@ -71,25 +71,43 @@ bool use_tc(int m, int n, int k, int group_size, int bits)
     return m >= kTcMinM || !stream_supported(m, n, k, norm_group(group_size, k), bits);
 }
 
-// Below the tensor-core sizes, decode-sized m (1..16) runs the persistent
-// kernel (wo_gemv.cu) when its plan exists and, for group-wise 4-bit weights,
-// the scales and zeros are 16-byte aligned (they are fetched by TMA); the
-// other cases run the cluster-split streaming kernel (wo_stream.cu).  The
-// environment variable WO_DECODE_KERNEL=stream forces the latter (an A/B
-// switch for measurements; both kernels give results within tolerance, but
-// not bit-identical ones).
-bool decode_forced_stream()
+// Below the tensor-core sizes, 4-bit weights at decode-sized m (1..16) run
+// the persistent kernel (wo_gemv.cu) where the cluster-split streaming
+// kernel (wo_stream.cu) cannot keep the GPU busy: when its grid needs more
+// than one resident wave (2 CTAs per SM), or fills fewer CTAs than there
+// are SMs while each streams 64 KB or more (long k, few channels).  Smaller
+// problems keep the cluster kernel, whose shorter critical path measured
+// faster at 2-16 MB of weights.  The environment variable WO_DECODE_KERNEL
+// overrides the choice for measurements and tests: "stream" forces the
+// cluster kernel, "persistent" the persistent one wherever it applies (the
+// two give results within tolerance of each other, not bit-identical ones).
+int decode_override()
 {
-    static const bool forced = [] {
-        const char* v = std::getenv("WO_DECODE_KERNEL");
-        return v && std::strcmp(v, "stream") == 0;
+    static const int v = [] {
+        const char* e = std::getenv("WO_DECODE_KERNEL");
+        if (!e)
+            return 0;
+        if (std::strcmp(e, "stream") == 0)
+            return 1;
+        if (std::strcmp(e, "persistent") == 0)
+            return 2;
+        return 0;
     }();
-    return forced;
+    return v;
 }
 
 bool use_gemv_shape(int m, int n, int k, int group, int bits)
 {
-    return m >= 1 && m <= 16 && !decode_forced_stream() && gemv_supported(m, n, k, group, bits);
+    if (m < 1 || m > 16 || decode_override() == 1 || !gemv_supported(m, n, k, group, bits))
+        return false;
+    if (decode_override() == 2)
+        return true;
+    const StreamPlan c = plan_stream(m, n, k, group, bits, OUT_PLAIN, 0);
+    if (!c.valid)
+        return true;
+    const long long ctas = (long long)c.grid_x * c.splits;
+    const double bytes_per_cta = (double)n * k * bits / 8.0 / (double)ctas;
+    return ctas > 2LL * num_sms() || (ctas < num_sms() && bytes_per_cta >= 65536.0);
 }
 
 bool use_gemv(const GemmArgs& a)

@@ -20,12 +20,10 @@
 // the same number of weight bytes as one continuous pipeline across strip
 // boundaries: no wave quantisation.  A CTA's range covers whole strips
 // (their outputs are written directly) and up to two strip pieces; a
-// piece's fp32 partial sums go to the workspace, and once a CTA has
-// streamed its whole range it counts its pieces: the CTA whose piece of a
+// piece's fp32 partial sums go to the workspace and the CTA whose piece of a
 // strip arrives last sums the strip's pieces in k order and writes the
-// outputs (no CTA ever waits for another, nothing stalls the stream, and
-// the order of every sum is fixed by the shape, so results are bit-for-bit
-// repeatable).
+// outputs (no CTA ever waits for another; the order of every sum is fixed
+// by the shape, so results are bit-for-bit repeatable).
 //
 // Per CTA: one producer warp whose lane 0 fills a ring of shared-memory
 // stages with TMA tensor copies (the packed weights of the strip's 16
@@ -78,11 +76,14 @@ constexpr int kSzGroups = 8;                        // groups per scale box (16 
 constexpr int kGvWBytes = 2 * kGvNw * kGvTps * kTileBytes;
 constexpr int kGvSzBox = kGvCh * kSzGroups * 2;     // one box of scales (or zeros)
 
-template <int MT>
+// ONE (m = 1): the stage's activations are one unswizzled box of 128
+// values; else two boxes of 64 k by 8 * MT rows (rows past m read as zeros)
+// with the 128-byte swizzle that ldmatrix reads conflict-free.
+template <int MT, bool ONE>
 struct GvGeom {
-    static constexpr int ROWS = 8 * MT;       // activation rows fetched (past m: zeros)
-    static constexpr int A_BOX = ROWS * 128;  // 64 k of ROWS rows, 128-byte swizzle
-    static constexpr int A_BYTES = 2 * A_BOX;
+    static constexpr int ROWS = ONE ? 1 : 8 * MT;
+    static constexpr int A_BOX = ONE ? 2 * kGvStageK : ROWS * 128;
+    static constexpr int A_BYTES = ONE ? A_BOX : 2 * A_BOX;
     static constexpr int NV = 2 * MT * 4;     // accumulator values per lane
 };
 
@@ -93,6 +94,7 @@ struct GvParams {
     int nstrips;
     long long T;       // units (strip, stage) in all
     int lg_tpg;        // log2(group / 64), group-wise
+    int G;             // groups per channel
     int stages;        // ring stages
     int stage_bytes;
     int tx;            // bytes a stage receives
@@ -133,11 +135,20 @@ __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r
                  : "r"(addr));
 }
 
-__device__ __forceinline__ uint16_t lds_u16(uint32_t saddr)
+// Shared-memory loads at byte offset `off` of the CTA's shared window
+// (shared-space addresses: measured 10 % faster than C++ loads through the
+// window's generic pointer).  Volatile, so they stay between the mbarrier
+// wait that makes a stage's data visible and the arrive that releases it.
+__device__ __forceinline__ uint16_t lds_u16(const uint8_t* smem, uint32_t off)
 {
     uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr));
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_addr(smem) + off));
     return v;
+}
+
+__device__ __forceinline__ uint4 lds_v4(const uint8_t* smem, uint32_t off)
+{
+    return lds128(smem_addr(smem) + off);
 }
 
 // d += a . b, and d = a . b with a zero accumulator (the first k-step of a
@@ -209,21 +220,29 @@ struct U4Off {
 // MT: 8-row activation blocks (1 or 2); ONE: m == 1 (MT == 1), tiles spread
 // over the 8 output columns; GROUPED: scales and zeros per group (boxes in
 // the stage) rather than per channel; ZEROS: group-wise zeros given.
+constexpr int kGvCtasPerSm = 2;
+constexpr size_t kGvSmemBudget = 110 * 1024;  // per CTA: two CTAs per SM
+
 template <int ACT, int MT, bool ONE, bool GROUPED, bool ZEROS>
-__global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
+__global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
     gemv4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                  const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
                  const GvParams p)
 {
-    using Gm = GvGeom<MT>;
+    using Gm = GvGeom<MT, ONE>;
     constexpr int NV = Gm::NV, NW = kGvNw, CH = kGvCh, TPS = kGvTps;
+    // Group-wise scales and zeros: with every stage, the boxes of 8 groups by
+    // the strip's channels that cover it (a separate ring of boxes loaded
+    // once per 8 groups measured slower: with two slots the producer waits
+    // for the consumers at every box change, which shortens the stage ring).
     static_assert(!ONE || MT == 1, "one row fits one row block");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int S = p.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
+    const uint32_t zero_off = (uint32_t)(S * p.stage_bytes);  // 16 zero bytes
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + zero_off + 16);
     uint64_t* empty = full + S;
     int* abort_flag = reinterpret_cast<int*>(empty + S);
     int* last_flag = abort_flag + 1;
@@ -244,6 +263,7 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
         }
         *abort_flag = 0;
         *last_flag = 0;
+        *reinterpret_cast<uint4*>(smem + zero_off) = make_uint4(0u, 0u, 0u, 0u);
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmW);
@@ -275,7 +295,8 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
             auto load_a = [&](int s, int st) {
                 uint8_t* stage = smem + (size_t)s * p.stage_bytes;
                 tma_load_2d(stage, &tmA, &full[s], st * kGvStageK, 0);
-                tma_load_2d(stage + Gm::A_BOX, &tmA, &full[s], st * kGvStageK + 64, 0);
+                if constexpr (!ONE)
+                    tma_load_2d(stage + Gm::A_BOX, &tmA, &full[s], st * kGvStageK + 64, 0);
             };
             // the first ring's weights do not depend on the previous grid
             const int pre = nunits < S ? nunits : S;
@@ -310,6 +331,8 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
             }
             if (!ok) {
                 // let the copies already issued land before the CTA winds down
+                // (the loop only gives up at i >= pre, with stages [0, i)
+                // issued in full)
                 volatile int never = 0;
                 for (int j = i - S > 0 ? i - S : 0; j < i; ++j)
                     mbar_wait_bounded(&full[j % S], (j / S) & 1, &never, nullptr, 0, kWaitLimitNs);
@@ -383,8 +406,8 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
     auto scale_zero = [&](uint32_t sbox, int gi, int r, int h, float& sv, float& zv) {
         if constexpr (GROUPED) {
             const uint32_t off = (uint32_t)(((c_lo + 16 * r + 8 * h) * kSzGroups + gi) * 2);
-            sv = to_f32<ACT>(lds_u16(sbox + off));
-            const float z = ZEROS ? to_f32<ACT>(lds_u16(sbox + (uint32_t)kGvSzBox + off)) : 0.f;
+            sv = to_f32<ACT>(lds_u16(smem, sbox + off));
+            const float z = ZEROS ? to_f32<ACT>(lds_u16(smem, sbox + (uint32_t)kGvSzBox + off)) : 0.f;
             zv = fmaf(-(h ? U4Off<ACT>::hi : U4Off<ACT>::lo), sv, z);
         } else {
             sv = ps[r][h];
@@ -441,14 +464,9 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
             }
     };
 
-    // pieces of strips this CTA shares with others (its first and its last
-    // segment at most): counted and, by the CTA whose piece arrives last,
-    // summed only once the CTA's whole range is streamed, so that no fence or
-    // atomic ever stalls the stream
-    int pend_strip[2] = {-1, -1};
-    int npend = 0;
-
-    // the segment's sums -> C (a whole strip) or the workspace (a piece)
+    // the segment's sums -> C (a whole strip) or the workspace (a piece; the
+    // CTA whose piece of the strip arrives last sums the strip's pieces in k
+    // order and stores them)
     auto seg_end = [&](int st_last) {
         asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs: after the previous grid
         float fin[2][MT][4];
@@ -478,108 +496,94 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
                 store_c(strip, fin);
             return;
         }
-        const int wf = worker_of((long long)strip * p.nst, p.T, P);
-        float4* dst = reinterpret_cast<float4*>(
-            p.partial + (((size_t)strip * p.maxseg + ((int)blockIdx.x - wf)) * CH + (size_t)(32 * warp + lane)) * NV);
+        const long long su0 = (long long)strip * p.nst;
+        const int wf = worker_of(su0, p.T, P);
+        const int nseg = worker_of(su0 + p.nst - 1, p.T, P) - wf + 1;
+        const float* base = p.partial + ((size_t)strip * p.maxseg * CH + (size_t)(32 * warp + lane)) * NV;
         if (ok) {
+            float4* dst = reinterpret_cast<float4*>(const_cast<float*>(base) + (size_t)((int)blockIdx.x - wf) * CH * NV);
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
                 for (int j = 0; j < MT; ++j)
                     __stcg(dst + r * MT + j, make_float4(fin[r][j][0], fin[r][j][1], fin[r][j][2], fin[r][j][3]));
         }
-        if (npend < 2)
-            pend_strip[npend++] = strip;
-    };
-
-    // after the range: count this CTA's pieces; the last piece of a strip
-    // to arrive sums the strip's pieces in k order (slot order) and stores
-    auto finish_pieces = [&]() {
-        if (npend == 0)
-            return;
-        // every consumer's pieces are written; the CTA barrier orders them
-        // before thread 0's fence, which releases them at GPU scope ahead of
-        // the arrival counts
+        // every consumer's piece is written; the CTA barrier orders those
+        // writes before thread 0's fence, which releases them at GPU scope
+        // ahead of the arrival count
         asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
         if (threadIdx.x == 0) {
             int last = 0;
             if (!*abort) {
                 __threadfence();
-                for (int i = 0; i < npend; ++i) {
-                    const int sp = pend_strip[i];
-                    const long long su0 = (long long)sp * p.nst;
-                    const int nseg = worker_of(su0 + p.nst - 1, p.T, P) - worker_of(su0, p.T, P) + 1;
-                    if (atomicAdd(p.counters + sp, 1u) == (unsigned)(nseg - 1))
-                        last |= 1 << i;
-                }
+                last = atomicAdd(p.counters + strip, 1u) == (unsigned)(nseg - 1) ? 1 : 0;
                 if (last)
                     __threadfence();  // acquire: every other piece is visible
             }
             *last_flag = last;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
-        const int last = *(volatile int*)last_flag;
-        for (int i = 0; i < npend; ++i) {
-            if (!((last >> i) & 1))
-                continue;
-            const int sp = pend_strip[i];
-            const long long su0 = (long long)sp * p.nst;
-            const int nseg = worker_of(su0 + p.nst - 1, p.T, P) - worker_of(su0, p.T, P) + 1;
-            const float* base = p.partial + ((size_t)sp * p.maxseg * CH + (size_t)(32 * warp + lane)) * NV;
-            float fin[2][MT][4];
+        if (!*(volatile int*)last_flag)
+            return;
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+        for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int j = 0; j < MT; ++j)
+            for (int j = 0; j < MT; ++j)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        fin[r][j][q] = 0.f;
-            // RB pieces' loads in flight at a time
-            constexpr int RB = MT == 1 ? 4 : 2;
-            for (int j0 = 0; j0 < nseg; j0 += RB) {
-                float4 x[RB][2 * MT];
+                for (int q = 0; q < 4; ++q)
+                    fin[r][j][q] = 0.f;
+        // slot order = k order; RB pieces' loads in flight at a time
+        constexpr int RB = MT == 1 ? 4 : 2;
+        for (int j0 = 0; j0 < nseg; j0 += RB) {
+            float4 x[RB][2 * MT];
 #pragma unroll
-                for (int b = 0; b < RB; ++b)
+            for (int b = 0; b < RB; ++b)
 #pragma unroll
-                    for (int v = 0; v < 2 * MT; ++v)
-                        x[b][v] = j0 + b < nseg
-                                      ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(j0 + b) * CH * NV) + v)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int v = 0; v < 2 * MT; ++v)
+                    x[b][v] = j0 + b < nseg
+                                  ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(j0 + b) * CH * NV) + v)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int b = 0; b < RB; ++b)
+            for (int b = 0; b < RB; ++b)
 #pragma unroll
-                    for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < 2; ++r)
 #pragma unroll
-                        for (int j = 0; j < MT; ++j) {
-                            fin[r][j][0] += x[b][r * MT + j].x;
-                            fin[r][j][1] += x[b][r * MT + j].y;
-                            fin[r][j][2] += x[b][r * MT + j].z;
-                            fin[r][j][3] += x[b][r * MT + j].w;
-                        }
-            }
-            store_c(sp, fin);
-            if (threadIdx.x == 0)
-                p.counters[sp] = 0u;  // ready for the next call
+                    for (int j = 0; j < MT; ++j) {
+                        fin[r][j][0] += x[b][r * MT + j].x;
+                        fin[r][j][1] += x[b][r * MT + j].y;
+                        fin[r][j][2] += x[b][r * MT + j].z;
+                        fin[r][j][3] += x[b][r * MT + j].w;
+                    }
         }
+        store_c(strip, fin);
+        if (threadIdx.x == 0)
+            p.counters[strip] = 0u;  // ready for the next call
     };
 
-    // one packed tile (both blocks) of the stage at `stage`, tile tl of it
+    // one packed tile (both blocks) of the stage at offset `stage` of the
+    // shared window, tile tl of it
+    const uint32_t sbase = smem_addr(smem);  // shared-space address (ldmatrix)
     auto do_tile = [&](uint32_t stage, uint32_t sbox, int kt0, int tl, int x0) {
-        const uint4 v0 = lds128(stage + w_lane0 + (uint32_t)(tl * kTileBytes));
-        const uint4 v1 = lds128(stage + w_lane1 + (uint32_t)(tl * kTileBytes));
+        const uint4 v0 = lds_v4(smem, stage + w_lane0 + (uint32_t)(tl * kTileBytes));
+        const uint4 v1 = lds_v4(smem, stage + w_lane1 + (uint32_t)(tl * kTileBytes));
         const uint32_t one = ones_x2<ACT>();
         const uint32_t ones[4] = {one, one, one, one};
         if constexpr (ONE) {
             // activations in column (kt0 + tl) mod 8 only: lanes of that
             // column (g) keep them, the others get zeros
             const int kt = kt0 + tl;
-            const uint32_t msk = g == (kt & 7) ? 0xFFFFFFFFu : 0u;
+            // ldmatrix of the tile's 64 activations as the B fragments of its
+            // four k-steps (matrix i = 8 values of k, row r = column r): the
+            // rows of the tile's column r = kt mod 8 point at the activations,
+            // every other row at 16 zero bytes, so the other columns get zeros
+            const uint32_t act = sbase + stage + (uint32_t)(tl * 128 + (lane >> 3) * 16);
+            const bool mine = (lane & 7) == (kt & 7);
+            uint32_t bf[4][2];
+            ldsm_x4(mine ? act : sbase + zero_off, bf[0][0], bf[0][1], bf[1][0], bf[1][1]);
+            ldsm_x4(mine ? act + 64u : sbase + zero_off, bf[2][0], bf[2][1], bf[3][0], bf[3][1]);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const int kk = tl * 64 + 16 * ks;  // k within the stage
-                // row 0 of the swizzled activation box: chunks are not permuted
-                const uint32_t ab = stage + (uint32_t)((kk >> 6) * Gm::A_BOX + (kk & 63) * 2 + 4 * t);
-                const uint32_t b0 = lds32(ab) & msk, b1 = lds32(ab + 16) & msk;
+                const uint32_t b0 = bf[ks][0], b1 = bf[ks][1];
                 const uint32_t w0 = ks == 0 ? v0.x : ks == 1 ? v0.y : ks == 2 ? v0.z : v0.w;
                 const uint32_t w1 = ks == 0 ? v1.x : ks == 1 ? v1.y : ks == 2 ? v1.z : v1.w;
                 uint32_t a0[4], a1[4];
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const int kk = tl * 64 + 16 * ks;
-                const uint32_t box = stage + (uint32_t)((kk >> 6) * Gm::A_BOX);
+                const uint32_t box = sbase + stage + (uint32_t)((kk >> 6) * Gm::A_BOX);
                 const uint32_t col = ((((uint32_t)(kk & 63) >> 3) + a_hi) ^ a_xor) << 4;
                 uint32_t b[MT][2];
                 if constexpr (MT == 1)
@@ -651,21 +655,20 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
         const int s = i % S;
         const bool strip_end = st == p.nst - 1;
         const bool seg_last = strip_end || i == nunits - 1;
+        const int x0 = GROUPED ? (((st * TPS) >> p.lg_tpg) / kSzGroups) * kSzGroups : 0;
         if (ok)
             ok = __all_sync(0xffffffffu,
                             mbar_wait_bounded(&full[s], (i / S) & 1, abort, p.err, 32, kWaitLimitNs));
         if (ok) {
             const int kt0 = st * TPS;
-            const uint32_t stage = smem_addr(smem + (size_t)s * p.stage_bytes);
+            const uint32_t stage = (uint32_t)(s * p.stage_bytes);  // offset in the shared window
             const uint32_t sbox = stage + (uint32_t)(Gm::A_BYTES + kGvWBytes);
-            const int x0 = GROUPED ? ((kt0 >> p.lg_tpg) / kSzGroups) * kSzGroups : 0;
             do_tile(stage, sbox, kt0, 0, x0);
             const bool two = kt0 + 1 < p.ktiles;  // a strip's last stage may hold one tile
             if (two)
                 do_tile(stage, sbox, kt0, 1, x0);
             if constexpr (ONE) {
-                // a segment that ends inside a column window folds it now,
-                // while this stage's scale boxes are still in place
+                // a segment that ends inside a column window folds it now
                 const int kt_last = kt0 + (two ? 1 : 0);
                 if (seg_last && (kt_last & 7) != 7)
                     fold_window(sbox, kt_last, x0);
@@ -690,7 +693,6 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
             ++st;
         }
     }
-    finish_pieces();
 }
 
 }  // namespace
@@ -699,8 +701,6 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, 2)
 
 namespace {
 
-constexpr int kGvCtasPerSm = 2;
-constexpr size_t kGvSmemBudget = 110 * 1024;  // per CTA: two CTAs per SM
 
 struct GvPlan {
     int mt, stages, stage_bytes, grid, nstrips, nst, maxseg;
@@ -724,16 +724,16 @@ GvPlan plan_gemv(int m, int n, int k, int group, int bits)
     if (bits != 4 || m < 1 || m > 16)
         return P;
     P.mt = m <= 8 ? 1 : 2;
-    const int a_bytes = 2 * 8 * P.mt * 128;
+    const bool one = m == 1;
+    const int a_bytes = one ? 2 * kGvStageK : 2 * 8 * P.mt * 128;
     const bool grouped = group != k;
     if (grouped) {
         const int G = k / group;
         if (G % kSzGroups != 0 || ilog2_exact(group / 64) < 0)
             return P;  // scale boxes need 8-group-aligned rows; groups of 64 * 2^j
     }
-    const int sz_bytes = grouped ? 2 * kGvSzBox : 0;
-    P.stage_bytes = (a_bytes + kGvWBytes + sz_bytes + 1023) / 1024 * 1024;
-    const size_t fixed = 1024 + 256;
+    P.stage_bytes = (a_bytes + kGvWBytes + (grouped ? 2 * kGvSzBox : 0) + 1023) / 1024 * 1024;
+    const size_t fixed = 1024 + 512;
     int stages = (int)((kGvSmemBudget - fixed) / P.stage_bytes);
     if (stages > 8)
         stages = 8;
@@ -760,12 +760,13 @@ GvPlan plan_gemv(int m, int n, int k, int group, int bits)
 template <int ACT, int MT, bool ONE, bool GROUPED, bool ZEROS>
 cudaError_t launch_gemv_t(const GemmArgs& a, const GvPlan& plan, cudaStream_t s)
 {
-    using Gm = GvGeom<MT>;
+    using Gm = GvGeom<MT, ONE>;
     CUtensorMap ma, mw, ms, mz;
     const CUtensorMapDataType dt16 =
         ACT == ACT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!make_tmap_2d(&ma, dt16, a.A, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2, 64, Gm::ROWS,
-                      CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_tmap_2d(&ma, dt16, a.A, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2,
+                      ONE ? kGvStageK : 64, Gm::ROWS,
+                      ONE ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int ktiles = a.k / 64;
     if (!make_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT64, a.B, (uint64_t)ktiles * 64, (uint64_t)a.n / 16,
@@ -791,6 +792,7 @@ cudaError_t launch_gemv_t(const GemmArgs& a, const GvPlan& plan, cudaStream_t s)
     p.nstrips = plan.nstrips;
     p.T = plan.T;
     p.lg_tpg = GROUPED ? ilog2_exact(a.group / 64) : 0;
+    p.G = G;
     p.stages = plan.stages;
     p.stage_bytes = plan.stage_bytes;
     p.tx = Gm::A_BYTES + kGvWBytes + (GROUPED ? kGvSzBox * (ZEROS ? 2 : 1) : 0);

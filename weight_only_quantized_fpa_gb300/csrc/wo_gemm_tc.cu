@@ -36,6 +36,13 @@
 // Every mbarrier wait is bounded: a wait that runs out records an error word
 // in the workspace header and the CTA winds down (see the abort path).
 //
+// Programmatic dependent launch: a CTA sets up (barriers, TMEM, tensor-map
+// prefetch) and starts fetching its weight codes while the previous kernel
+// on the stream is still finishing; the roles that touch anything that
+// kernel may produce or read -- activations (warp 2), the 4-bit prepass's
+// pre-scaled scales (dequantisation warps), outputs, row scales and the
+// workspace (epilogue, drain helpers) -- first wait for it to complete.
+//
 // Operand types: 8-bit codes run the MMA in the activation dtype, in which
 // q - 128 is exact.  4-bit codes run it in fp16, with both operands brought
 // into fp16's range by powers of two that the epilogue undoes: a prepass
@@ -279,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // work units: (output tile, k range); unit u is tile u / splits, k blocks
     // [(u % splits) kps, + kps)
     const int splits = p.splits, kps = p.num_kb / splits;
@@ -430,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t* empty = codes ? bars->emptyC : bars->emptyA;
             int c = 0;  // k blocks issued, over all tiles
             bool ok = true;
+            if (!codes)  // activations: after the previous kernel on the stream
+                asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int it = 0; it < my_tiles && ok; ++it) {
                 const int u = (int)blockIdx.x + it * (int)gridDim.x;
                 int m0, n0;
@@ -515,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- epilogue: TMEM lane quadrant q = warp % 4 ----
         const int q = warp - kEpilogueWarp0;
         volatile int* is_last = &bars->is_last;
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs, row scales, workspace
         for (int it = 0; it < my_tiles; ++it) {
             const int u = (int)blockIdx.x + it * (int)gridDim.x;
             const int tile = u / splits;
@@ -613,6 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kDequantWarp0) {
         // ---- dequantisation ----
         const int dw = warp - kDequantWarp0;
+        if (BITS == 4 || helpers)  // the prepass's scales / the helpers' C stores
+            asm volatile("griddepcontrol.wait;" ::: "memory");
         auto n0_of = [&](int c) {
             const int u = (int)blockIdx.x + (c / kps) * (int)gridDim.x;
             int m0, n0;
@@ -828,6 +841,9 @@ __global__ void __launch_bounds__(kPrepThreads)
                    int a_ctas, int k, const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
                    int n, int G, uint32_t* __restrict__ sz, uint16_t* __restrict__ colscale)
 {
+    // the GEMM kernel behind this one may start its set-up now: it waits for
+    // this grid before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if ((int)blockIdx.x < a_ctas) {
         prep_a_row(A, A16, rowscale, (int)blockIdx.x, k);
         return;
@@ -897,8 +913,17 @@ cudaError_t launch_tc_t(const CUtensorMap& ma, const void* B, TcParams tp, cudaS
     if (!make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, B, row_bytes / 4, (uint64_t)tp.n / 16,
                       row_bytes, BK * 16 * BITS / 8 / 4, BN / 16, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    kern<<<grid, kThreads, smem, s>>>(ma, mc, tp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mc, tp);
 }
 
 template <int BITS, int OT, int ACT>

@@ -109,10 +109,14 @@ WO_API size_t wo_workspace_size(int m, int n, int k, int group_size, int bits);
  *   bits 4: group_size 64 or 128 (a multiple of 64 dividing k), or -1/k.
  * Requires n % 64 == 0, k % 64 == 0 and k > 0; m == 0 or n == 0 is a no-op.
  * The kernel is chosen by m: for 4-bit weights at decode-sized m (1..16)
- * a persistent weight-streaming kernel (group-wise weights also need
- * 16-byte aligned scales and zeros and k / group_size a multiple of 8), else
- * up to m = 64 a cluster-split weight-streaming kernel, and a tcgen05
- * tensor-core kernel for larger m (wo_gemm_plan reports the choice).  Results are deterministic: identical inputs give
+ * a persistent weight-streaming kernel where the cluster-split one cannot
+ * fill the GPU (group-wise weights also need 16-byte aligned scales and
+ * zeros and k / group_size a multiple of 8); for 8-bit weights at 17..64
+ * rows (n % 128 == 0) a tcgen05 kernel with the weights as the MMA's rows
+ * while n / 128 is at most the SM count, the m >= 65 tensor-core kernel for
+ * wider n; otherwise up to m = 64 a cluster-split weight-streaming kernel,
+ * and a tcgen05 tensor-core kernel for larger m (wo_gemm_plan reports the
+ * choice).  Results are deterministic: identical inputs give
  * bit-identical C.
  * Ordering: the small-m kernel uses programmatic dependent launch.  It may
  * start reading B_packed, scales, zeros and bias while the previous
@@ -136,7 +140,9 @@ WO_API wo_status wo_gemm(const void* A, const uint8_t* B_packed, const void* sca
 typedef enum {
     WO_KERNEL_STREAM = 0,            /* cluster-split weight streaming (m <= 64) */
     WO_KERNEL_TENSOR_CORE = 1,       /* tcgen05 tensor cores (m >= 65) */
-    WO_KERNEL_STREAM_PERSISTENT = 2  /* persistent weight streaming (4-bit, m <= 16) */
+    WO_KERNEL_STREAM_PERSISTENT = 2, /* persistent weight streaming (4-bit, m <= 16) */
+    WO_KERNEL_TENSOR_CORE_SWAP_AB = 3 /* tcgen05 with the weights as the MMA's rows
+                                        (8-bit, 17 <= m <= 64) */
 } wo_kernel;
 
 typedef struct {
@@ -144,8 +150,8 @@ typedef struct {
     int tile_m;            /* rows of C per CTA tile (streaming: m) */
     int tile_n;            /* output channels per CTA tile (persistent: per strip) */
     int k_splits;          /* CTAs of one cluster (streaming), units per tile along k
-                              (tensor cores), or the most pieces one strip's k range is
-                              cut into across CTAs (persistent) */
+                              (tensor cores, swap AB), or the most pieces one strip's k
+                              range is cut into across CTAs (persistent) */
     int ctas;              /* CTAs launched */
     int stages;            /* streaming: shared-memory ring stages per CTA; else 0 */
     size_t workspace_bytes; /* == wo_workspace_size */

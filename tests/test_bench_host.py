@@ -107,3 +107,17 @@ def test_widened_workloads(name, act, group, ms):
     assert w["dtype"] == ("bf16" if act == inputs.BF16 else "f16")
     c = inputs.workload_case(w["config"], 0)
     assert c.act_dtype == act and c.scales.shape == ((c.n,) if group == -1 else (c.n, c.k // group))
+
+
+@pytest.mark.parametrize("name,kernel", [("w8_decode", "stream_kernel"), ("w8_large", "gemm_tc_kernel"),
+                                         ("w8_mid", "gemm_tc_kernel")])
+def test_roofline_kernel_follows_the_plans(name, kernel):
+    # the roofline names the kernel that carries most of the step's bytes (or
+    # flops) by the library's own plan of each case; w8_mid's bytes are mostly
+    # the 37888-channel cases, which have more 128-channel blocks than SMs and
+    # so run on the tensor-core kernel
+    import weight_only_quantized_fpa_gb300 as wo
+    wo.load_library()
+    k, src = bench.dominant_kernel(wo, bench.workload_cases(name), bench.WORKLOADS[name]["unit"] != "GB/s")
+    assert k == kernel and all(os.path.exists(os.path.join(ROOT, "weight_only_quantized_fpa_gb300", "csrc", f))
+                               for f in src)

@@ -229,6 +229,65 @@ def test_split_k_long_reduction_w4(wo):
     _check_full(DeviceCase(c), "split-k w4")
 
 
+# ------------------------------------- 17..64 rows (between the regimes) --
+#
+# 8-bit weights at 17..64 rows take the swap-AB tensor-core kernel while n
+# has at most one block of 128 output channels per SM: the blocks are the
+# MMA's rows, the activation rows its columns, and a block's k range is
+# split across CTAs to fill the SMs (the splits' fp32 sums added in split
+# order by the last split to arrive).  Wider n goes to the m >= 65
+# tensor-core kernel.  test_mid_shapes_on_the_other_kernels runs the same
+# cases on the streaming and the m >= 65 tensor-core kernels.
+MID = [
+    # m, n, k, act, bias
+    (17, 384, 2048, inputs.F16, True),     # 3 blocks, 8 splits
+    (24, 4608, 3584, inputs.BF16, True),
+    (33, 256, 4160, inputs.F16, False),    # 65 k blocks: a short last split
+    (48, 3584, 3584, inputs.BF16, True),
+    (64, 1152, 6144, inputs.F16, True),
+    (40, 19456, 1024, inputs.F16, True),   # 152 blocks: no split
+    (64, 3584, 18944, inputs.BF16, False),  # long k
+    (40, 37888, 1024, inputs.F16, True),   # 296 blocks: the m >= 65 kernel
+]
+
+
+@pytest.mark.parametrize("m,n,k,act,bias", MID)
+def test_mid_shapes(wo, m, n, k, act, bias):
+    if not os.environ.get("WO_MID_KERNEL"):
+        want = "tensor_core_swap_ab" if n // 128 <= torch.cuda.get_device_properties(0).multi_processor_count \
+            else "tensor_core"
+        assert wo.gemm_plan(m, n, k, 8, -1, act)["kernel"] == want
+    c = inputs.make_gemm_case(15, m + n + k, m, n, k, bits=8, group_size=-1, act_dtype=act,
+                              scale_lo=0.001, scale_hi=0.01, with_zeros=False, with_bias=bias)
+    dc = DeviceCase(c)
+    _check_full(dc, f"mid m{m} n{n} k{k}")
+    C1 = dc.run().clone()
+    C2 = dc.run()
+    torch.cuda.synchronize()
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))  # splits summed in order
+
+
+@pytest.mark.parametrize("kernel", ["stream", "tensor_core"])
+def test_mid_shapes_on_the_other_kernels(wo, kernel):
+    # the same cases in a process whose wo_gemm takes another kernel at
+    # 17..64 rows (the choice is read once per process)
+    if os.environ.get("WO_MID_KERNEL"):
+        pytest.skip("already forced")
+    env = dict(os.environ, WO_MID_KERNEL=kernel)
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.abspath(__file__), "-q", "-m", "gpu",
+                        "-p", "no:cacheprovider", "-k", "test_mid_shapes and not other_kernels"],
+                       env=env, capture_output=True, text=True, timeout=600,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    assert "passed" in r.stdout
+
+
+@pytest.mark.parametrize("case", range(len(inputs.W8_MID["shapes"])))
+def test_w8_mid_full(wo, case):
+    dc = DeviceCase(inputs.workload_case(11, case))
+    _check_full(dc, dc.c.name)
+
+
 # ------------------------------------------------ A16W8 decode (config 2) --
 
 @pytest.mark.parametrize("case", range(len(inputs.W8_DECODE["shapes"])))

@@ -44,9 +44,11 @@ def test_tensor_core_tile_configurations(m, n, k, bits, group, tile, splits):
 
 @pytest.mark.parametrize("bits,group", [(8, -1), (4, 64), (4, 128), (4, -1)])
 def test_kernel_choice_by_m(bits, group):
+    # 8-bit weights take the swap-AB tensor-core kernel at 17..64 rows
     n, k = 512, 2048
-    for m, kern in [(1, "stream"), (16, "stream"), (17, "stream"),
-                    (64, "stream"), (65, "tensor_core"), (256, "tensor_core")]:
+    mid = "tensor_core_swap_ab" if bits == 8 else "stream"
+    for m, kern in [(1, "stream"), (16, "stream"), (17, mid),
+                    (64, mid), (65, "tensor_core"), (256, "tensor_core")]:
         assert wo.gemm_plan(m, n, k, bits, group)["kernel"] == kern, (m, bits, group)
 
 
@@ -69,9 +71,9 @@ def test_4bit_decode_kernel_choice(n, k, group, persistent):
     assert wo.gemm_plan(17, n, k, 4, group)["kernel"] == "stream"
 
 
-@pytest.mark.parametrize("m,n,k,bits,group", [(24, 4608, 3584, 8, -1), (32, 3584, 18944, 8, -1),
-                                              (24, 37888, 3584, 8, -1), (20, 2048, 13312, 4, 64),
-                                              (64, 131072, 2048, 4, 64), (48, 3584, 3584, 8, -1)])
+@pytest.mark.parametrize("m,n,k,bits,group", [(24, 4608, 3584, 4, 64), (32, 3584, 18944, 4, 64),
+                                              (24, 37888, 3584, 4, -1), (20, 2048, 13312, 4, 64),
+                                              (64, 131072, 2048, 4, 64), (48, 3584 + 64, 3584, 8, -1)])
 def test_stream_plans_fill_one_resident_wave(m, n, k, bits, group):
     p = wo.gemm_plan(m, n, k, bits, group, wo.WO_F16)
     assert p["kernel"] == "stream" and p["tile_m"] == m
@@ -115,6 +117,32 @@ def test_grouped_4bit_decode_with_unaligned_row_of_groups_uses_the_cluster_kerne
 @pytest.mark.parametrize("m,n,k", [(1, 4608, 3584), (4, 3584, 18944), (16, 37888, 3584)])
 def test_8bit_decode_uses_the_cluster_kernel(m, n, k):
     assert wo.gemm_plan(m, n, k, 8, -1, wo.WO_F16)["kernel"] == "stream"
+
+
+@pytest.mark.parametrize("m,n,k", [(24, 4608, 3584), (32, 3584, 3584), (48, 37888, 3584),
+                                   (64, 3584, 18944), (17, 384, 2048), (40, 128 * SMS, 1024),
+                                   (40, 128 * SMS + 128, 1024)])
+def test_swap_ab_plans(m, n, k):
+    # 8-bit weights at 17..64 rows: blocks of 128 output channels, k split so
+    # that the (block, split) items fill the SMs one item each, each split at
+    # least 4 k blocks unless there is one, at most 8; the splits' fp32 sums
+    # in the workspace after the header and counter area.  With more blocks
+    # than SMs the m >= 65 tensor-core kernel takes the shape.
+    p = wo.gemm_plan(m, n, k, 8, -1, wo.WO_F16)
+    nb, nkb = n // 128, k // 64
+    if nb > SMS:
+        assert p["kernel"] == "tensor_core"
+        return
+    assert p["kernel"] == "tensor_core_swap_ab" and p["tile_m"] == m and p["tile_n"] == 128
+    sp = p["k_splits"]
+    assert 1 <= sp <= 8
+    assert sp == 1 or nkb // sp >= 4 or -(-nkb // sp) >= 4
+    assert p["ctas"] == nb * sp and nb * sp <= SMS
+    want = max(min(SMS // nb, max(nkb // 4, 1), 8), 1)
+    kps = -(-nkb // want)
+    assert sp == -(-nkb // kps)
+    partial = nb * sp * 128 * 64 * 4 if sp > 1 else 0
+    assert p["workspace_bytes"] == 256 + 65536 + -(-partial // 256) * 256
 
 
 def test_plan_argument_rules():

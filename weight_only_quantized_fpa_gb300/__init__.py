@@ -205,7 +205,8 @@ def gemm_plan(m: int, n: int, k: int, bits: int, group_size: int = -1,
               act_dtype: int = WO_BF16) -> dict:
     """The configuration wo_gemm runs for this problem, as a dict."""
     p = wo_gemm_plan(m, n, k, group_size, bits, act_dtype)
-    kernel = {0: "stream", 1: "tensor_core", 2: "stream_persistent"}[int(p.kernel)]
+    kernel = {0: "stream", 1: "tensor_core", 2: "stream_persistent",
+              3: "tensor_core_swap_ab"}[int(p.kernel)]
     return {"kernel": kernel, "tile_m": p.tile_m,
             "tile_n": p.tile_n, "k_splits": p.k_splits, "ctas": p.ctas, "stages": p.stages,
             "workspace_bytes": int(p.workspace_bytes)}

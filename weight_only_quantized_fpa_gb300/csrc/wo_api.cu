@@ -66,9 +66,53 @@ wo_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WO_OK : WO_ERR_
 
 // Kernel choice by m: the weight-streaming kernel below kTcMinM rows (when
 // its shared-memory ring fits), the tensor-core kernel otherwise.
+// WO_MID_KERNEL overrides the choice at 17..64 rows for measurements:
+// "stream" (the cluster-split streaming kernel), "tensor_core" (the m >= 65
+// kernel); unset, 8-bit weights there take the swap-AB kernel.
+int mid_override()
+{
+    static const int v = [] {
+        const char* e = std::getenv("WO_MID_KERNEL");
+        if (!e)
+            return 0;
+        if (std::strcmp(e, "stream") == 0)
+            return 1;
+        if (std::strcmp(e, "tensor_core") == 0)
+            return 2;
+        return 0;
+    }();
+    return v;
+}
+
+// 8-bit weights at 17..64 rows (between the decode sizes and the tensor-core
+// kernel's) and at most one block of 128 channels per SM: the swap-AB
+// tensor-core kernel, whose MMA rows are the output channels and whose
+// columns are the activation rows.
+bool use_mid(int m, int n, int k, int bits)
+{
+    return m > 16 && m < kTcMinM && mid_override() == 0 && plan_mid(m, n, k, bits).valid;
+}
+
+// 8-bit weights at 17..64 rows with more blocks of 128 channels than SMs:
+// the m >= 65 tensor-core kernel (one MMA per 256 channels and 16 k, no k
+// split needed to fill the SMs) streams them faster than either small-m
+// kernel.
+bool mid_wide(int m, int n, int k, int bits)
+{
+    return m > 16 && m < kTcMinM && bits == 8 && mid_override() == 0 && n % 128 == 0 && k % 64 == 0 &&
+           n / 128 > num_sms();
+}
+
+// The tensor-core kernel: from kTcMinM rows, for the wide 8-bit shapes
+// above, or below where neither the swap-AB kernel nor the streaming
+// kernel's ring fits.
 bool use_tc(int m, int n, int k, int group_size, int bits)
 {
-    return m >= kTcMinM || !stream_supported(m, n, k, norm_group(group_size, k), bits);
+    if (m >= kTcMinM || (mid_override() == 2 && m > 16) || mid_wide(m, n, k, bits))
+        return true;
+    if (use_mid(m, n, k, bits))
+        return false;
+    return !stream_supported(m, n, k, norm_group(group_size, k), bits);
 }
 
 // Below the tensor-core sizes, 4-bit weights at decode-sized m (1..16) run
@@ -180,6 +224,8 @@ size_t wo_workspace_size(int m, int n, int k, int group_size, int bits)
         // the larger of the two activation dtypes' needs
         return plan_tc(m, n, k, norm_group(group_size, k), bits, WO_BF16).ws_bytes;
     }
+    if (use_mid(m, n, k, bits))
+        return plan_mid(m, n, k, bits).ws_bytes;
     // either small-m kernel may run (the persistent one needs its partial sums)
     const size_t gv = use_gemv_shape(m, n, k, norm_group(group_size, k), bits)
                           ? gemv_workspace_bytes(m, n, k, norm_group(group_size, k), bits)
@@ -234,6 +280,8 @@ static wo_status gemm_launch(const GemmArgs& a, cudaStream_t s)
 {
     if (use_tc(a.m, a.n, a.k, a.group, a.bits))
         return cuda_status(launch_tc(a, plan_tc(a.m, a.n, a.k, a.group, a.bits, a.act), s));
+    if (use_mid(a.m, a.n, a.k, a.bits))
+        return cuda_status(launch_mid(a, s));
     if (use_gemv(a))
         return cuda_status(launch_gemv(a, s));
     return cuda_status(launch_stream_gemm(a, s));
@@ -276,6 +324,15 @@ wo_status wo_gemm_plan(int m, int n, int k, int group_size, int bits, wo_dtype a
         plan->tile_n = p.bn;
         plan->k_splits = p.splits;
         plan->ctas = (int)(units < num_sms() ? units : num_sms());
+        return WO_OK;
+    }
+    if (use_mid(m, n, k, bits)) {
+        const MidPlan mp = plan_mid(m, n, k, bits);
+        plan->kernel = WO_KERNEL_TENSOR_CORE_SWAP_AB;
+        plan->tile_m = m;
+        plan->tile_n = mp.ch;
+        plan->k_splits = mp.ksplit;
+        plan->ctas = mp.ctas;
         return WO_OK;
     }
     if (use_gemv_shape(m, n, k, g, bits)) {

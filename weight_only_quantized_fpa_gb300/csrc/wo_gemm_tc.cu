@@ -437,6 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t* full = codes ? bars->fullC : bars->fullA;
             uint64_t* empty = codes ? bars->emptyC : bars->emptyA;
             int c = 0;  // k blocks issued, over all tiles
+            int s = 0;  // c % S and the parity of c / S, kept as counters (no division per block)
+            uint32_t ph = 0;
             bool ok = true;
             if (!codes)  // activations: after the previous kernel on the stream
                 asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -445,10 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int m0, n0;
                 tile_coords(p, u / splits, TM, BN, m0, n0);
                 const int kb0 = (u % splits) * kps;
-                for (int kb = kb0; kb < kb0 + kps; ++kb, ++c) {
-                    const int s = c % S;
-                    if (!mbar_wait_bounded(&empty[s], ((c / S) & 1) ^ 1, abort, p.err, codes ? 1 : 9,
-                                           kWaitLimitNs)) {
+                for (int kb = kb0; kb < kb0 + kps; ++kb, ++c, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0) {
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort, p.err, codes ? 1 : 9, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
@@ -473,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait_bounded(&full[i % S], (i / S) & 1, &never, nullptr, 0, kWaitLimitNs);
             }
         }
+        __syncwarp();  // the whole warp reaches the closing CTA barrier together
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer ----
@@ -958,12 +959,23 @@ cudaError_t launch_tc_bn(const CUtensorMap& ma, const void* B, const TcParams& t
 // gemm_tc_kernel: warp 0 codes TMA, warp 2 activation TMA, warp 1 MMA,
 // warps 4-7 epilogue (TMEM lanes are channels, columns are tokens), warps
 // 8-15 dequantisation.
+//
+// The same kernel serves wo_gemm between the decode sizes and the
+// tensor-core kernel's (8-bit weights, 17..64 rows, at most one block of 128
+// output channels per SM: PLAIN): one "expert" of m rows, items (block of
+// 128 output channels, k split), the epilogue writing
+// round(acc * scale[n] + bias[n]) in the activation dtype.  A channel
+// block's k range is split so that the items fill the SMs, one item per SM;
+// each split stores its fp32 sums in the workspace, one 128-byte line of
+// channels per row, and the split that arrives last sums them in split
+// order and writes the block (deterministic; no item waits for another).
 
 constexpr int kMoeNT = 64;  // token rows per chunk (the MMA's N)
 
 // TWO: an item carries two 128-row weight halves that share each token tile
 // (the gated fc1's gate and up rows, or 256 consecutive fc2 channels).
-template <bool TWO>
+// PLAIN: a plain GEMM of at most 64 rows.
+template <bool TWO, bool PLAIN>
 struct MoeCfg {
     static constexpr int WR = TWO ? 256 : 128;           // weight rows per item
     static constexpr int A_BYTES = kMoeNT * BK * 2;       // 8 KiB of token rows
@@ -971,8 +983,12 @@ struct MoeCfg {
     static constexpr int B_BYTES = WR * BK * 2;           // dequantised operand
     // The codes stream from HBM: their ring holds 128 KiB, the bytes in flight
     // one SM needs at HBM rate under load; token rows come from L2 and the
-    // operand ring only covers the dequant -> MMA hand-off.
-    static constexpr int SA = 4, SC = TWO ? 8 : 16, S2 = TWO ? 2 : 3;
+    // operand ring only covers the dequant -> MMA hand-off.  A plain GEMM's
+    // item is short (one k split of one channel block): a deeper operand ring
+    // lets the dequantisation run ahead of the MMAs.
+    static constexpr int SA = 4;
+    static constexpr int SC = PLAIN ? 8 : (TWO ? 8 : 16);
+    static constexpr int S2 = PLAIN ? 4 : (TWO ? 2 : 3);
     static_assert(SC <= 16 && S2 <= 4 && SA <= 8, "barrier arrays");
     static constexpr int COLS = (TWO ? 2 : 1) * kMoeNT;   // TMEM columns per accumulator
     static constexpr uint32_t TMEM_COLS = 2 * COLS;
@@ -980,8 +996,8 @@ struct MoeCfg {
 };
 
 struct MoeTcParams {
-    const int* offsets;      // [E + 1] row ranges of the experts (rows in expert order)
-    int E, nb;               // experts, items (128 or 256 channels) per expert
+    const int* offsets;      // [E + 1] row ranges of the experts (rows in expert order); PLAIN: null
+    int E, nb;               // experts, channel blocks (128 or 256 channels) per expert
     int num_kb;              // K / BK
     int inter;               // gated: channel distance gate -> up (and h row length)
     int n_out;               // plain: output row length (hidden)
@@ -990,24 +1006,51 @@ struct MoeTcParams {
     uint16_t* H;             // gated output h [rows, inter]
     float* Y;                // fp32 output [rows, n_out]
     unsigned* err;
+    // PLAIN (one expert of m rows):
+    int m;                   // rows (<= kMoeNT)
+    int ksplit, kps;         // k splits per channel block, k blocks per split
+    const uint16_t* bias;    // [n_out] or null
+    uint16_t* C;             // [m, n_out]
+    float* partial;          // ksplit > 1: [nb][ksplit][kMoeNT rows][128 channels] fp32
+    unsigned* counters;      // ksplit > 1: [nb], zero between calls
 };
 
 // Chunks of expert e's rows: its row range and how many kMoeNT chunks it needs.
 __device__ __forceinline__ void moe_rows(const MoeTcParams& p, int e, int& r0, int& cnt, int& chunks)
 {
-    r0 = p.offsets[e];
-    cnt = p.offsets[e + 1] - r0;
+    r0 = p.offsets ? p.offsets[e] : 0;
+    cnt = p.offsets ? p.offsets[e + 1] - r0 : p.m;
     chunks = cnt > 0 ? (cnt + kMoeNT - 1) / kMoeNT : 0;
 }
 
-template <bool GATED, bool WIDE, int ACT>
+// Item `it`: its expert, channel block, k split and k blocks [kb0, kb1).
+__device__ __forceinline__ void moe_item(const MoeTcParams& p, int it, int& e, int& nb, int& ks, int& kb0,
+                                         int& kb1)
+{
+    if (p.offsets) {
+        e = it / p.nb;
+        nb = it % p.nb;
+        ks = 0;
+        kb0 = 0;
+        kb1 = p.num_kb;
+    } else {
+        e = 0;
+        nb = it / p.ksplit;
+        ks = it % p.ksplit;
+        kb0 = ks * p.kps;
+        kb1 = min(kb0 + p.kps, p.num_kb);
+    }
+}
+
+template <bool GATED, bool WIDE, bool PLAIN, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
                   const MoeTcParams p)
 {
+    static_assert(!(PLAIN && (GATED || WIDE)), "plain GEMM items are 128 channels");
     constexpr bool TWO = GATED || WIDE;
     constexpr int CH = WIDE ? 256 : 128;  // output channels per item
-    using Cfg = MoeCfg<TWO>;
+    using Cfg = MoeCfg<TWO, PLAIN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1018,8 +1061,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_kb = p.num_kb;
-    const int items = p.E * p.nb;
+    const int items = PLAIN ? p.nb * p.ksplit : p.E * p.nb;
+    if constexpr (PLAIN)  // a wo_gemm: the next kernel may start its set-up
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::SA; ++s) {
@@ -1061,17 +1105,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t* full = codes ? bars->fullC : bars->fullA;
             uint64_t* empty = codes ? bars->emptyC : bars->emptyA;
             int c = 0;
+            int s = 0;  // c % S and the parity of c / S, kept as counters (no division per block)
+            uint32_t ph = 0;
             bool ok = true;
+            if (PLAIN && !codes)  // activations: after the previous kernel on the stream
+                asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-                const int e = it / p.nb, nb = it % p.nb;
+                int e, nb, ks, kb0, kb1;
+                moe_item(p, it, e, nb, ks, kb0, kb1);
                 int r0, cnt, chunks;
                 moe_rows(p, e, r0, cnt, chunks);
                 const int wrow = (e * p.rows_per_expert_w + nb * CH) / 16;  // 16-channel block row
                 for (int ch = 0; ch < chunks && ok; ++ch) {
-                    for (int kb = 0; kb < num_kb; ++kb, ++c) {
-                        const int s = c % S;
-                        if (!mbar_wait_bounded(&empty[s], ((c / S) & 1) ^ 1, abort, p.err, codes ? 21 : 22,
-                                               kWaitLimitNs)) {
+                    for (int kb = kb0; kb < kb1; ++kb, ++c, s = s + 1 == S ? 0 : s + 1, ph ^= s == 0) {
+                        if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort, p.err, codes ? 21 : 22, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
@@ -1097,6 +1144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait_bounded(&full[i % S], (i / S) & 1, &never, nullptr, 0, kWaitLimitNs);
             }
         }
+        __syncwarp();  // the whole warp reaches the closing CTA barrier together
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer: D[channels, tokens] += W[channels, k] . X[tokens, k]^T ----
@@ -1104,8 +1152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int c = 0, t = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                int e, nb, ks, kb0, kb1;
+                moe_item(p, it, e, nb, ks, kb0, kb1);
                 int r0, cnt, chunks;
-                moe_rows(p, it / p.nb, r0, cnt, chunks);
+                moe_rows(p, e, r0, cnt, chunks);
                 for (int ch = 0; ch < chunks && ok; ++ch, ++t) {
                     const int acc = t & 1;
                     if (!mbar_wait_bounded(&bars->tempty[acc], ((t >> 1) & 1) ^ 1, abort, p.err, 27,
@@ -1115,7 +1165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d = tmem + (uint32_t)(acc * Cfg::COLS);
-                    for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                    for (int kb = kb0; kb < kb1; ++kb, ++c) {
                         const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
                         if (!mbar_wait_bounded(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 23,
                                                kWaitLimitNs) ||
@@ -1131,10 +1181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < BK / 16; ++j) {
                             mma_f16(d, wd + (uint64_t)(2 * j), xd + (uint64_t)(2 * j), idesc,
-                                    (kb > 0 || j > 0) ? 1u : 0u);
+                                    (kb > kb0 || j > 0) ? 1u : 0u);
                             if constexpr (TWO)  // second half: operand rows 128..255, 16 KiB on
                                 mma_f16(d + kMoeNT, desc_sw128(w_s + 128 * 128) + (uint64_t)(2 * j),
-                                        xd + (uint64_t)(2 * j), idesc, (kb > 0 || j > 0) ? 1u : 0u);
+                                        xd + (uint64_t)(2 * j), idesc, (kb > kb0 || j > 0) ? 1u : 0u);
                         }
                         mma_commit(&bars->emptyA[sa]);
                         mma_commit(&bars->empty2[s2]);
@@ -1148,6 +1198,113 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(&bars->mma_done, 0, &never, p.err, 28, kWaitLimitNs);
         }
         __syncwarp();
+    } else if (PLAIN && warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+        // ---- plain GEMM epilogue: lane = channel (TMEM lane quadrant warp % 4),
+        // column = row of C; one accumulator per item (m <= kMoeNT) ----
+        const int q = warp - kEpilogueWarp0;
+        volatile int* is_last = &bars->is_last;
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // outputs and workspace
+        const int cnt = p.m;
+        // this lane's channel as round(v * s + b) into row `row` of C
+        auto store_c = [&](int row, int ch, float v, float sc, float bi) {
+            p.C[(size_t)row * p.n_out + ch] = from_f32<ACT>(v * sc + bi);
+        };
+        int t = 0;
+        for (int it = blockIdx.x; it < items; it += gridDim.x, ++t) {
+            int e, nb, ks, kb0, kb1;
+            moe_item(p, it, e, nb, ks, kb0, kb1);
+            const int ch0 = nb * CH + q * 32 + lane;  // this lane's channel
+            const float s0 = to_f32<ACT>(ld_nc_u16(p.scales + ch0));
+            const float b0 = p.bias ? to_f32<ACT>(ld_nc_u16(p.bias + ch0)) : 0.f;
+            const int acc = t & 1;
+            const bool got = mbar_wait_bounded(&bars->tfull[acc], (t >> 1) & 1, abort, p.err, 29, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, got && !*abort))  // tcgen05.ld needs the whole warp
+                break;
+            // split ks's fp32 sums, [row][128 channels]: this lane's channel
+            float* part = p.partial + ((size_t)nb * p.ksplit + ks) * CH * kMoeNT + q * 32 + lane;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Cfg::COLS);
+#pragma unroll 1
+            for (int cc = 0; cc < kMoeNT / 32; ++cc) {
+                const int tok0 = cc * 32;
+                if (tok0 >= cnt)
+                    break;  // warp-uniform
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + (uint32_t)(cc * 32), r);
+                tmem_ld_wait();
+                if (p.ksplit == 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (tok0 + j < cnt)
+                            store_c(tok0 + j, ch0, __uint_as_float(r[j]), s0, b0);
+                } else {
+                    // one 128-byte row of channels per row of C: each store is a
+                    // whole line for the warp
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (tok0 + j < cnt)
+                            __stcg(part + (size_t)(tok0 + j) * 128, __uint_as_float(r[j]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->tempty[acc]);
+            if (p.ksplit == 1)
+                continue;
+            // k split: the split that arrives last at the block's counter sums the
+            // splits in order (the CTA barrier orders every epilogue thread's
+            // stores before the fence that releases them with the count)
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (warp == kEpilogueWarp0 && lane == 0) {
+                if (*abort) {
+                    *is_last = -1;
+                } else {
+                    __threadfence();
+                    const unsigned prev = atomicAdd(p.counters + nb, 1u);
+                    *is_last = prev == (unsigned)(p.ksplit - 1) ? 1 : 0;
+                    if (prev == (unsigned)(p.ksplit - 1))
+                        __threadfence();
+                }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const int last = *is_last;
+            if (last < 0)
+                break;  // every epilogue warp read the same value
+            if (!last)
+                continue;
+            const float* base = p.partial + (size_t)nb * p.ksplit * CH * kMoeNT + q * 32 + lane;
+#pragma unroll 1
+            for (int t0 = 0; t0 < cnt; t0 += 16) {
+                const float* src = base + (size_t)t0 * 128;
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    v[j] = 0.f;
+                // four splits' loads in flight at a time, summed in split order
+#pragma unroll 1
+                for (int sp = 0; sp < p.ksplit; sp += 4) {
+                    float x[4][16];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            x[b][j] = (sp + b < p.ksplit && t0 + j < cnt)
+                                          ? __ldcg(src + (size_t)(sp + b) * CH * kMoeNT + (size_t)j * 128)
+                                          : 0.f;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        if (sp + b < p.ksplit)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                v[j] += x[b][j];
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (t0 + j < cnt)
+                        store_c(t0 + j, ch0, v[j], s0, b0);
+            }
+            if (warp == kEpilogueWarp0 && lane == 0)
+                p.counters[nb] = 0u;  // ready for the next call
+        }
     } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
         // ---- epilogue: lane = channel (TMEM lane quadrant warp % 4), column = token ----
         const int q = warp - kEpilogueWarp0;
@@ -1210,10 +1367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int c = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+            int e, nb, ks, kb0, kb1;
+            moe_item(p, it, e, nb, ks, kb0, kb1);
             int r0, cnt, chunks;
-            moe_rows(p, it / p.nb, r0, cnt, chunks);
+            moe_rows(p, e, r0, cnt, chunks);
             for (int ch = 0; ch < chunks && ok; ++ch) {
-                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                for (int kb = kb0; kb < kb1; ++kb, ++c) {
                     const int sc = c % Cfg::SC, s2 = c % Cfg::S2;
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait_bounded(&bars->fullC[sc], (c / Cfg::SC) & 1, abort, p.err,
@@ -1243,20 +1402,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool GATED, bool WIDE, int ACT>
+template <bool GATED, bool WIDE, bool PLAIN, int ACT>
 cudaError_t launch_moe_tc_t(const CUtensorMap& ma, const CUtensorMap& mc, const MoeTcParams& mp,
                             cudaStream_t s)
 {
-    constexpr int smem = MoeCfg<GATED || WIDE>::SMEM + (int)sizeof(Barriers) + 1024;
+    constexpr int smem = MoeCfg<GATED || WIDE, PLAIN>::SMEM + (int)sizeof(Barriers) + 1024;
     static_assert(smem <= 232448, "shared memory per CTA");
-    auto kern = moe_tc_kernel<GATED, WIDE, ACT>;
+    auto kern = moe_tc_kernel<GATED, WIDE, PLAIN, ACT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
-    const int items = mp.E * mp.nb;
+    const int items = PLAIN ? mp.nb * mp.ksplit : mp.E * mp.nb;
     const int grid = items < num_sms() ? items : num_sms();
-    kern<<<grid, kThreads, smem, s>>>(ma, mc, mp);
-    return cudaGetLastError();
+    if constexpr (!PLAIN) {
+        kern<<<grid, kThreads, smem, s>>>(ma, mc, mp);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mc, mp);
 }
 
 }  // namespace
@@ -1403,13 +1575,85 @@ cudaError_t launch_moe_tc(bool gated, int act, const void* rows, int total_rows,
                       BK * 16 / 4, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     if (gated)
-        return act == WO_F16 ? launch_moe_tc_t<true, false, ACT_F16>(ma, mc, mp, s)
-                             : launch_moe_tc_t<true, false, ACT_BF16>(ma, mc, mp, s);
+        return act == WO_F16 ? launch_moe_tc_t<true, false, false, ACT_F16>(ma, mc, mp, s)
+                             : launch_moe_tc_t<true, false, false, ACT_BF16>(ma, mc, mp, s);
     if (wide)
-        return act == WO_F16 ? launch_moe_tc_t<false, true, ACT_F16>(ma, mc, mp, s)
-                             : launch_moe_tc_t<false, true, ACT_BF16>(ma, mc, mp, s);
-    return act == WO_F16 ? launch_moe_tc_t<false, false, ACT_F16>(ma, mc, mp, s)
-                         : launch_moe_tc_t<false, false, ACT_BF16>(ma, mc, mp, s);
+        return act == WO_F16 ? launch_moe_tc_t<false, true, false, ACT_F16>(ma, mc, mp, s)
+                             : launch_moe_tc_t<false, true, false, ACT_BF16>(ma, mc, mp, s);
+    return act == WO_F16 ? launch_moe_tc_t<false, false, false, ACT_F16>(ma, mc, mp, s)
+                         : launch_moe_tc_t<false, false, false, ACT_BF16>(ma, mc, mp, s);
+}
+
+// ---- 8-bit weights at 17..64 rows: the swap-AB expert kernel as a plain GEMM
+
+MidPlan plan_mid(int m, int n, int k, int bits)
+{
+    MidPlan P{};
+    P.valid = false;
+    if (bits != 8 || m < 1 || m > kMoeNT || n % 128 != 0 || k % BK != 0)
+        return P;
+    // blocks of 128 channels, the MMA's rows.  With more blocks than SMs the
+    // m >= 65 tensor-core kernel (128 x 256 tiles, one MMA per 256 channels
+    // and 16 k) streams the weights faster: this kernel is for the shapes
+    // whose blocks alone leave SMs idle, which it fills by splitting k.
+    P.ch = 128;
+    P.nb = n / P.ch;
+    if (P.nb > num_sms())
+        return P;
+    const int num_kb = k / BK;
+    // as many (block, split) items as fit the SMs one each: an SM that ran a
+    // second item would hold back the block its split belongs to, and the
+    // last split's reduction behind it.  Each split keeps at least 4 k blocks;
+    // at most 8 splits (the last split to arrive reads them all back).
+    int ks = num_sms() / P.nb;
+    const int ks_max = num_kb / 4 > 1 ? num_kb / 4 : 1;
+    if (ks > ks_max)
+        ks = ks_max;
+    if (ks > 8)
+        ks = 8;
+    if (ks < 1)
+        ks = 1;
+    P.kps = (num_kb + ks - 1) / ks;
+    P.ksplit = (num_kb + P.kps - 1) / P.kps;
+    P.ctas = P.nb * P.ksplit;
+    P.partial_bytes = P.ksplit > 1 ? align_up((size_t)P.nb * P.ksplit * P.ch * kMoeNT * 4, 256) : 0;
+    P.ws_bytes = kWsScratch + P.partial_bytes;
+    P.valid = (size_t)P.nb <= kWsCounters;
+    return P;
+}
+
+cudaError_t launch_mid(const GemmArgs& a, cudaStream_t s)
+{
+    const MidPlan P = plan_mid(a.m, a.n, a.k, a.bits);
+    if (!P.valid)
+        return cudaErrorInvalidValue;
+    MoeTcParams mp{};
+    mp.offsets = nullptr;
+    mp.E = 1;
+    mp.nb = P.nb;
+    mp.num_kb = a.k / BK;
+    mp.n_out = a.n;
+    mp.rows_per_expert_w = a.n;
+    mp.scales = static_cast<const uint16_t*>(a.scales);
+    mp.err = static_cast<unsigned*>(a.ws);
+    mp.m = a.m;
+    mp.ksplit = P.ksplit;
+    mp.kps = P.kps;
+    mp.bias = static_cast<const uint16_t*>(a.bias);
+    mp.C = static_cast<uint16_t*>(a.C);
+    char* ws = static_cast<char*>(a.ws);
+    mp.counters = reinterpret_cast<unsigned*>(ws + kWsHeader);
+    mp.partial = P.ksplit > 1 ? reinterpret_cast<float*>(ws + kWsScratch) : nullptr;
+    CUtensorMap ma, mc;
+    if (!make_tmap_2d(&ma, a.act == WO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      a.A, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2, BK, kMoeNT, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const uint64_t row_bytes = (uint64_t)a.k * 16;
+    if (!make_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.B, row_bytes / 4, (uint64_t)a.n / 16, row_bytes,
+                      BK * 16 / 4, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    return a.act == WO_F16 ? launch_moe_tc_t<false, false, true, ACT_F16>(ma, mc, mp, s)
+                           : launch_moe_tc_t<false, false, true, ACT_BF16>(ma, mc, mp, s);
 }
 
 }  // namespace wo

@@ -90,6 +90,19 @@ struct TcPlan {
 TcPlan plan_tc(int m, int n, int k, int group, int bits, int act, bool allow_split = true);
 cudaError_t launch_tc(const GemmArgs& a, const TcPlan& p, cudaStream_t s);
 
+// 8-bit weights at 17..64 rows: the swap-AB expert kernel as a plain GEMM
+// (channel blocks of 128 or 256 by k splits; wo_gemm_tc.cu)
+struct MidPlan {
+    int ch, nb;            // channels per block, blocks
+    int ksplit, kps;       // k splits per block, k blocks per split
+    int ctas;
+    size_t partial_bytes;  // fp32 sums of the splits
+    size_t ws_bytes;       // total, header and counter area included
+    bool valid;
+};
+MidPlan plan_mid(int m, int n, int k, int bits);
+cudaError_t launch_mid(const GemmArgs& a, cudaStream_t s);
+
 // MoE expert GEMMs on the tensor cores (8-bit codes; hidden and inter
 // multiples of 128): gated fc1 -> h [rows, inter] in the activation dtype,
 // or fc2 -> fp32 [rows, n_out]; rows are in expert order, offsets[E + 1].

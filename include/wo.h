@@ -52,7 +52,8 @@ typedef enum {
     WO_ERR_UNSUPPORTED = 2, /* a valid combination this library does not run */
     WO_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
     WO_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
-    WO_ERR_TIMEOUT = 5      /* a kernel gave up a bounded wait (see wo_check_workspace) */
+    WO_ERR_TIMEOUT = 5,     /* a kernel gave up a bounded wait (see wo_check_workspace) */
+    WO_ERR_BOUNDS = 6       /* debug build: an index check failed (see wo_debug_bounds) */
 } wo_status;
 
 typedef enum { WO_F16 = 0, WO_BF16 = 1 } wo_dtype;
@@ -332,6 +333,21 @@ WO_API wo_status wo_noalloc_check(void* stream);
  * again before its next use.
  */
 WO_API wo_status wo_check_workspace(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Index checks of the debug build (no counterpart on the pages; a stand-in
+ * for a memory checker, which this project's GPUs do not offer).  A library
+ * compiled with -DWO_DEBUG_BOUNDS=1 checks every global index its kernels
+ * compute (plain loads and stores; TMA boxes are clipped by the hardware)
+ * against the extent of the buffer; a failed check skips the access and
+ * records a site code (0x100-0x7ff, the kernel family in the high digit) in
+ * a device word instead of faulting.  This call waits for the device, then
+ * reads and clears those words: WO_OK if no check failed since the last
+ * call, WO_ERR_BOUNDS with the first failed check's site in *site (may be
+ * NULL); WO_ERR_UNSUPPORTED from a library built without the checks;
+ * WO_ERR_CUDA if the device reported an error.
+ */
+WO_API wo_status wo_debug_bounds(unsigned* site);
 
 /*
  * Self-test of the failure path (no counterpart on the pages): launches one

@@ -318,3 +318,27 @@ def test_moe_workspace_size_invalid_is_zero(lib):
     assert wo.wo_moe_workspace_size(16, 4096, 1408, 2, 3) == 0
     assert wo.wo_moe_workspace_size(1024, 4096, 1408, 64, 2) > \
         wo.wo_moe_workspace_size(16, 4096, 1408, 64, 2)
+
+
+def test_debug_bounds_entry_in_a_normal_build(lib):
+    # a library built without the index checks says so, touching no GPU
+    assert wo.wo_status_string(6) == "WO_ERR_BOUNDS"
+    assert wo.wo_debug_bounds() == (2, 0)  # WO_ERR_UNSUPPORTED
+    lib.wo_debug_bounds.argtypes = [ctypes.c_void_p]
+    assert lib.wo_debug_bounds(None) == 2  # site may be NULL
+    lib.wo_debug_bounds.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+
+
+def test_index_checked_build_compiles_and_is_selected_by_the_environment(monkeypatch):
+    # the -DWO_DEBUG_BOUNDS=1 library builds beside the normal one, exports the
+    # same entry points, and WO_DEBUG_BOUNDS=1 selects it at load time
+    path = wo_build.build(debug_bounds=True)
+    assert path == wo_build.LIB_DEBUG_BOUNDS and os.path.exists(path)
+    assert path != wo_build.LIB
+    dbg = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    monkeypatch.setenv("WO_DEBUG_BOUNDS", "1")
+    assert wo.library_path() == wo_build.LIB_DEBUG_BOUNDS
+    monkeypatch.delenv("WO_DEBUG_BOUNDS")
+    assert wo.library_path() == wo_build.LIB

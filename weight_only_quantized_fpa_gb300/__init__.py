@@ -32,7 +32,7 @@ WO_F16 = 0
 WO_BF16 = 1
 
 _STATUS = {0: "WO_OK", 1: "WO_ERR_INVALID_ARG", 2: "WO_ERR_UNSUPPORTED",
-           3: "WO_ERR_WORKSPACE", 4: "WO_ERR_CUDA", 5: "WO_ERR_TIMEOUT"}
+           3: "WO_ERR_WORKSPACE", 4: "WO_ERR_CUDA", 5: "WO_ERR_TIMEOUT", 6: "WO_ERR_BOUNDS"}
 
 
 class WoError(RuntimeError):
@@ -45,8 +45,13 @@ _lock = threading.Lock()
 _lib = None
 
 
+def debug_bounds_requested() -> bool:
+    """WO_DEBUG_BOUNDS=1 in the environment selects the index-checked build."""
+    return os.environ.get("WO_DEBUG_BOUNDS", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_DEBUG_BOUNDS if debug_bounds_requested() else _build.LIB
 
 
 def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
@@ -57,13 +62,13 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB
+        path = library_path()
         if not os.path.exists(path):
             if not build_if_missing:
                 raise RuntimeError(
                     f"libwo.so is not built ({path}); run "
                     "`python -c 'import __graft_entry__ as g; g.build()'` first")
-            _build.build()
+            _build.build(debug_bounds=debug_bounds_requested())
         lib = ctypes.CDLL(path)
         P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         lib.wo_status_string.argtypes = [I]
@@ -104,6 +109,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.wo_noalloc_check.restype = I
         lib.wo_noalloc_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
         lib.wo_noalloc_selftest_wait_timeout.restype = I
+        lib.wo_debug_bounds.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.wo_debug_bounds.restype = I
         _lib = lib
         return lib
 
@@ -285,6 +292,15 @@ def wo_noalloc_check(stream=None) -> int:
     """Synchronise and return the status the kernels left in the built-in
     scratch of wo_gemm_tc_noalloc (the word is cleared)."""
     return int(load_library().wo_noalloc_check(_stream_ptr(stream)))
+
+
+def wo_debug_bounds() -> tuple[int, int]:
+    """(status, site) of the index checks since the last call: (WO_OK, 0), or
+    WO_ERR_BOUNDS with the first failing check's site; WO_ERR_UNSUPPORTED in
+    a library built without them.  Waits for the device; clears the words."""
+    site = ctypes.c_uint(0)
+    st = int(load_library().wo_debug_bounds(ctypes.byref(site)))
+    return st, int(site.value)
 
 
 def wo_noalloc_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -16,6 +16,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libwo.so")
+# the index-checked debug build (-DWO_DEBUG_BOUNDS=1): every computed global
+# index is checked against its buffer's extent, failures recorded, not
+# trapped (csrc/wo_bounds.cuh); loaded instead of LIB when the environment
+# sets WO_DEBUG_BOUNDS=1
+BUILD_DEBUG_BOUNDS = os.path.join(BUILD, "debug_bounds")
+LIB_DEBUG_BOUNDS = os.path.join(BUILD_DEBUG_BOUNDS, "libwo_debug_bounds.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -51,16 +57,21 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          debug_bounds: bool = False) -> str:
+    out_dir = BUILD_DEBUG_BOUNDS if debug_bounds else BUILD
+    lib_path = LIB_DEBUG_BOUNDS if debug_bounds else LIB
+    os.makedirs(out_dir, exist_ok=True)
     deps = _deps()
-    if not force and not _stale(LIB, deps):
-        return LIB
+    if not force and not _stale(lib_path, deps):
+        return lib_path
     cc = nvcc()
     flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE] + (extra_flags or [])
+    if debug_bounds:
+        flags = flags + ["-DWO_DEBUG_BOUNDS=1"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(out_dir, os.path.basename(src).replace(".cu", ".o"))
         cmd = [cc, *flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -74,15 +85,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug_bounds="--debug-bounds" in sys.argv))

@@ -11,6 +11,7 @@
 // ordinary group-wise kernels run on the sorted operands.
 #include <atomic>
 
+#include "wo_bounds.cuh"
 #include "wo_internal.h"
 
 namespace wo {
@@ -67,9 +68,10 @@ __global__ void __launch_bounds__(kGatherThreads)
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = (unsigned)idx[2 * i] < (unsigned)k ? ld_cg_u16(a + idx[2 * i]) : 0u;
+            const uint32_t lo =
+                in_bounds((unsigned)idx[2 * i] < (unsigned)k, 0x601) ? ld_cg_u16(a + idx[2 * i]) : 0u;
             const uint32_t hi =
-                (unsigned)idx[2 * i + 1] < (unsigned)k ? ld_cg_u16(a + idx[2 * i + 1]) : 0u;
+                in_bounds((unsigned)idx[2 * i + 1] < (unsigned)k, 0x601) ? ld_cg_u16(a + idx[2 * i + 1]) : 0u;
             w[i] = lo | (hi << 16);
         }
         *reinterpret_cast<uint4*>(Ap + (size_t)r * k + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(kGatherSmemThreads)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int j = tid; j < k; j += kGatherSmemThreads) {
         const int v = __ldg(perm + j);
-        pos[j] = (uint16_t)((unsigned)v < (unsigned)k ? v : k);
+        pos[j] = (uint16_t)(in_bounds((unsigned)v < (unsigned)k, 0x602) ? v : k);
     }
     if (tid < 8)
         row[k + tid] = 0;
@@ -189,5 +191,7 @@ cudaError_t launch_gather_cols(const void* A, const int32_t* perm, void* Ap, int
     return cudaLaunchKernelEx(&cfg, act_order_gather_kernel, static_cast<const uint16_t*>(A), perm,
                               static_cast<uint16_t*>(Ap), m, k);
 }
+
+unsigned bounds_take_act_order() { return bounds_take_local(); }
 
 }  // namespace wo

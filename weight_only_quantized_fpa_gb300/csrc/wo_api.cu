@@ -179,8 +179,34 @@ const char* wo_status_string(wo_status s)
     case WO_ERR_WORKSPACE: return "WO_ERR_WORKSPACE";
     case WO_ERR_CUDA: return "WO_ERR_CUDA";
     case WO_ERR_TIMEOUT: return "WO_ERR_TIMEOUT";
+    case WO_ERR_BOUNDS: return "WO_ERR_BOUNDS";
     }
     return "WO_ERR_UNKNOWN";
+}
+
+wo_status wo_debug_bounds(unsigned* site)
+{
+#if !defined(WO_DEBUG_BOUNDS) || !WO_DEBUG_BOUNDS
+    if (site)
+        *site = 0;
+    return WO_ERR_UNSUPPORTED;
+#else
+    if (site)
+        *site = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return WO_ERR_CUDA;
+    // every translation unit's word is read (and so cleared); the first
+    // non-zero one is reported
+    const unsigned words[] = {bounds_take_stream(), bounds_take_gemv(),      bounds_take_gemm_tc(),
+                              bounds_take_pack(),   bounds_take_act_order(), bounds_take_moe()};
+    for (unsigned w : words)
+        if (w) {
+            if (site)
+                *site = w;
+            return WO_ERR_BOUNDS;
+        }
+    return WO_OK;
+#endif
 }
 
 size_t wo_packed_bytes(int n, int k, int bits)

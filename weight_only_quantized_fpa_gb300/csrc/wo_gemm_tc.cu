@@ -58,6 +58,7 @@
 // activation is in range; only values more than 2^24 below their channel's
 // (or row's) largest fall into fp16's subnormals, where their share of the
 // sum is below the output's rounding.
+#include "wo_bounds.cuh"
 #include "wo_common.cuh"
 #include "wo_internal.h"
 #include "wo_sm100.cuh"
@@ -122,6 +123,7 @@ struct TcParams {
     int c_v8;                // C 32-byte aligned (and n % 16 == 0): 32-byte stores
     int splits;              // k split: units per output tile (1: none)
     float* partial;          // splits > 1: fp32 partial tiles, [tile * splits + s][h][BN / 32][128][32]
+    size_t partial_floats;   // its extent (index checks of the debug build)
     unsigned* counters;      // splits > 1: per-tile arrival counters (kept at zero between calls)
     unsigned* err;           // workspace error word
 };
@@ -176,7 +178,8 @@ __device__ __forceinline__ void load_scales(const TcParams& p, int n0, int kb, i
             const int ch = n0 + nb * 16 + g;
             c.lo[r] = 0u;
             c.hi[r] = 0u;
-            if (ch < p.n) {  // n is a multiple of 16: row ch + 8 is in range too
+            if (ch < p.n && in_bounds((size_t)(ch + 8) * p.G + gi < (size_t)p.n * p.G, 0x301)) {
+                // n is a multiple of 16: row ch + 8 is in range too
                 const size_t lo = (size_t)ch * p.G + gi;
                 c.lo[r] = ld_nc_u32(p.sz + lo);
                 c.hi[r] = ld_nc_u32(p.sz + lo + (size_t)8 * p.G);
@@ -380,6 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             packed[j] = (uint32_t)from_f32<ACT>(v0) | ((uint32_t)from_f32<ACT>(v1) << 16);
         }
+        if (!in_bounds(row < p.m && nc >= 0 && nc + 32 <= p.n, 0x302))
+            return;
         uint16_t* dst = p.C + (size_t)row * p.n + nc;
         if (p.c_v8) {  // two 32-byte stores: whole sectors
 #pragma unroll
@@ -565,6 +570,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // [h][cc][row of the sub-tile][32]: a warp writes 4 KiB contiguously
                         float4* dst = reinterpret_cast<float4*>(
                             part + ((size_t)(h * (BN / 32) + cc) * BM + q * 32 + lane) * 32);
+                        if (!in_bounds((size_t)(reinterpret_cast<float*>(dst) - p.partial) + 32 <= p.partial_floats,
+                                       0x303))
+                            continue;
 #pragma unroll
                         for (int w = 0; w < 8; ++w)
                             dst[w] = make_float4(__uint_as_float(r[4 * w]), __uint_as_float(r[4 * w + 1]),
@@ -579,7 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort) {
                     *is_last = -1;
                 } else {
-                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
+                    const unsigned prev =
+                        in_bounds(tile < (int)kWsCounters, 0x304) ? atomicAdd(p.counters + tile, 1u) : 0u;
                     *is_last = prev == (unsigned)(splits - 1) ? 1 : 0;
                 }
             }
@@ -609,9 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j)
                             v[j] = 0.f;
                         // split 0's block: this warp's 32 rows x 32 floats, 4 KB
-                        split_sum(p.partial + (size_t)tile * splits * TM * BN +
-                                      ((size_t)(h * (BN / 32) + cc) * BM + q * 32) * 32,
-                                  (size_t)TM * BN, splits, stg, lane, v);
+                        const size_t blk0 = (size_t)tile * splits * TM * BN +
+                                            ((size_t)(h * (BN / 32) + cc) * BM + q * 32) * 32;
+                        if (in_bounds(blk0 + (size_t)(splits - 1) * TM * BN + 32 * 32 <= p.partial_floats, 0x305))
+                            split_sum(p.partial + blk0, (size_t)TM * BN, splits, stg, lane, v);
                         uint32_t sc[16], bi[16];
                         gather(cc, sc, bi);
                         if (row < p.m)
@@ -1012,6 +1022,8 @@ struct MoeTcParams {
     const uint16_t* bias;    // [n_out] or null
     uint16_t* C;             // [m, n_out]
     float* partial;          // ksplit > 1: [nb][ksplit][kMoeNT rows][128 channels] fp32
+    size_t partial_floats;   // its extent (index checks of the debug build)
+    int rows_total;          // rows of H / Y (MoE) or C (plain)
     unsigned* counters;      // ksplit > 1: [nb], zero between calls
 };
 
@@ -1207,15 +1219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cnt = p.m;
         // this lane's channel as round(v * s + b) into row `row` of C
         auto store_c = [&](int row, int ch, float v, float sc, float bi) {
-            p.C[(size_t)row * p.n_out + ch] = from_f32<ACT>(v * sc + bi);
+            if (in_bounds(row < p.m && ch < p.n_out, 0x401))
+                p.C[(size_t)row * p.n_out + ch] = from_f32<ACT>(v * sc + bi);
         };
         int t = 0;
         for (int it = blockIdx.x; it < items; it += gridDim.x, ++t) {
             int e, nb, ks, kb0, kb1;
             moe_item(p, it, e, nb, ks, kb0, kb1);
             const int ch0 = nb * CH + q * 32 + lane;  // this lane's channel
-            const float s0 = to_f32<ACT>(ld_nc_u16(p.scales + ch0));
-            const float b0 = p.bias ? to_f32<ACT>(ld_nc_u16(p.bias + ch0)) : 0.f;
+            const bool ch_ok = in_bounds(ch0 < p.n_out, 0x402);
+            const float s0 = ch_ok ? to_f32<ACT>(ld_nc_u16(p.scales + ch0)) : 0.f;
+            const float b0 = p.bias && ch_ok ? to_f32<ACT>(ld_nc_u16(p.bias + ch0)) : 0.f;
             const int acc = t & 1;
             const bool got = mbar_wait_bounded(&bars->tfull[acc], (t >> 1) & 1, abort, p.err, 29, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, got && !*abort))  // tcgen05.ld needs the whole warp
@@ -1242,7 +1256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // whole line for the warp
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (tok0 + j < cnt)
+                        if (tok0 + j < cnt &&
+                            in_bounds((size_t)(part - p.partial) + (size_t)(tok0 + j) * 128 < p.partial_floats, 0x403))
                             __stcg(part + (size_t)(tok0 + j) * 128, __uint_as_float(r[j]));
                 }
             }
@@ -1259,7 +1274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *is_last = -1;
                 } else {
                     __threadfence();
-                    const unsigned prev = atomicAdd(p.counters + nb, 1u);
+                    const unsigned prev =
+                        in_bounds(nb < (int)kWsCounters, 0x404) ? atomicAdd(p.counters + nb, 1u) : 0u;
                     *is_last = prev == (unsigned)(p.ksplit - 1) ? 1 : 0;
                     if (prev == (unsigned)(p.ksplit - 1))
                         __threadfence();
@@ -1287,7 +1303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int b = 0; b < 4; ++b)
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            x[b][j] = (sp + b < p.ksplit && t0 + j < cnt)
+                            x[b][j] = (sp + b < p.ksplit && t0 + j < cnt &&
+                                       in_bounds((size_t)(src - p.partial) + (size_t)(sp + b) * CH * kMoeNT +
+                                                         (size_t)j * 128 < p.partial_floats, 0x405))
                                           ? __ldcg(src + (size_t)(sp + b) * CH * kMoeNT + (size_t)j * 128)
                                           : 0.f;
 #pragma unroll
@@ -1315,8 +1333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             moe_rows(p, e, r0, cnt, chunks);
             const int chl = nb * CH + q * 32 + lane;  // output channel within the expert
             const uint16_t* se = p.scales + (size_t)e * p.rows_per_expert_w;
-            const float s0 = to_f32<ACT>(ld_nc_u16(se + chl));
-            const float s1 = TWO ? to_f32<ACT>(ld_nc_u16(se + (GATED ? p.inter : 128) + chl)) : 0.f;
+            const bool ch_ok = in_bounds((GATED ? p.inter : 128) * (TWO ? 1 : 0) + chl < p.rows_per_expert_w, 0x406);
+            const float s0 = ch_ok ? to_f32<ACT>(ld_nc_u16(se + chl)) : 0.f;
+            const float s1 = TWO && ch_ok ? to_f32<ACT>(ld_nc_u16(se + (GATED ? p.inter : 128) + chl)) : 0.f;
             bool ok = true;
             for (int ch = 0; ch < chunks; ++ch, ++t) {
                 const int acc = t & 1;
@@ -1340,7 +1359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if (tok0 + j < cnt) {  // rows past the expert's range are not its own
+                        if (tok0 + j < cnt &&  // rows past the expert's range are not its own
+                            in_bounds(r0 + tok0 + j < p.rows_total &&
+                                          chl + (WIDE ? 128 : 0) < (GATED ? p.inter : p.n_out), 0x407)) {
                             const size_t row = (size_t)(r0 + tok0 + j);
                             const float g = __uint_as_float(r[j]) * s0;
                             if constexpr (GATED) {
@@ -1498,6 +1519,7 @@ cudaError_t launch_tc(const GemmArgs& a, const TcPlan& plan, cudaStream_t s)
     char* const cs_at = sz_at + plan.sz_bytes;
     char* const part_at = cs_at + plan.colscale_bytes;
     tp.partial = plan.splits > 1 ? reinterpret_cast<float*>(part_at) : nullptr;
+    tp.partial_floats = plan.splits > 1 ? plan.partial_bytes / 4 : 0;
     // stream the larger operand once (A: m*k*2 bytes, codes: n*k*bits/8)
     tp.m_fast = (double)a.m * 2.0 <= (double)a.n * a.bits / 8.0;
 
@@ -1561,6 +1583,7 @@ cudaError_t launch_moe_tc(bool gated, int act, const void* rows, int total_rows,
     mp.scales = static_cast<const uint16_t*>(scales);
     mp.H = gated ? static_cast<uint16_t*>(out) : nullptr;
     mp.Y = gated ? nullptr : static_cast<float*>(out);
+    mp.rows_total = total_rows;
     mp.err = err;
     // token rows: [total_rows, k], kMoeNT x 64 boxes, 128-byte swizzle
     CUtensorMap ma, mc;
@@ -1644,6 +1667,8 @@ cudaError_t launch_mid(const GemmArgs& a, cudaStream_t s)
     char* ws = static_cast<char*>(a.ws);
     mp.counters = reinterpret_cast<unsigned*>(ws + kWsHeader);
     mp.partial = P.ksplit > 1 ? reinterpret_cast<float*>(ws + kWsScratch) : nullptr;
+    mp.partial_floats = P.ksplit > 1 ? P.partial_bytes / 4 : 0;
+    mp.rows_total = a.m;
     CUtensorMap ma, mc;
     if (!make_tmap_2d(&ma, a.act == WO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       a.A, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2, BK, kMoeNT, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -1655,5 +1680,7 @@ cudaError_t launch_mid(const GemmArgs& a, cudaStream_t s)
     return a.act == WO_F16 ? launch_moe_tc_t<false, false, true, ACT_F16>(ma, mc, mp, s)
                            : launch_moe_tc_t<false, false, true, ACT_BF16>(ma, mc, mp, s);
 }
+
+unsigned bounds_take_gemm_tc() { return bounds_take_local(); }
 
 }  // namespace wo

@@ -57,6 +57,7 @@
 // that runs out records an error word in the workspace and the CTA winds
 // down without a hang (every consumer warp still passes every named
 // barrier, skipping the work).
+#include "wo_bounds.cuh"
 #include "wo_common.cuh"
 #include "wo_internal.h"
 #include "wo_sm100.cuh"
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
             for (int h = 0; h < 2; ++h) {
                 const int ch = (blk + r) * 16 + g + 8 * h;
                 ps[r][h] = pz[r][h] = 0.f;
-                if (!GROUPED && active) {
+                if (!GROUPED && active && in_bounds(ch < p.N, 0x201)) {
                     const float sv = to_f32<ACT>(ld_nc_u16(p.scales + ch));
                     const float zv = p.zeros ? to_f32<ACT>(ld_nc_u16(p.zeros + ch)) : 0.f;
                     ps[r][h] = sv;
@@ -448,7 +449,9 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
         for (int r = 0; r < 2; ++r)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                bb[r][h] = p.bias ? to_f32<ACT>(ld_nc_u16(p.bias + (blk + r) * 16 + g + 8 * h)) : 0.f;
+                bb[r][h] = p.bias && in_bounds((blk + r) * 16 + g + 8 * h < p.N, 0x202)
+                               ? to_f32<ACT>(ld_nc_u16(p.bias + (blk + r) * 16 + g + 8 * h))
+                               : 0.f;
 #pragma unroll
         for (int j = 0; j < MT; ++j)
 #pragma unroll
@@ -459,7 +462,8 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int ch = (blk + r) * 16 + g + 8 * (q >> 1);
-                    p.C[(size_t)row * p.N + ch] = from_f32<ACT>(fin[r][j][q] + bb[r][q >> 1]);
+                    if (in_bounds(ch < p.N, 0x203))
+                        p.C[(size_t)row * p.N + ch] = from_f32<ACT>(fin[r][j][q] + bb[r][q >> 1]);
                 }
             }
     };
@@ -500,7 +504,8 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
         const int wf = worker_of(su0, p.T, P);
         const int nseg = worker_of(su0 + p.nst - 1, p.T, P) - wf + 1;
         const float* base = p.partial + ((size_t)strip * p.maxseg * CH + (size_t)(32 * warp + lane)) * NV;
-        if (ok) {
+        if (ok && in_bounds(strip < p.nstrips && (int)blockIdx.x - wf >= 0 && (int)blockIdx.x - wf < p.maxseg &&
+                                nseg <= p.maxseg, 0x204)) {
             float4* dst = reinterpret_cast<float4*>(const_cast<float*>(base) + (size_t)((int)blockIdx.x - wf) * CH * NV);
 #pragma unroll
             for (int r = 0; r < 2; ++r)
@@ -514,7 +519,7 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
         asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");
         if (threadIdx.x == 0) {
             int last = 0;
-            if (!*abort) {
+            if (!*abort && in_bounds(strip < p.nstrips, 0x206)) {
                 __threadfence();
                 last = atomicAdd(p.counters + strip, 1u) == (unsigned)(nseg - 1) ? 1 : 0;
                 if (last)
@@ -540,7 +545,7 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
             for (int b = 0; b < RB; ++b)
 #pragma unroll
                 for (int v = 0; v < 2 * MT; ++v)
-                    x[b][v] = j0 + b < nseg
+                    x[b][v] = j0 + b < nseg && in_bounds(j0 + b < p.maxseg, 0x205)
                                   ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)(j0 + b) * CH * NV) + v)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -882,5 +887,7 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t s)
         return cudaErrorInvalidValue;
     return a.act == WO_F16 ? launch_gemv_a<ACT_F16>(a, plan, s) : launch_gemv_a<ACT_BF16>(a, plan, s);
 }
+
+unsigned bounds_take_gemv() { return bounds_take_local(); }
 
 }  // namespace wo

@@ -30,6 +30,16 @@ int num_sms();  // SM count of the current device (152 when none is visible)
 // gives up after limit_us and records its code in *err (wo_selftest.cu)
 cudaError_t launch_wait_timeout(unsigned* err, unsigned limit_us, cudaStream_t s);
 
+// Index checks of the debug build (wo_bounds.cuh): each translation unit's
+// first failed site since the last call, cleared; 0 for none (always 0 in a
+// build without the checks).
+unsigned bounds_take_stream();
+unsigned bounds_take_gemv();
+unsigned bounds_take_gemm_tc();
+unsigned bounds_take_pack();
+unsigned bounds_take_act_order();
+unsigned bounds_take_moe();
+
 // ---- pack -----------------------------------------------------------------
 // perm (pack only, optional): packed column j takes row-major column perm[j]
 cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits, bool unpack,

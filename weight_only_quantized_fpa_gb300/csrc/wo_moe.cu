@@ -27,6 +27,7 @@
 // take several passes over their weights.
 #include <cuda_runtime.h>
 
+#include "wo_bounds.cuh"
 #include "wo_common.cuh"
 #include "wo_internal.h"
 #include "wo_stream.h"
@@ -183,10 +184,10 @@ __global__ void __launch_bounds__(kSortWarps * 32)
         const unsigned same = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(same & ((1u << lane) - 1u));
         int p = 0;
-        if (ok)
+        if (ok && in_bounds(e >= 0 && e < E, 0x701))
             p = off[e] + my[e] + rank;
         __syncwarp();
-        if (ok) {
+        if (ok && in_bounds(e >= 0 && e < E && p < P, 0x702)) {
             pos[slot] = p;
             perm_tok[p] = slot / topk;
             if (rank == __popc(same) - 1)  // last lane of this expert's group
@@ -198,9 +199,11 @@ __global__ void __launch_bounds__(kSortWarps * 32)
 
 // A rows in expert order: a_sorted[p] = A[perm_tok[p]] (16-byte pieces).
 __global__ void gather_rows_kernel(const uint4* __restrict__ A, const int* __restrict__ perm_tok,
-                                   uint4* __restrict__ a_sorted, int row_vecs)
+                                   uint4* __restrict__ a_sorted, int row_vecs, int T)
 {
     const int p = blockIdx.x;
+    if (!in_bounds(perm_tok[p] >= 0 && perm_tok[p] < T, 0x703))
+        return;
     const uint4* src = A + (size_t)perm_tok[p] * row_vecs;
     uint4* dst = a_sorted + (size_t)p * row_vecs;
     for (int i = threadIdx.x; i < row_vecs; i += blockDim.x)
@@ -210,13 +213,15 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ A, const int* __res
 template <int ACT>
 __global__ void combine_kernel(const float* __restrict__ Y, const int* __restrict__ pos,
                                const float* __restrict__ wts, uint16_t* __restrict__ out,
-                               int hidden, int topk)
+                               int hidden, int topk, int P)
 {
     const int tok = blockIdx.x;
     for (int c = threadIdx.x; c < hidden; c += blockDim.x) {
         float v = 0.f;
         for (int j = 0; j < topk; ++j) {
             const int p = pos[(size_t)tok * topk + j];
+            if (!in_bounds(p >= 0 && p < P, 0x704))
+                continue;
             v = fmaf(wts[(size_t)tok * topk + j], Y[(size_t)p * hidden + c], v);
         }
         out[(size_t)tok * hidden + c] = from_f32<ACT>(v);
@@ -253,7 +258,7 @@ cudaError_t launch_moe(const void* A, const float* logits, const uint8_t* fc1, c
         return err;
 
     gather_rows_kernel<<<P, 128, 0, s>>>(static_cast<const uint4*>(A), perm_tok,
-                                         reinterpret_cast<uint4*>(a_sorted), H / 8);
+                                         reinterpret_cast<uint4*>(a_sorted), H / 8, T);
     if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
 
@@ -266,7 +271,7 @@ cudaError_t launch_moe(const void* A, const float* logits, const uint8_t* fc1, c
         if ((err = launch_moe_tc(false, ACT, h, P, I, fc2, fc2_s, E, H, 0, offsets, y, errw, s)) !=
             cudaSuccess)
             return err;
-        combine_kernel<ACT><<<T, 256, 0, s>>>(y, pos, wts, static_cast<uint16_t*>(out), H, topk);
+        combine_kernel<ACT><<<T, 256, 0, s>>>(y, pos, wts, static_cast<uint16_t*>(out), H, topk, P);
         return cudaGetLastError();
     }
 
@@ -320,13 +325,16 @@ cudaError_t launch_moe(const void* A, const float* logits, const uint8_t* fc1, c
     if ((err = launch_stream(p2, P2, 8, ACT, OUT_F32, E, s)) != cudaSuccess)
         return err;
 
-    combine_kernel<ACT><<<T, 256, 0, s>>>(y, pos, wts, static_cast<uint16_t*>(out), H, topk);
+    combine_kernel<ACT><<<T, 256, 0, s>>>(y, pos, wts, static_cast<uint16_t*>(out), H, topk, P);
     return cudaGetLastError();
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+unsigned bounds_take_moe() { return bounds_take_local(); }
+
 }  // namespace wo
 
 using namespace wo;

@@ -12,6 +12,7 @@
 // inverse the two nibbles of a row-major byte (k even and k + 1) come from
 // the same lane word (registers R and R + 4 of the layout), so no two threads
 // share a destination byte.
+#include "wo_bounds.cuh"
 #include "wo_common.cuh"
 #include "wo_internal.h"
 
@@ -62,8 +63,9 @@ __global__ void pack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict
                     int kg = kt * KT + kk;
                     if (perm)
                         kg = perm[kg];
-                    const uint32_t v =
-                        (unsigned)kg < (unsigned)k ? src[(size_t)(nb * 16 + row) * k + kg] : 0u;
+                    const uint32_t v = (unsigned)kg < (unsigned)k && in_bounds(nb * 16 + row < n, 0x501)
+                                           ? src[(size_t)(nb * 16 + row) * k + kg]
+                                           : 0u;
                     w |= v << (8 * j);
                 }
                 words[wi] = w;
@@ -78,8 +80,9 @@ __global__ void pack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict
                     int kg = kt * KT + kk;
                     if (perm)
                         kg = perm[kg];
-                    const uint8_t byte =
-                        (unsigned)kg < (unsigned)k ? src[(size_t)(nb * 16 + row) * kb + kg / 2] : 0;
+                    const uint8_t byte = (unsigned)kg < (unsigned)k && in_bounds(nb * 16 + row < n, 0x501)
+                                             ? src[(size_t)(nb * 16 + row) * kb + kg / 2]
+                                             : 0;
                     const uint32_t q = (kg & 1) ? (byte >> 4) : (byte & 0x0F);
                     w |= q << (4 * p);
                 }
@@ -110,8 +113,8 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
             for (int b = 0; b < 16; ++b) {
                 int row, kk;
                 u8_coord(b, g, t, row, kk);
-                dst[(size_t)(nb * 16 + row) * k + kt * KT + kk] =
-                    (uint8_t)(words[b >> 2] >> (8 * (b & 3)));
+                if (in_bounds(nb * 16 + row < n && kt * KT + kk < k, 0x502))
+                    dst[(size_t)(nb * 16 + row) * k + kt * KT + kk] = (uint8_t)(words[b >> 2] >> (8 * (b & 3)));
             }
         } else {
             const int kb = k / 2;
@@ -121,8 +124,8 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
                     u4_coord(s, p, g, t, row, kk);
                     const uint32_t lo = (words[s] >> (4 * p)) & 0xF;
                     const uint32_t hi = (words[s] >> (4 * (p + 4))) & 0xF;
-                    dst[(size_t)(nb * 16 + row) * kb + (kt * KT + kk) / 2] =
-                        (uint8_t)(lo | (hi << 4));
+                    if (in_bounds(nb * 16 + row < n && kt * KT + kk < k, 0x502))
+                        dst[(size_t)(nb * 16 + row) * kb + (kt * KT + kk) / 2] = (uint8_t)(lo | (hi << 4));
                 }
             }
         }
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kEmbedWarps * 32)
             const int kt = sg * kEmbedTiles + (lane >> 2) + 8 * j;
             vj[j] = make_uint4(0u, 0u, 0u, 0u);
             scj[j] = zcj[j] = 0.f;
-            if (valid && kt < ktiles) {
+            if (valid && kt < ktiles && in_bounds((size_t)id * G + (size_t)(kt * KT) / group < (size_t)vocab * G, 0x503)) {
                 vj[j] = *reinterpret_cast<const uint4*>(
                     B + ((((size_t)(id / 16) * ktiles + kt) * 32 + 4 * g + t4) * 16));
                 // one scale (and zero) per k tile: groups are whole tiles or more
@@ -223,7 +226,8 @@ __global__ void __launch_bounds__(kEmbedWarps * 32)
         uint4* dst = reinterpret_cast<uint4*>(out + (size_t)tok * hidden + (size_t)sg * SEG);
         const uint4* src = reinterpret_cast<const uint4*>(seg);
         for (int i = lane; i < nvals / 8; i += 32)
-            dst[i] = src[i];
+            if (in_bounds(tok < T && (size_t)sg * SEG + (size_t)(i + 1) * 8 <= (size_t)hidden, 0x504))
+                dst[i] = src[i];
         __syncwarp();
     }
 }
@@ -288,5 +292,7 @@ cudaError_t launch_pack(const uint8_t* src, uint8_t* dst, int n, int k, int bits
     }
     return cudaGetLastError();
 }
+
+unsigned bounds_take_pack() { return bounds_take_local(); }
 
 }  // namespace wo

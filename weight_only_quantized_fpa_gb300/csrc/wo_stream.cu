@@ -44,6 +44,7 @@
 // the CTA winds down (the producer first lets its copies in flight land).
 #include <cooperative_groups.h>
 
+#include "wo_bounds.cuh"
 #include "wo_common.cuh"
 #include "wo_internal.h"
 #include "wo_sm100.cuh"
@@ -138,8 +139,9 @@ __device__ __forceinline__ PlainEpi load_plain_epi(const StreamParams& p, const 
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int ch = blk[r] * 16 + g + 8 * h;
-            e.s[r][h] = GROUPED ? 1.f : to_f32<ACT>(ld_nc_u16(sx + ch));
-            e.b[r][h] = p.bias ? to_f32<ACT>(ld_nc_u16(p.bias + ch)) : 0.f;
+            const bool ok = in_bounds(ch < p.N, 0x101);
+            e.s[r][h] = GROUPED || !ok ? 1.f : to_f32<ACT>(ld_nc_u16(sx + ch));
+            e.b[r][h] = p.bias && ok ? to_f32<ACT>(ld_nc_u16(p.bias + ch)) : 0.f;
         }
     return e;
 }
@@ -163,6 +165,8 @@ __device__ __forceinline__ void stream_epilogue(const StreamParams& p, const flo
             if constexpr (OUT == OUT_GATED) {
                 const int ch0 = blk[0] * 16 + g + 8 * (q >> 1);
                 const int ch1 = blk[1] * 16 + g + 8 * (q >> 1);
+                if (!in_bounds(ch0 < p.inter && ch1 < p.N && row < (size_t)p.a_rows_total, 0x102))
+                    continue;
                 const float gate = acc[0][j][q] * to_f32<ACT>(ld_nc_u16(sx + ch0));
                 const float up = acc[1][j][q] * to_f32<ACT>(ld_nc_u16(sx + ch1));
                 p.C[row * p.inter + ch0] = from_f32<ACT>(gate / (1.f + expf(-gate)) * up);
@@ -170,6 +174,8 @@ __device__ __forceinline__ void stream_epilogue(const StreamParams& p, const flo
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int ch = blk[r] * 16 + g + 8 * (q >> 1);
+                    if (!in_bounds(ch < p.N && row < (size_t)p.a_rows_total, 0x103))
+                        continue;
                     float v = acc[r][j][q];
                     if constexpr (OUT == OUT_PLAIN) {
                         if constexpr (!GROUPED)
@@ -351,9 +357,11 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                     if (idx < 32 * gc) {
                         const int ch = idx / gc, gg = idx % gc;
                         const size_t src = (size_t)(blk[ch >> 4] * 16 + (ch & 15)) * p.G + g_lo + gg;
-                        sv[b] = ld_nc_u16(sx + src);
-                        if (p.zeros)
-                            zv[b] = ld_nc_u16(p.zeros + src);
+                        if (in_bounds(src < (size_t)p.N * p.G, 0x104)) {
+                            sv[b] = ld_nc_u16(sx + src);
+                            if (p.zeros)
+                                zv[b] = ld_nc_u16(p.zeros + src);
+                        }
                     }
                 }
 #pragma unroll
@@ -782,5 +790,7 @@ cudaError_t launch_stream_gemm(const GemmArgs& a, cudaStream_t s)
     p.err = static_cast<unsigned*>(a.ws);
     return launch_stream(p, P, a.bits, a.act, OUT_PLAIN, P.splits, s);
 }
+
+unsigned bounds_take_stream() { return bounds_take_local(); }
 
 }  // namespace wo

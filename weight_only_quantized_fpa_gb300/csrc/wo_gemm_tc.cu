@@ -497,9 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb0 = (((int)blockIdx.x + it * (int)gridDim.x) % splits) * kps;
                 for (int kb = kb0; kb < kb0 + kps; ++kb, ++c) {
                     const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
-                    if (!mbar_wait_bounded(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 2,
+                    // sleeping waits: the MMA thread polling the ring barriers
+                    // slows the arrivals on them (m = 256 / 1024: 4-7 % measured)
+                    if (!mbar_wait_bounded<false, true>(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 2,
                                            kWaitLimitNs) ||
-                        !mbar_wait_bounded(&bars->full2[s2], (c / Cfg::S2) & 1, abort, p.err, 3,
+                        !mbar_wait_bounded<false, true>(&bars->full2[s2], (c / Cfg::S2) & 1, abort, p.err, 3,
                                            kWaitLimitNs)) {
                         ok = false;
                         break;
@@ -1179,10 +1181,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t d = tmem + (uint32_t)(acc * Cfg::COLS);
                     for (int kb = kb0; kb < kb1; ++kb, ++c) {
                         const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
-                        if (!mbar_wait_bounded(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 23,
-                                               kWaitLimitNs) ||
-                            !mbar_wait_bounded(&bars->full2[s2], (c / Cfg::S2) & 1, abort, p.err, 24,
-                                               kWaitLimitNs)) {
+                        // the MMA thread sleeps while it waits: polling the
+                        // operand barrier slows the dequantisation warps'
+                        // arrivals on it (3-10 % measured)
+                        if (!mbar_wait_bounded<false, true>(&bars->fullA[sa], (c / Cfg::SA) & 1, abort, p.err, 23,
+                                                            kWaitLimitNs) ||
+                            !mbar_wait_bounded<false, true>(&bars->full2[s2], (c / Cfg::S2) & 1, abort, p.err, 24,
+                                                            kWaitLimitNs)) {
                             ok = false;
                             break;
                         }

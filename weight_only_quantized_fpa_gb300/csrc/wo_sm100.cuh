@@ -58,6 +58,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait that lets the thread sleep until the phase completes (a
+// suspend-time hint of 1 ms, far above any phase the kernels wait for):
+// for warps that wait long, so that they do not take issue slots from the
+// warps they wait for.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // The same try_wait with acquire semantics at cluster scope: the waiter
 // sees every write that arrivals from other CTAs of the cluster released.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
@@ -77,13 +94,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // (or at once when another thread of the CTA has already given up, seen
 // through *abort).  Returns false when it gave up; the first thread to give
 // up records `code` in *err and raises *abort.  CLUSTER selects the
-// cluster-scope acquire.
-template <bool CLUSTER = false>
+// cluster-scope acquire; SLEEP the try_wait that sleeps until the phase
+// completes (CTA scope).
+template <bool CLUSTER = false, bool SLEEP = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned* err,
                                                   unsigned code, uint64_t limit_ns)
 {
-    auto try_wait = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    static_assert(!(CLUSTER && SLEEP), "the sleeping wait is CTA-scope");
+    auto try_wait = [&]() {
+        return CLUSTER ? mbar_try_wait_cluster(bar, parity)
+                       : SLEEP ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity);
+    };
     if (try_wait())
         return true;
     const uint64_t t0 = globaltimer();

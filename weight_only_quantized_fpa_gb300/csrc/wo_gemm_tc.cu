@@ -1003,7 +1003,10 @@ struct MoeCfg {
     static constexpr int S2 = PLAIN ? 4 : (TWO ? 2 : 3);
     static_assert(SC <= 16 && S2 <= 4 && SA <= 8, "barrier arrays");
     static constexpr int COLS = (TWO ? 2 : 1) * kMoeNT;   // TMEM columns per accumulator
-    static constexpr uint32_t TMEM_COLS = 2 * COLS;
+    // two items in flight, each as two partial accumulators (even and odd k
+    // blocks, issued by two threads)
+    static constexpr uint32_t TMEM_COLS = 4 * COLS;
+    static_assert(TMEM_COLS <= 512, "tensor memory");
     static constexpr int SMEM = SA * A_BYTES + SC * C_BYTES + S2 * B_BYTES;
 };
 
@@ -1093,10 +1096,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->empty2[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&bars->tfull[a], 1);
+            mbar_init(&bars->tfull[a], 2);  // the two MMA issuers
             mbar_init(&bars->tempty[a], 4 * 32);
         }
-        mbar_init(&bars->mma_done, 1);
+        mbar_init(&bars->mma_done, 2);
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -1159,9 +1162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();  // the whole warp reaches the closing CTA barrier together
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3) {
         if (lane == 0) {
-            // ---- MMA issuer: D[channels, tokens] += W[channels, k] . X[tokens, k]^T ----
+            // ---- MMA issuers: D[channels, tokens] += W[channels, k] . X[tokens, k]^T.
+            // Warp 1 takes an item's even k blocks into partial accumulator 0,
+            // warp 3 its odd ones into partial 1: one thread's per-k-block work
+            // (waits, MMA issue, commits) bounded the weight stream, two
+            // threads on two schedulers halve it.  The epilogue adds the two
+            // partials (in that order). ----
+            const int part = warp >> 1;
             constexpr uint32_t idesc = idesc_f16(ACT == ACT_BF16 ? 1u : 0u, 128, kMoeNT);
             int c = 0, t = 0;
             bool ok = true;
@@ -1178,8 +1187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(acc * Cfg::COLS);
+                    const uint32_t d = tmem + (uint32_t)((2 * acc + part) * Cfg::COLS);
+                    bool first = true;
                     for (int kb = kb0; kb < kb1; ++kb, ++c) {
+                        if (((kb - kb0) & 1) != part)
+                            continue;  // the other issuer's k block (c still counts it)
                         const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
                         // the MMA thread sleeps while it waits: polling the
                         // operand barrier slows the dequantisation warps'
@@ -1198,21 +1210,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < BK / 16; ++j) {
                             mma_f16(d, wd + (uint64_t)(2 * j), xd + (uint64_t)(2 * j), idesc,
-                                    (kb > kb0 || j > 0) ? 1u : 0u);
+                                    (!first || j > 0) ? 1u : 0u);
                             if constexpr (TWO)  // second half: operand rows 128..255, 16 KiB on
                                 mma_f16(d + kMoeNT, desc_sw128(w_s + 128 * 128) + (uint64_t)(2 * j),
-                                        xd + (uint64_t)(2 * j), idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+                                        xd + (uint64_t)(2 * j), idesc, (!first || j > 0) ? 1u : 0u);
                         }
+                        first = false;
                         mma_commit(&bars->emptyA[sa]);
                         mma_commit(&bars->empty2[s2]);
                     }
+                    // (an issuer without a k block in the item arrives at once;
+                    // the epilogue then reads only partial 0)
                     if (ok)
                         mma_commit(&bars->tfull[acc]);
                 }
             }
             mma_commit(&bars->mma_done);
-            volatile int never = 0;
-            mbar_wait_bounded(&bars->mma_done, 0, &never, p.err, 28, kWaitLimitNs);
+            if (part == 0) {  // warp 1 frees TMEM after the closing barrier
+                volatile int never = 0;
+                mbar_wait_bounded(&bars->mma_done, 0, &never, p.err, 28, kWaitLimitNs);
+            }
         }
         __syncwarp();
     } else if (PLAIN && warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
@@ -1242,7 +1259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // split ks's fp32 sums, [row][128 channels]: this lane's channel
             float* part = p.partial + ((size_t)nb * p.ksplit + ks) * CH * kMoeNT + q * 32 + lane;
             tc_fence_after();
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Cfg::COLS);
+            // the item's two partial accumulators (even and odd k blocks; a
+            // one-block item has only the first)
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(2 * acc * Cfg::COLS);
+            const bool two_parts = kb1 - kb0 > 1;
 #pragma unroll 1
             for (int cc = 0; cc < kMoeNT / 32; ++cc) {
                 const int tok0 = cc * 32;
@@ -1251,6 +1271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + (uint32_t)(cc * 32), r);
                 tmem_ld_wait();
+                if (two_parts) {
+                    uint32_t r2[32];
+                    tmem_ld_32x32b_x32(tbase + (uint32_t)(Cfg::COLS + cc * 32), r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                }
                 if (p.ksplit == 1) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
@@ -1351,7 +1379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * Cfg::COLS);
+                // the chunk's two partial accumulators (even and odd k blocks)
+                const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(2 * acc * Cfg::COLS);
+                const bool two_parts = p.num_kb > 1;
 #pragma unroll 1
                 for (int cc = 0; cc < kMoeNT / 32; ++cc) {
                     const int tok0 = ch * kMoeNT + cc * 32;
@@ -1362,6 +1392,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (TWO)
                         tmem_ld_32x32b_x32(tbase + (uint32_t)(kMoeNT + cc * 32), u);
                     tmem_ld_wait();
+                    if (two_parts) {
+                        uint32_t r2[32];
+                        tmem_ld_32x32b_x32(tbase + (uint32_t)(Cfg::COLS + cc * 32), r2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+                        if constexpr (TWO) {
+                            tmem_ld_32x32b_x32(tbase + (uint32_t)(Cfg::COLS + kMoeNT + cc * 32), r2);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                u[j] = __float_as_uint(__uint_as_float(u[j]) + __uint_as_float(r2[j]));
+                        }
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         if (tok0 + j < cnt &&  // rows past the expert's range are not its own

@@ -131,7 +131,7 @@ struct TcParams {
 struct Barriers {
     uint64_t fullA[8], emptyA[8];  // A ring (TMA -> MMA)
     uint64_t fullC[16], emptyC[16];  // code ring (TMA -> dequant warps)
-    uint64_t full2[4], empty2[4];  // operand ring (dequant warps -> MMA)
+    uint64_t full2[8], empty2[8];  // operand ring (dequant warps -> MMA)
     uint64_t tfull[2], tempty[2];  // the two TMEM accumulators (MMA <-> epilogue)
     uint64_t mma_done;             // every MMA issued has completed (teardown)
     uint32_t tmem_base;
@@ -993,15 +993,16 @@ struct MoeCfg {
     static constexpr int A_BYTES = kMoeNT * BK * 2;       // 8 KiB of token rows
     static constexpr int C_BYTES = WR * BK;               // packed codes of a k block
     static constexpr int B_BYTES = WR * BK * 2;           // dequantised operand
-    // The codes stream from HBM: their ring holds 128 KiB, the bytes in flight
-    // one SM needs at HBM rate under load; token rows come from L2 and the
-    // operand ring only covers the dequant -> MMA hand-off.  A plain GEMM's
-    // item is short (one k split of one channel block): a deeper operand ring
-    // lets the dequantisation run ahead of the MMAs.
+    // The codes stream from HBM, token rows come from L2, and the operand
+    // ring covers the dequant -> MMA hand-off.  Measured: with two MMA
+    // issuers the operand ring paces the items, so the plain GEMM's rings
+    // take 12 code and 6 operand stages (224 KiB; 3584 x 18944 m = 24: 26.5
+    // -> 24.5 us) and the two-half MoE items 6 and 3 (224 KiB; MoE step
+    // +3 %).
     static constexpr int SA = 4;
-    static constexpr int SC = PLAIN ? 8 : (TWO ? 8 : 16);
-    static constexpr int S2 = PLAIN ? 4 : (TWO ? 2 : 3);
-    static_assert(SC <= 16 && S2 <= 4 && SA <= 8, "barrier arrays");
+    static constexpr int SC = PLAIN ? 12 : (TWO ? 6 : 16);
+    static constexpr int S2 = PLAIN ? 6 : 3;
+    static_assert(SC <= 16 && S2 <= 8 && SA <= 8, "barrier arrays");
     static constexpr int COLS = (TWO ? 2 : 1) * kMoeNT;   // TMEM columns per accumulator
     // two items in flight, each as two partial accumulators (even and odd k
     // blocks, issued by two threads)

@@ -97,10 +97,15 @@ struct TcCfg {
     static constexpr int NT = (BN / 16) * TPN;                   // packed tiles per k block
     static constexpr int R = NT / kDequantWarps;                 // tiles per dequant warp
     static constexpr int PF = 3;                                 // 4-bit scales loaded ahead
-    // accumulators of MS sub-tiles: two (the epilogue of one tile overlaps the
-    // next tile's main loop) when they fit in the 512 TMEM columns, else one
-    static constexpr int NACC = 2 * MS * BN <= 512 ? 2 : 1;
-    static constexpr uint32_t TMEM_COLS = NACC * MS * BN;
+    // 128-row tiles (MS = 1) keep each accumulator as two partial sums, the
+    // even and odd k blocks, issued by two MMA threads (one thread's per-k-
+    // block work otherwise paces these tiles' k loop); the drain adds them.
+    static constexpr int PARTS = MS == 1 ? 2 : 1;
+    // accumulators of MS sub-tiles (x PARTS): two (the epilogue of one tile
+    // overlaps the next tile's main loop) when they fit in the 512 TMEM
+    // columns, else one
+    static constexpr int NACC = 2 * MS * BN * PARTS <= 512 ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = NACC * MS * BN * PARTS;
     static_assert(TMEM_COLS <= 512, "tensor memory");
     static constexpr int SMEM = SA * A_BYTES + SC * C_BYTES + S2 * B_BYTES;  // + barriers
     static_assert(NT % kDequantWarps == 0, "tiles per k block must split evenly");
@@ -315,10 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->empty2[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(&bars->tfull[a], 1);
+            mbar_init(&bars->tfull[a], Cfg::PARTS);  // one commit per MMA issuer
             mbar_init(&bars->tempty[a], helpers ? 4 * 32 + kDequantWarps : 4 * 32);
         }
-        mbar_init(&bars->mma_done, 1);
+        mbar_init(&bars->mma_done, Cfg::PARTS);
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -400,6 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMEM -> C for the chunks x = part, part + nparts, ... of unit `it`'s
     // accumulator (x walks the MS sub-tiles' 32-column chunks), rows of this
     // warp's TMEM lane quadrant; stage_cols(n0) of the tile came first
+    // r += the 32 columns of TMEM at `col` (a second partial accumulator)
+    auto add_partial = [&](uint32_t col, uint32_t (&r)[32]) {
+        uint32_t r2[32];
+        tmem_ld_32x32b_x32(col, r2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+    };
     auto drain = [&](int it, int part, int nparts) {
         const int acc = it % Cfg::NACC, qd = warp & 3;
         int m0, n0;
@@ -418,9 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rs_h = h;
             }
             uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)((acc * MS + h) * BN + cc * 32),
-                               r);
+            const uint32_t col = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)((acc * MS * Cfg::PARTS + h) * BN + cc * 32);
+            tmem_ld_32x32b_x32(col, r);
             tmem_ld_wait();
+            if (Cfg::PARTS == 2 && kps > 1)  // the odd k blocks' partial sums
+                add_partial(col + (uint32_t)BN, r);
             uint32_t sc[16], bi[16];
             gather(cc, sc, bi);
             if (row < p.m) {
@@ -479,10 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();  // the whole warp reaches the closing CTA barrier together
-    } else if (warp == 1) {
+    } else if (warp == 1 || (Cfg::PARTS == 2 && warp == 3)) {
         if (lane == 0) {
-            // ---- MMA issuer ----
+            // ---- MMA issuers: warp 1 (and with two partial sums, warp 3 for the
+            // odd k blocks of each unit, into the columns after the first) ----
             constexpr uint32_t idesc = idesc_f16(OT == ACT_BF16 ? 1u : 0u, BM, BN);
+            const int pt = warp >> 1;  // partial sum of this issuer
             int c = 0;
             bool ok = true;
             for (int it = 0; it < my_tiles && ok; ++it) {
@@ -493,9 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * MS * BN);
+                const uint32_t d = tmem + (uint32_t)((acc * MS * Cfg::PARTS + pt) * BN);
                 const int kb0 = (((int)blockIdx.x + it * (int)gridDim.x) % splits) * kps;
+                bool first = true;
                 for (int kb = kb0; kb < kb0 + kps; ++kb, ++c) {
+                    if (Cfg::PARTS == 2 && ((kb - kb0) & 1) != pt)
+                        continue;  // the other issuer's k block (c still counts it)
                     const int sa = c % Cfg::SA, s2 = c % Cfg::S2;
                     // sleeping waits: the MMA thread polling the ring barriers
                     // slows the arrivals on them (m = 256 / 1024: 4-7 % measured)
@@ -515,18 +536,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < BK / 16; ++j)  // +32 bytes per 16-wide k step
                             mma_f16(d + (uint32_t)(h * BN), ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j),
-                                    idesc, (kb > kb0 || j > 0) ? 1u : 0u);
+                                    idesc, (!first || j > 0) ? 1u : 0u);
                     }
+                    first = false;
                     mma_commit(&bars->emptyA[sa]);
                     mma_commit(&bars->empty2[s2]);
                 }
                 if (ok)
                     mma_commit(&bars->tfull[acc]);
             }
-            // every MMA issued must finish before TMEM is released (also on abort)
+            // every MMA issued must finish before TMEM is released (also on
+            // abort); warp 1 frees it after the closing barrier
             mma_commit(&bars->mma_done);
-            volatile int never = 0;
-            mbar_wait_bounded(&bars->mma_done, 0, &never, p.err, 8, kWaitLimitNs);
+            if (pt == 0) {
+                volatile int never = 0;
+                mbar_wait_bounded(&bars->mma_done, 0, &never, p.err, 8, kWaitLimitNs);
+            }
         }
         __syncwarp();
     } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
@@ -565,10 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (n0 + cc * 32 >= p.n)
                             break;
                         uint32_t r[32];
-                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) +
-                                               (uint32_t)((acc * MS + h) * BN + cc * 32),
-                                           r);
+                        const uint32_t col = tmem + ((uint32_t)(q * 32) << 16) +
+                                             (uint32_t)((acc * MS * Cfg::PARTS + h) * BN + cc * 32);
+                        tmem_ld_32x32b_x32(col, r);
                         tmem_ld_wait();
+                        if (Cfg::PARTS == 2 && kps > 1)
+                            add_partial(col + (uint32_t)BN, r);
                         // [h][cc][row of the sub-tile][32]: a warp writes 4 KiB contiguously
                         float4* dst = reinterpret_cast<float4*>(
                             part + ((size_t)(h * (BN / 32) + cc) * BM + q * 32 + lane) * 32);

@@ -80,6 +80,11 @@ SMALL = [
     (130, 448, 12288, 4, 64, inputs.BF16, True, True),  # 4-bit, k split in 4, ragged
     (200, 384, 3584, 8, -1, inputs.F16, False, True),   # 128 x 128 tiles, k split in 2, ragged
     (130, 320, 4096, 4, 64, inputs.BF16, True, False),  # 4-bit 128 x 128 tiles, k split in 2
+    # one k block: the second MMA issuer of a 128-row tile has nothing to
+    # issue and the drain reads only the first partial sum
+    (70, 192, 64, 8, -1, inputs.F16, False, True),
+    (129, 256, 64, 4, 64, inputs.BF16, True, True),
+    (300, 320, 192, 8, -1, inputs.BF16, False, True),   # 3 k blocks: 2 + 1 between the issuers
 ]
 
 
@@ -248,6 +253,8 @@ MID = [
     (40, 19456, 1024, inputs.F16, True),   # 152 blocks: no split
     (64, 3584, 18944, inputs.BF16, False),  # long k
     (40, 37888, 1024, inputs.F16, True),   # 296 blocks: the m >= 65 kernel
+    (20, 256, 64, inputs.F16, True),       # one k block: one partial accumulator
+    (40, 512, 192, inputs.BF16, False),    # 3 k blocks: 2 + 1 between the MMA issuers
 ]
 
 

@@ -136,37 +136,67 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
 // CPUInt4EmbeddingMethod.embedding: gather the rows of the token ids,
 // dequantise w = (q - offset) * scale (+ zero) in fp32, round once to the
 // activation dtype).  Row r of a 16-row block lives in lanes 4 (r % 8) + t,
-// t = 0..3, of each of its block's tiles.  A warp takes one token and
-// kEmbedTiles consecutive k tiles: lane L reads the 16-byte chunk t = L % 4
-// of tile L / 4, writes the codes of its row into a shared-memory copy of
-// the row segment, and the warp then stores the segment with 16-byte
-// stores (one tile per lane measured faster than two, at more warps of
-// work).  Ids outside [0, vocab) give a zero row.
-constexpr int kEmbedTiles = 8;
-constexpr int kEmbedPerLane = kEmbedTiles / 8;
+// t = 0..3, of each of its block's tiles, and within a lane's words its
+// codes are every other nibble (4-bit: the nibbles of registers R with
+// R & 1 == r / 8) or every other byte pair (8-bit: bytes 2 (r / 8) and
+// 2 (r / 8) + 1 of each word).  A warp takes one token and kEmbedTiles
+// consecutive k tiles: lane L reads the 16-byte chunk t = L % 4 of tiles
+// L / 4 + 8 j, shifts its row's codes into place, dequantises them and
+// writes them as value pairs into a shared-memory copy of the row segment
+// (tiles padded by 16 bytes, so the 32 lanes' pair stores hit 32 banks);
+// the warp then stores the segment with 16-byte stores.  Ids outside
+// [0, vocab) give a zero row (scale and zero 0; the codes are not read).
+constexpr int kEmbedPerLane = 2;
+constexpr int kEmbedTiles = 8 * kEmbedPerLane;
 constexpr int kEmbedWarps = 8;
 
+// (q - off) * s + z with one rounding, q = byte `sel` of x: the byte is
+// placed in the low mantissa bits of 2^23, so the float is 2^23 + q exactly
+// and the subtraction leaves q - off exactly; (q - off) * s is exact in fp32
+// (at most 8 + 11 significant bits), so the fused multiply-add rounds the
+// same sum as the product-then-add of the definition.
+__device__ __forceinline__ float embed_dq(uint32_t x, uint32_t sel, float magic, float s, float z)
+{
+    const float q = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u | sel)) - magic;
+    return fmaf(q, s, z);
+}
+
+// Two values rounded to the activation dtype, `lo` in the low half.
+template <int ACT>
+__device__ __forceinline__ uint32_t embed_pack2(float lo, float hi)
+{
+    uint32_t r;
+    if constexpr (ACT == ACT_BF16)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 template <int BITS, int ACT>
-__global__ void __launch_bounds__(kEmbedWarps * 32)
+__global__ void __launch_bounds__(kEmbedWarps * 32, 6)
     embed_kernel(const int32_t* __restrict__ ids, int T, const uint8_t* __restrict__ B,
                  const uint16_t* __restrict__ scales, const uint16_t* __restrict__ zeros,
                  uint16_t* __restrict__ out, int vocab, int hidden, int G, int group)
 {
     constexpr int KT = Geom<BITS>::KT;
-    constexpr int SEG = kEmbedTiles * KT;  // values of a warp's row segment
-    __shared__ __align__(16) uint16_t seg_sm[kEmbedWarps][SEG];
+    constexpr int TS = KT + 8;                    // a tile's values in shared memory, padded
+    constexpr float kMagic = 8388608.f + (BITS == 8 ? 128.f : 8.f);
+    __shared__ __align__(16) uint16_t seg_sm[kEmbedWarps][kEmbedTiles * TS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint16_t* seg = seg_sm[warp];
     const int ktiles = hidden / KT;
     const int segs = (ktiles + kEmbedTiles - 1) / kEmbedTiles;  // segments per row
     const long long total = (long long)T * segs;
+    const int t4 = lane & 3;
     for (long long w = (long long)blockIdx.x * kEmbedWarps + warp; w < total;
          w += (long long)gridDim.x * kEmbedWarps) {
         const int tok = (int)(w / segs), sg = (int)(w % segs);
         const int id = ids[tok];
         const bool valid = id >= 0 && id < vocab;
         const int r = valid ? id % 16 : 0;
-        const int g = r & 7, t4 = lane & 3;
+        const int g = r & 7;
+        const uint32_t hi_row = (uint32_t)(r >> 3);  // the row is the upper one of its lane pair
         uint4 vj[kEmbedPerLane];
         float scj[kEmbedPerLane], zcj[kEmbedPerLane];
 #pragma unroll
@@ -185,49 +215,43 @@ __global__ void __launch_bounds__(kEmbedWarps * 32)
         }
 #pragma unroll
         for (int j = 0; j < kEmbedPerLane; ++j) {
-          const int tl = (lane >> 2) + 8 * j;
-          const int kt = sg * kEmbedTiles + tl;
-          if (kt < ktiles) {
-            const uint32_t words[4] = {vj[j].x, vj[j].y, vj[j].z, vj[j].w};
-            const float sc = scj[j], zc = zcj[j];
-            auto put = [&](int kk, int q) {
-                float x = 0.f;
-                if (valid) {
-                    x = (float)(q - (BITS == 8 ? 128 : 8)) * sc;
-                    if (zeros)
-                        x += zc;
-                }
-                seg[tl * KT + kk] = from_f32<ACT>(x);
-            };
-            if constexpr (BITS == 8) {
+            const int tl = (lane >> 2) + 8 * j;
+            if (sg * kEmbedTiles + tl < ktiles) {
+                const uint32_t words[4] = {vj[j].x, vj[j].y, vj[j].z, vj[j].w};
+                const float sc = scj[j], zc = zcj[j];
+                uint32_t* dst = reinterpret_cast<uint32_t*>(seg + tl * TS);
+                if constexpr (BITS == 8) {
+                    // word 2s + w: bytes 2h, 2h + 1 are k = 16 s + 2 t + 8 w and k + 1
 #pragma unroll
-                for (int b = 0; b < 16; ++b) {
-                    int row, kk;
-                    u8_coord(b, g, t4, row, kk);
-                    if (row == r)
-                        put(kk, (int)((words[b >> 2] >> (8 * (b & 3))) & 0xFFu));
-                }
-            } else {
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4)
-#pragma unroll
-                    for (int p4 = 0; p4 < 8; ++p4) {
-                        int row, kk;
-                        u4_coord(s4, p4, g, t4, row, kk);
-                        if (row == r)
-                            put(kk, (int)((words[s4] >> (4 * p4)) & 0xFu));
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const uint32_t x = words[wi] >> (16 * hi_row);
+                        const int k0 = 16 * (wi >> 1) + 2 * t4 + 8 * (wi & 1);
+                        dst[k0 / 2] = embed_pack2<ACT>(embed_dq(x, 0, kMagic, sc, zc),
+                                                       embed_dq(x, 1, kMagic, sc, zc));
                     }
+                } else {
+                    // word s, shifted to the row's registers: nibble 0 is k = 16 s + 2 t,
+                    // nibble 4 is k + 1, nibble 2 is k + 8, nibble 6 is k + 9
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint32_t x = (words[s] >> (4 * hi_row)) & 0x0F0F0F0Fu;
+                        const int k0 = 16 * s + 2 * t4;
+                        dst[k0 / 2] = embed_pack2<ACT>(embed_dq(x, 0, kMagic, sc, zc),
+                                                       embed_dq(x, 2, kMagic, sc, zc));
+                        dst[k0 / 2 + 4] = embed_pack2<ACT>(embed_dq(x, 1, kMagic, sc, zc),
+                                                           embed_dq(x, 3, kMagic, sc, zc));
+                    }
+                }
             }
-          }
         }
         __syncwarp();
         // the segment's valid part: 16-byte stores, consecutive lanes
-        const int nvals = (ktiles - sg * kEmbedTiles < kEmbedTiles ? ktiles - sg * kEmbedTiles : kEmbedTiles) * KT;
-        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)tok * hidden + (size_t)sg * SEG);
-        const uint4* src = reinterpret_cast<const uint4*>(seg);
-        for (int i = lane; i < nvals / 8; i += 32)
-            if (in_bounds(tok < T && (size_t)sg * SEG + (size_t)(i + 1) * 8 <= (size_t)hidden, 0x504))
-                dst[i] = src[i];
+        constexpr int CPT = KT / 8;  // 16-byte chunks per tile
+        const int ntiles = ktiles - sg * kEmbedTiles < kEmbedTiles ? ktiles - sg * kEmbedTiles : kEmbedTiles;
+        uint4* dstg = reinterpret_cast<uint4*>(out + (size_t)tok * hidden + (size_t)sg * kEmbedTiles * KT);
+        for (int i = lane; i < ntiles * CPT; i += 32)
+            if (in_bounds(tok < T && (size_t)sg * kEmbedTiles * KT + (size_t)(i + 1) * 8 <= (size_t)hidden, 0x504))
+                dstg[i] = *reinterpret_cast<const uint4*>(seg + (i / CPT) * TS + (i % CPT) * 8);
         __syncwarp();
     }
 }

@@ -207,6 +207,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     constexpr int NV = 2 * MT * 4;  // accumulator values per lane
     // decode rows (m <= 16): split each block's mma chain over even / odd k-steps
     constexpr bool DUAL = !GROUPED && OUT == OUT_PLAIN && MT <= 2;
+    // full stages load all their weight tiles before the first mma step
+    // (decode sizes only: more rows would spill the accumulators)
+    constexpr bool LOADS_FIRST = MT <= 2;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled activation boxes
@@ -418,85 +421,102 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 const int kt_s = c0 + st * TPS;
                 const int ntile = min(TPS, c1 - kt_s);
                 const uint32_t stage = smem_addr(smem + (size_t)s * SG::STAGE);
-                if (active) {
+                // one packed tile of each of the warp's two blocks: mma steps
+                // (and, 4-bit, the group's scale and zero when it ends)
+                auto do_tile = [&](const uint4 v0, const uint4 v1, int tl) {
 #pragma unroll
-                    for (int tl = 0; tl < TPS; ++tl) {
-                      if (tl < ntile) {
-                        const uint4 v0 = lds128(stage + w_lane0 + (uint32_t)(tl * kTileBytes));
-                        const uint4 v1 = lds128(stage + w_lane1 + (uint32_t)(tl * kTileBytes));
+                    for (int ks = 0; ks < KS; ++ks) {
+                        uint32_t a0[4], a1[4];
+                        tile_frag<BITS, ACT>(v0, ks, a0);
+                        tile_frag<BITS, ACT>(v1, ks, a1);
+                        // activation fragments of rows 8j..8j+7 (ldmatrix
+                        // through the 128-byte swizzle; rows past the
+                        // valid count only feed output columns that are
+                        // never stored)
+                        const int kk = tl * KT + 16 * ks;           // k within the stage
+                        const uint32_t box = stage + (uint32_t)((kk >> 6) * SG::A_BOX);
+                        const uint32_t chunk = (uint32_t)((kk & 63) >> 3);
+                        const uint32_t col = (((chunk + a_hi) ^ a_xor) << 4);
+                        uint32_t b[MT][2];
+                        if constexpr (MT == 1) {
+                            ldsm_x2(box + a_row + col, b[0][0], b[0][1]);
+                        } else {
 #pragma unroll
-                        for (int ks = 0; ks < KS; ++ks) {
-                            uint32_t a0[4], a1[4];
-                            tile_frag<BITS, ACT>(v0, ks, a0);
-                            tile_frag<BITS, ACT>(v1, ks, a1);
-                            // activation fragments of rows 8j..8j+7 (ldmatrix
-                            // through the 128-byte swizzle; rows past the
-                            // valid count only feed output columns that are
-                            // never stored)
-                            const int kk = tl * KT + 16 * ks;           // k within the stage
-                            const uint32_t box = stage + (uint32_t)((kk >> 6) * SG::A_BOX);
-                            const uint32_t chunk = (uint32_t)((kk & 63) >> 3);
-                            const uint32_t col = (((chunk + a_hi) ^ a_xor) << 4);
-                            uint32_t b[MT][2];
-                            if constexpr (MT == 1) {
-                                ldsm_x2(box + a_row + col, b[0][0], b[0][1]);
-                            } else {
+                            for (int jp = 0; jp < MT / 2; ++jp)
+                                if (16 * jp < rows)
+                                    ldsm_x4(box + a_row + (uint32_t)(jp * 16 * 128) + col, b[2 * jp][0],
+                                            b[2 * jp][1], b[2 * jp + 1][0], b[2 * jp + 1][1]);
+                        }
 #pragma unroll
-                                for (int jp = 0; jp < MT / 2; ++jp)
-                                    if (16 * jp < rows)
-                                        ldsm_x4(box + a_row + (uint32_t)(jp * 16 * 128) + col, b[2 * jp][0],
-                                                b[2 * jp][1], b[2 * jp + 1][0], b[2 * jp + 1][1]);
-                            }
-#pragma unroll
-                            for (int j = 0; j < MT; ++j) {
-                                if (8 * j < rows) {  // warp-uniform
-                                    if constexpr (GROUPED) {
-                                        mma16816<ACT>(gp[0][j], a0, b[j][0], b[j][1]);
-                                        mma16816<ACT>(gp[1][j], a1, b[j][0], b[j][1]);
-                                        const uint32_t one = ones_x2<ACT>();
-                                        const uint32_t ones[4] = {one, one, one, one};
-                                        mma16816<ACT>(rs[j], ones, b[j][0], b[j][1]);
-                                    } else {
-                                        // DUAL: odd k-steps into a second set (gp), so
-                                        // two independent mma chains per block
-                                        float (&d0)[4] = (DUAL && (ks & 1)) ? gp[0][j] : acc[0][j];
-                                        float (&d1)[4] = (DUAL && (ks & 1)) ? gp[1][j] : acc[1][j];
-                                        mma16816<ACT>(d0, a0, b[j][0], b[j][1]);
-                                        mma16816<ACT>(d1, a1, b[j][0], b[j][1]);
-                                    }
+                        for (int j = 0; j < MT; ++j) {
+                            if (8 * j < rows) {  // warp-uniform
+                                if constexpr (GROUPED) {
+                                    mma16816<ACT>(gp[0][j], a0, b[j][0], b[j][1]);
+                                    mma16816<ACT>(gp[1][j], a1, b[j][0], b[j][1]);
+                                    const uint32_t one = ones_x2<ACT>();
+                                    const uint32_t ones[4] = {one, one, one, one};
+                                    mma16816<ACT>(rs[j], ones, b[j][0], b[j][1]);
+                                } else {
+                                    // DUAL: odd k-steps into a second set (gp), so
+                                    // two independent mma chains per block
+                                    float (&d0)[4] = (DUAL && (ks & 1)) ? gp[0][j] : acc[0][j];
+                                    float (&d1)[4] = (DUAL && (ks & 1)) ? gp[1][j] : acc[1][j];
+                                    mma16816<ACT>(d0, a0, b[j][0], b[j][1]);
+                                    mma16816<ACT>(d1, a1, b[j][0], b[j][1]);
                                 }
                             }
                         }
-                        if constexpr (GROUPED) {
-                            const int ktile = kt_s + tl;
-                            if (((ktile + 1) % p.tiles_per_group == 0) || (ktile + 1 == c1)) {
-                                const int gl = ktile / p.tiles_per_group - g_lo;
+                    }
+                    if constexpr (GROUPED) {
+                        const int ktile = kt_s + tl;
+                        if (((ktile + 1) % p.tiles_per_group == 0) || (ktile + 1 == c1)) {
+                            const int gl = ktile / p.tiles_per_group - g_lo;
 #pragma unroll
-                                for (int r = 0; r < 2; ++r) {
-                                    const int ch = r * 16 + g;
-                                    const float s_lo = to_f32<ACT>(ws_s[ch * p.g_span + gl]);
-                                    const float s_hi = to_f32<ACT>(ws_s[(ch + 8) * p.g_span + gl]);
-                                    const float z_lo = to_f32<ACT>(ws_z[ch * p.g_span + gl]);
-                                    const float z_hi = to_f32<ACT>(ws_z[(ch + 8) * p.g_span + gl]);
+                            for (int r = 0; r < 2; ++r) {
+                                const int ch = r * 16 + g;
+                                const float s_lo = to_f32<ACT>(ws_s[ch * p.g_span + gl]);
+                                const float s_hi = to_f32<ACT>(ws_s[(ch + 8) * p.g_span + gl]);
+                                const float z_lo = to_f32<ACT>(ws_z[ch * p.g_span + gl]);
+                                const float z_hi = to_f32<ACT>(ws_z[(ch + 8) * p.g_span + gl]);
 #pragma unroll
-                                    for (int j = 0; j < MT; ++j) {
-                                        acc[r][j][0] = fmaf(s_lo, gp[r][j][0], fmaf(z_lo, rs[j][0], acc[r][j][0]));
-                                        acc[r][j][1] = fmaf(s_lo, gp[r][j][1], fmaf(z_lo, rs[j][1], acc[r][j][1]));
-                                        acc[r][j][2] = fmaf(s_hi, gp[r][j][2], fmaf(z_hi, rs[j][2], acc[r][j][2]));
-                                        acc[r][j][3] = fmaf(s_hi, gp[r][j][3], fmaf(z_hi, rs[j][3], acc[r][j][3]));
-#pragma unroll
-                                        for (int q = 0; q < 4; ++q)
-                                            gp[r][j][q] = 0.f;
-                                    }
-                                }
-#pragma unroll
-                                for (int j = 0; j < MT; ++j)
+                                for (int j = 0; j < MT; ++j) {
+                                    acc[r][j][0] = fmaf(s_lo, gp[r][j][0], fmaf(z_lo, rs[j][0], acc[r][j][0]));
+                                    acc[r][j][1] = fmaf(s_lo, gp[r][j][1], fmaf(z_lo, rs[j][1], acc[r][j][1]));
+                                    acc[r][j][2] = fmaf(s_hi, gp[r][j][2], fmaf(z_hi, rs[j][2], acc[r][j][2]));
+                                    acc[r][j][3] = fmaf(s_hi, gp[r][j][3], fmaf(z_hi, rs[j][3], acc[r][j][3]));
 #pragma unroll
                                     for (int q = 0; q < 4; ++q)
-                                        rs[j][q] = 0.f;
+                                        gp[r][j][q] = 0.f;
+                                }
                             }
+#pragma unroll
+                            for (int j = 0; j < MT; ++j)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    rs[j][q] = 0.f;
                         }
-                      }
+                    }
+                };
+                if (active) {
+                    if (LOADS_FIRST && ntile == TPS) {
+                        // a full stage: every weight load first, so that the
+                        // conversions and mma steps of one tile overlap the
+                        // loads of the next (one basic block for all tiles)
+                        uint4 v0[TPS], v1[TPS];
+#pragma unroll
+                        for (int tl = 0; tl < TPS; ++tl) {
+                            v0[tl] = lds128(stage + w_lane0 + (uint32_t)(tl * kTileBytes));
+                            v1[tl] = lds128(stage + w_lane1 + (uint32_t)(tl * kTileBytes));
+                        }
+#pragma unroll
+                        for (int tl = 0; tl < TPS; ++tl)
+                            do_tile(v0[tl], v1[tl], tl);
+                    } else {
+#pragma unroll
+                        for (int tl = 0; tl < TPS; ++tl)
+                            if (tl < ntile)
+                                do_tile(lds128(stage + w_lane0 + (uint32_t)(tl * kTileBytes)),
+                                        lds128(stage + w_lane1 + (uint32_t)(tl * kTileBytes)), tl);
                     }
                 }
                 __syncwarp();

@@ -568,9 +568,8 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
     // one packed tile (both blocks) of the stage at offset `stage` of the
     // shared window, tile tl of it
     const uint32_t sbase = smem_addr(smem);  // shared-space address (ldmatrix)
-    auto do_tile = [&](uint32_t stage, uint32_t sbox, int kt0, int tl, int x0) {
-        const uint4 v0 = lds_v4(smem, stage + w_lane0 + (uint32_t)(tl * kTileBytes));
-        const uint4 v1 = lds_v4(smem, stage + w_lane1 + (uint32_t)(tl * kTileBytes));
+    auto do_tile = [&](uint32_t stage, uint32_t sbox, int kt0, int tl, int x0, const uint4 v0,
+                       const uint4 v1) {
         const uint32_t one = ones_x2<ACT>();
         const uint32_t ones[4] = {one, one, one, one};
         if constexpr (ONE) {
@@ -668,10 +667,27 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
             const int kt0 = st * TPS;
             const uint32_t stage = (uint32_t)(s * p.stage_bytes);  // offset in the shared window
             const uint32_t sbox = stage + (uint32_t)(Gm::A_BYTES + kGvWBytes);
-            do_tile(stage, sbox, kt0, 0, x0);
             const bool two = kt0 + 1 < p.ktiles;  // a strip's last stage may hold one tile
-            if (two)
-                do_tile(stage, sbox, kt0, 1, x0);
+            const uint32_t t1 = (uint32_t)kTileBytes;
+            if constexpr (MT == 1) {
+                // both tiles' weight loads before the first tile's work, so
+                // that the second tile's loads overlap it (more rows would
+                // spill: their accumulators take the registers)
+                const uint4 v00 = lds_v4(smem, stage + w_lane0), v01 = lds_v4(smem, stage + w_lane1);
+                uint4 v10 = v00, v11 = v01;
+                if (two) {
+                    v10 = lds_v4(smem, stage + w_lane0 + t1);
+                    v11 = lds_v4(smem, stage + w_lane1 + t1);
+                }
+                do_tile(stage, sbox, kt0, 0, x0, v00, v01);
+                if (two)
+                    do_tile(stage, sbox, kt0, 1, x0, v10, v11);
+            } else {
+                do_tile(stage, sbox, kt0, 0, x0, lds_v4(smem, stage + w_lane0), lds_v4(smem, stage + w_lane1));
+                if (two)
+                    do_tile(stage, sbox, kt0, 1, x0, lds_v4(smem, stage + w_lane0 + t1),
+                            lds_v4(smem, stage + w_lane1 + t1));
+            }
             if constexpr (ONE) {
                 // a segment that ends inside a column window folds it now
                 const int kt_last = kt0 + (two ? 1 : 0);

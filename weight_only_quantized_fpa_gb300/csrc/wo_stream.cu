@@ -210,6 +210,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     // full stages load all their weight tiles before the first mma step
     // (decode sizes only: more rows would spill the accumulators)
     constexpr bool LOADS_FIRST = MT <= 2;
+    // ... and their activation fragments too
+    constexpr bool ACT_FIRST = LOADS_FIRST && MT == 1;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled activation boxes
@@ -421,35 +423,44 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 const int kt_s = c0 + st * TPS;
                 const int ntile = min(TPS, c1 - kt_s);
                 const uint32_t stage = smem_addr(smem + (size_t)s * SG::STAGE);
+                // activation fragments of rows 8j..8j+7 for k step ks of tile
+                // tl (ldmatrix through the 128-byte swizzle; rows past the
+                // valid count only feed output columns that are never stored)
+                auto load_b = [&](int tl, int ks, uint32_t (&b)[MT][2]) {
+                    const int kk = tl * KT + 16 * ks;  // k within the stage
+                    const uint32_t box = stage + (uint32_t)((kk >> 6) * SG::A_BOX);
+                    const uint32_t chunk = (uint32_t)((kk & 63) >> 3);
+                    const uint32_t col = (((chunk + a_hi) ^ a_xor) << 4);
+                    if constexpr (MT == 1) {
+                        ldsm_x2(box + a_row + col, b[0][0], b[0][1]);
+                    } else {
+#pragma unroll
+                        for (int jp = 0; jp < MT / 2; ++jp)
+                            if (jp == 0 || 16 * jp < rows)  // rows >= 1
+                                ldsm_x4(box + a_row + (uint32_t)(jp * 16 * 128) + col, b[2 * jp][0],
+                                        b[2 * jp][1], b[2 * jp + 1][0], b[2 * jp + 1][1]);
+                    }
+                };
                 // one packed tile of each of the warp's two blocks: mma steps
-                // (and, 4-bit, the group's scale and zero when it ends)
-                auto do_tile = [&](const uint4 v0, const uint4 v1, int tl) {
+                // (and, 4-bit, the group's scale and zero when it ends);
+                // bpre: the tile's activation fragments, loaded earlier, or null
+                auto do_tile = [&](const uint4 v0, const uint4 v1, int tl, const uint32_t (*bpre)[MT][2]) {
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
                         uint32_t a0[4], a1[4];
                         tile_frag<BITS, ACT>(v0, ks, a0);
                         tile_frag<BITS, ACT>(v1, ks, a1);
-                        // activation fragments of rows 8j..8j+7 (ldmatrix
-                        // through the 128-byte swizzle; rows past the
-                        // valid count only feed output columns that are
-                        // never stored)
-                        const int kk = tl * KT + 16 * ks;           // k within the stage
-                        const uint32_t box = stage + (uint32_t)((kk >> 6) * SG::A_BOX);
-                        const uint32_t chunk = (uint32_t)((kk & 63) >> 3);
-                        const uint32_t col = (((chunk + a_hi) ^ a_xor) << 4);
                         uint32_t b[MT][2];
-                        if constexpr (MT == 1) {
-                            ldsm_x2(box + a_row + col, b[0][0], b[0][1]);
-                        } else {
+                        if (bpre) {
 #pragma unroll
-                            for (int jp = 0; jp < MT / 2; ++jp)
-                                if (16 * jp < rows)
-                                    ldsm_x4(box + a_row + (uint32_t)(jp * 16 * 128) + col, b[2 * jp][0],
-                                            b[2 * jp][1], b[2 * jp + 1][0], b[2 * jp + 1][1]);
+                            for (int j = 0; j < MT; ++j)
+                                b[j][0] = bpre[ks][j][0], b[j][1] = bpre[ks][j][1];
+                        } else {
+                            load_b(tl, ks, b);
                         }
 #pragma unroll
                         for (int j = 0; j < MT; ++j) {
-                            if (8 * j < rows) {  // warp-uniform
+                            if (j == 0 || 8 * j < rows) {  // warp-uniform; rows >= 1
                                 if constexpr (GROUPED) {
                                     mma16816<ACT>(gp[0][j], a0, b[j][0], b[j][1]);
                                     mma16816<ACT>(gp[1][j], a1, b[j][0], b[j][1]);
@@ -508,15 +519,27 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                             v0[tl] = lds128(stage + w_lane0 + (uint32_t)(tl * kTileBytes));
                             v1[tl] = lds128(stage + w_lane1 + (uint32_t)(tl * kTileBytes));
                         }
+                        if constexpr (ACT_FIRST) {
+                            uint32_t bb[TPS][KS][MT][2];
 #pragma unroll
-                        for (int tl = 0; tl < TPS; ++tl)
-                            do_tile(v0[tl], v1[tl], tl);
+                            for (int tl = 0; tl < TPS; ++tl)
+#pragma unroll
+                                for (int ks = 0; ks < KS; ++ks)
+                                    load_b(tl, ks, bb[tl][ks]);
+#pragma unroll
+                            for (int tl = 0; tl < TPS; ++tl)
+                                do_tile(v0[tl], v1[tl], tl, bb[tl]);
+                        } else {
+#pragma unroll
+                            for (int tl = 0; tl < TPS; ++tl)
+                                do_tile(v0[tl], v1[tl], tl, nullptr);
+                        }
                     } else {
 #pragma unroll
                         for (int tl = 0; tl < TPS; ++tl)
                             if (tl < ntile)
                                 do_tile(lds128(stage + w_lane0 + (uint32_t)(tl * kTileBytes)),
-                                        lds128(stage + w_lane1 + (uint32_t)(tl * kTileBytes)), tl);
+                                        lds128(stage + w_lane1 + (uint32_t)(tl * kTileBytes)), tl, nullptr);
                     }
                 }
                 __syncwarp();

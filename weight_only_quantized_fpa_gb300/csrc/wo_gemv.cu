@@ -71,6 +71,7 @@ using namespace sm100;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr int kGvStageK = 128;                      // codes of k per stage
 constexpr int kGvTps = kGvStageK / 64;              // packed 4-bit tiles per block per stage
+static_assert(kGvTps % 2 == 0, "a stage starts at an even k tile");
 constexpr int kGvNw = 8;                            // consumer warps
 constexpr int kGvCh = kGvNw * 32;                   // channels per strip
 constexpr int kSzGroups = 8;                        // groups per scale box (16 bytes of 16-bit values)
@@ -593,8 +594,9 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
                 uint32_t a0[4], a1[4];
                 frag_u4_biased<ACT>(w0, a0);
                 frag_u4_biased<ACT>(w1, a1);
-                const int e = kt & 1;  // warp-uniform
-                if (e == 0) {
+                // kt0 is a multiple of the (even) tiles per stage, so kt and tl
+                // have the same parity: a compile-time choice after unrolling
+                if ((tl & 1) == 0) {
                     mma_acc<ACT>(wp[0][0], a0, b0, b1);
                     mma_acc<ACT>(wp[0][1], a1, b0, b1);
                     mma_acc<ACT>(wr[0], ones, b0, b1);
@@ -604,7 +606,7 @@ __global__ void __launch_bounds__((kGvNw + 1) * 32, kGvCtasPerSm)
                     mma_acc<ACT>(wr[1], ones, b0, b1);
                 }
             }
-            if ((kt & 7) == 7)
+            if ((tl & 1) && (kt & 7) == 7)  // only an odd tile ends a window of 8
                 fold_window(sbox, kt, x0);
         } else {
             float gp[2][MT][4], rs[MT][4];

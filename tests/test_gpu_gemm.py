@@ -101,9 +101,11 @@ def test_small_shapes(wo, m, n, k, bits, group, act, zeros, bias):
 # 256 channels (the last one partly past n), stages of 128 codes (a half
 # stage at the end when k % 128 == 64), strips cut into pieces across CTAs
 # when there are few of them (summed through the workspace by the last
-# piece to arrive).  The automatic choice sends many of these shapes to the
-# cluster kernel; test_decode_shapes_on_the_persistent_kernel runs them all
-# again with the persistent kernel forced.
+# piece to arrive).  The automatic choice sends these shapes to the cluster
+# kernel (it takes the persistent one only for grids wider than a resident
+# wave, like the full-size lm_head of the W4 workload);
+# test_decode_shapes_on_the_persistent_kernel runs them all again with the
+# persistent kernel forced.
 PERSISTENT = [
     # m, n, k, bits, group, act, zeros, bias
     (8, 320, 2048, 4, 64, inputs.F16, True, True),       # 8 rows: one activation row block
@@ -117,7 +119,7 @@ PERSISTENT = [
     (3, 128, 576, 4, -1, inputs.BF16, True, True),       # per channel, k % 128 == 64
     (1, 64, 11776, 4, 64, inputs.BF16, True, False),     # one strip over many CTAs
     (2, 4160, 192, 4, -1, inputs.F16, True, True),       # many strips, 2 stages each
-    (4, 320, 16384, 4, 64, inputs.BF16, True, True),     # persistent by the automatic choice
+    (4, 320, 16384, 4, 64, inputs.BF16, True, True),     # long k, few channels
     (7, 2368, 3136, 4, 64, inputs.BF16, True, True),     # k / 64 not a multiple of 8: cluster kernel
 ]
 

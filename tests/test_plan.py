@@ -3,12 +3,18 @@ counterpart of acext 1.2.1's getChosenConfig).  Pure host code: with no GPU
 visible the library plans for 152 SMs, GB300's count.  The GPU parity tests
 pick their small shapes to cover every tile configuration; these tests keep
 that true."""
+import json
+import os
+import subprocess
+import sys
+
 import pytest
 
 import weight_only_quantized_fpa_gb300 as wo
 from weight_only_quantized_fpa_gb300 import build as wo_build
 
 SMS = 152
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,16 +60,19 @@ def test_kernel_choice_by_m(bits, group):
 
 @pytest.mark.parametrize("n,k,group,persistent", [
     (131072, 2048, 64, True),   # the cluster kernel would need 512 CTAs: more than one wave
-    (2048, 13312, 64, True),    # 128 cluster CTAs of 106 KB each: SMs left idle
-    (2048, 13312, 128, True),
     (131072, 2048, -1, True),
+    (81920, 2048, 64, True),    # 320 cluster CTAs: just over one wave
+    (65536, 2048, 64, False),   # 256 cluster CTAs: one wave
+    (1024, 13312, 64, False),   # long k, few channels: 64 cluster CTAs still win
+    (2048, 13312, 128, False),
+    (320, 16384, 64, False),
     (13312, 2048, 64, False),   # 208 CTAs in one wave
     (2048, 2048, 64, False),    # 2 MB of weights: the cluster kernel's shorter critical path
     (3072, 2048, -1, False)])
 def test_4bit_decode_kernel_choice(n, k, group, persistent):
     # 4-bit decode sizes take the persistent kernel where the cluster-split
-    # one cannot keep the GPU busy; 8-bit decode always stays on the latter,
-    # and so does m = 17
+    # one would need more than one resident wave; 8-bit decode always stays
+    # on the latter, and so does m = 17
     for m in (1, 16):
         want = "stream_persistent" if persistent else "stream"
         assert wo.gemm_plan(m, n, k, 4, group)["kernel"] == want, (m, n, k)
@@ -85,16 +94,34 @@ def test_stream_plans_fill_one_resident_wave(m, n, k, bits, group):
     assert p["stages"] >= 1 and p["workspace_bytes"] == 256
 
 
-@pytest.mark.parametrize("m,n,k,bits,group", [(1, 2048, 13312, 4, 64), (4, 1024, 18944, 4, 64),
-                                              (16, 131072, 2048, 4, 128), (1, 131072, 2048, 4, 64),
-                                              (9, 256, 16384, 4, 128), (3, 320, 16384, 4, -1),
-                                              (2, 64, 65536, 4, 64)])
-def test_persistent_plans_split_the_weights_evenly(m, n, k, bits, group):
+PERSISTENT_SHAPES = [(1, 1024, 13312, 4, 64), (4, 1024, 18944, 4, 64), (16, 131072, 2048, 4, 128),
+                     (1, 131072, 2048, 4, 64), (9, 256, 16384, 4, 128), (3, 320, 16384, 4, -1),
+                     (2, 64, 65536, 4, 64)]
+
+
+@pytest.fixture(scope="module")
+def persistent_plans(lib):
+    # the persistent kernel's plans, also for shapes the automatic choice
+    # gives the cluster kernel: WO_DECODE_KERNEL (read once per process)
+    # forces it, in a child process
+    code = ("import json, sys\n"
+            "import weight_only_quantized_fpa_gb300 as wo\n"
+            "wo.load_library()\n"
+            "print(json.dumps([wo.gemm_plan(m, n, k, b, g, wo.WO_BF16) for m, n, k, b, g in json.loads(sys.argv[1])]))\n")
+    r = subprocess.run([sys.executable, "-c", code, json.dumps(PERSISTENT_SHAPES)], cwd=ROOT,
+                       env=dict(os.environ, WO_DECODE_KERNEL="persistent"), capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return dict(zip(PERSISTENT_SHAPES, json.loads(r.stdout.strip().splitlines()[-1])))
+
+
+@pytest.mark.parametrize("m,n,k,bits,group", PERSISTENT_SHAPES)
+def test_persistent_plans_split_the_weights_evenly(persistent_plans, m, n, k, bits, group):
     # decode sizes: strips of 256 channels by stages of 128 codes, the
     # strip-major units divided evenly over two CTAs per SM (fewer when there
     # are fewer units); pieces of a strip that several CTAs share sum through
     # the workspace after the header and counter area
-    p = wo.gemm_plan(m, n, k, bits, group, wo.WO_BF16)
+    p = persistent_plans[(m, n, k, bits, group)]
     assert p["kernel"] == "stream_persistent" and p["tile_m"] == m and p["tile_n"] == 256
     units = -(-n // 256) * -(-k // 128)
     assert p["ctas"] == min(units, 2 * SMS)

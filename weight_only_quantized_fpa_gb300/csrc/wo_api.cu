@@ -117,11 +117,11 @@ bool use_tc(int m, int n, int k, int group_size, int bits)
 
 // Below the tensor-core sizes, 4-bit weights at decode-sized m (1..16) run
 // the persistent kernel (wo_gemv.cu) where the cluster-split streaming
-// kernel (wo_stream.cu) cannot keep the GPU busy: when its grid needs more
-// than one resident wave (2 CTAs per SM), or fills fewer CTAs than there
-// are SMs while each streams 64 KB or more (long k, few channels).  Smaller
-// problems keep the cluster kernel, whose shorter critical path measured
-// faster at 2-16 MB of weights.  The environment variable WO_DECODE_KERNEL
+// kernel (wo_stream.cu) would need more than one resident wave of CTAs (2
+// per SM): the wide lm_head-like shapes (131072 x 2048: 39 against 68 us at
+// m = 1).  Everything else keeps the cluster kernel, long k with few
+// channels included (320 x 16384: 13.5 against 27.7 us at m = 1; 1024 x
+// 13312: 13.9 against 20.3 us; 2048 x 13312: 14.4 against 15.3 us).  The environment variable WO_DECODE_KERNEL
 // overrides the choice for measurements and tests: "stream" forces the
 // cluster kernel, "persistent" the persistent one wherever it applies (the
 // two give results within tolerance of each other, not bit-identical ones).
@@ -150,8 +150,7 @@ bool use_gemv_shape(int m, int n, int k, int group, int bits)
     if (!c.valid)
         return true;
     const long long ctas = (long long)c.grid_x * c.splits;
-    const double bytes_per_cta = (double)n * k * bits / 8.0 / (double)ctas;
-    return ctas > 2LL * num_sms() || (ctas < num_sms() && bytes_per_cta >= 65536.0);
+    return ctas > 2LL * num_sms();
 }
 
 bool use_gemv(const GemmArgs& a)

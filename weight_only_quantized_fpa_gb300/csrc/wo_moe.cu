@@ -210,21 +210,59 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ A, const int* __res
         dst[i] = src[i];
 }
 
+// A CTA per token; the token's rows and weights are read once into
+// registers (topk <= kMaxTopk), and a thread takes 8 channels at a time: two
+// 16-byte loads per row, one 16-byte store (hidden % 64 == 0, out 16-byte
+// aligned).  Per channel the sum is the same chain of fused multiply-adds
+// over j in ascending order.
+constexpr int kMaxTopk = 8;
+
 template <int ACT>
-__global__ void combine_kernel(const float* __restrict__ Y, const int* __restrict__ pos,
-                               const float* __restrict__ wts, uint16_t* __restrict__ out,
-                               int hidden, int topk, int P)
+__global__ void __launch_bounds__(256)
+    combine_kernel(const float* __restrict__ Y, const int* __restrict__ pos,
+                   const float* __restrict__ wts, uint16_t* __restrict__ out, int hidden, int topk,
+                   int P)
 {
     const int tok = blockIdx.x;
-    for (int c = threadIdx.x; c < hidden; c += blockDim.x) {
-        float v = 0.f;
-        for (int j = 0; j < topk; ++j) {
+    int pj[kMaxTopk];
+    float wj[kMaxTopk];
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) {
+        pj[j] = -1;  // j >= topk, or a position outside the rows: skipped
+        wj[j] = 0.f;
+        if (j < topk) {
             const int p = pos[(size_t)tok * topk + j];
-            if (!in_bounds(p >= 0 && p < P, 0x704))
-                continue;
-            v = fmaf(wts[(size_t)tok * topk + j], Y[(size_t)p * hidden + c], v);
+            if (in_bounds(p >= 0 && p < P, 0x704)) {
+                pj[j] = p;
+                wj[j] = wts[(size_t)tok * topk + j];
+            }
         }
-        out[(size_t)tok * hidden + c] = from_f32<ACT>(v);
+    }
+    for (int c = threadIdx.x * 8; c < hidden; c += blockDim.x * 8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j) {
+            if (pj[j] < 0)
+                continue;
+            const float4* y = reinterpret_cast<const float4*>(Y + (size_t)pj[j] * hidden + c);
+            const float4 a = y[0], b = y[1];
+            v[0] = fmaf(wj[j], a.x, v[0]);
+            v[1] = fmaf(wj[j], a.y, v[1]);
+            v[2] = fmaf(wj[j], a.z, v[2]);
+            v[3] = fmaf(wj[j], a.w, v[3]);
+            v[4] = fmaf(wj[j], b.x, v[4]);
+            v[5] = fmaf(wj[j], b.y, v[5]);
+            v[6] = fmaf(wj[j], b.z, v[6]);
+            v[7] = fmaf(wj[j], b.w, v[7]);
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = (uint32_t)from_f32<ACT>(v[2 * i]) | ((uint32_t)from_f32<ACT>(v[2 * i + 1]) << 16);
+        *reinterpret_cast<uint4*>(out + (size_t)tok * hidden + c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -356,7 +394,7 @@ wo_status wo_moe_ffn(const void* A, const float* gating_logits, const uint8_t* f
 {
     if (T < 0 || hidden <= 0 || inter <= 0 || hidden % 64 != 0 || inter % 64 != 0)
         return WO_ERR_INVALID_ARG;
-    if (experts < 1 || experts > 1024 || topk < 1 || topk > experts || topk > 8)
+    if (experts < 1 || experts > 1024 || topk < 1 || topk > experts || topk > kMaxTopk)
         return WO_ERR_INVALID_ARG;
     if (act_dtype != WO_F16 && act_dtype != WO_BF16)
         return WO_ERR_INVALID_ARG;

@@ -56,6 +56,9 @@ def test_w4_tiny(wo):
 SMALL = [
     # m, n, k, bits, group, act, zeros, bias
     (1, 64, 64, 8, -1, inputs.F16, False, True),
+    (12, 192, 320, 8, -1, inputs.F16, False, True),     # 9-16 rows, a part stage (2 of 4 tiles)
+    (16, 320, 576, 8, -1, inputs.BF16, False, False),   # 16 rows, bf16, a part stage
+    (7, 128, 1088, 8, -1, inputs.BF16, False, True),    # 1-8 rows, bf16, k split with a part stage
     (3, 192, 320, 8, -1, inputs.F16, False, True),
     (17, 256, 512, 8, -1, inputs.BF16, False, False),
     (5, 320, 1024, 4, 64, inputs.BF16, True, True),

@@ -110,8 +110,9 @@ WO_API size_t wo_workspace_size(int m, int n, int k, int group_size, int bits);
  *   bits 4: group_size 64 or 128 (a multiple of 64 dividing k), or -1/k.
  * Requires n % 64 == 0, k % 64 == 0 and k > 0; m == 0 or n == 0 is a no-op.
  * The kernel is chosen by m: for 4-bit weights at decode-sized m (1..16)
- * a persistent weight-streaming kernel where the cluster-split one cannot
- * fill the GPU (group-wise weights also need 16-byte aligned scales and
+ * a persistent weight-streaming kernel where the cluster-split one would
+ * need more than one resident wave of CTAs, as for a wide lm_head
+ * (group-wise weights also need 16-byte aligned scales and
  * zeros and k / group_size a multiple of 8); for 8-bit weights at 17..64
  * rows (n % 128 == 0) a tcgen05 kernel with the weights as the MMA's rows
  * while n / 128 is at most the SM count, the m >= 65 tensor-core kernel for
